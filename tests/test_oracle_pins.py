@@ -1,0 +1,338 @@
+"""Pins for the CPU oracle: each check compares it with something other than itself
+(hand-worked values, closed forms, library routines, an independent torch forward,
+brute force).  All CPU, no GPU."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import lopa_oracle as O
+OL = O
+from diffusion_lookahead_decoding_gb300 import synth
+from tests.independent_forward import block_layout, rope_complex, torch_forward
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+# A micro model with grouped-query attention (2 query heads per KV head).
+MICRO = synth.ModelShape(2, 64, 4, 2, 16, 128, 97, 10000.0)
+
+
+@pytest.fixture(scope="module")
+def micro_w():
+    return synth.make_weights(MICRO, seed=3, threads=1)
+
+
+# ----------------------------------------------------------------------------- formats
+def test_bf16_round_hand_cases():
+    cases = {
+        1.0: 1.0,
+        1 + 2 ** -8: 1.0,                 # exact midpoint, ties to even (fraction 0)
+        1 + 3 * 2 ** -8: 1 + 2 ** -6,     # midpoint between 1+2^-7 and 1+2^-6 -> even
+        1 + 2 ** -8 + 2 ** -30: 1 + 2 ** -7,  # just above the midpoint rounds up
+        -(1 + 2 ** -8 + 2 ** -30): -(1 + 2 ** -7),
+        3.0e38: (1 + 98 / 128) * 2.0 ** 127,  # 3e38/2^127 = 1.7632..; 0.7632*128 = 97.69 -> 98
+        3.4e38: math.inf,                 # beyond the largest finite bf16 + half ulp
+        2.0 ** -130: 2.0 ** -130,         # subnormal grid point
+        2.0 ** -134: 0.0,                 # half of the smallest subnormal -> even (0)
+        3 * 2.0 ** -134: 2.0 ** -132,     # 1.5 * 2^-133 -> 2 * 2^-133
+        0.0: 0.0,
+    }
+    xs = np.array(list(cases.keys()))
+    got = O.bf16_round(xs)
+    for x, g in zip(cases, got):
+        assert g == cases[x], (x, g, cases[x])
+
+
+def test_bf16_round_matches_torch_on_float32_inputs():
+    # torch rounds binary32 -> bf16 directly; on binary32 inputs both must agree.
+    g = torch.Generator().manual_seed(0)
+    x = torch.cat([torch.randn(200000, generator=g) * s for s in (1e-3, 1.0, 1e3, 1e30)])
+    x = torch.cat([x, torch.tensor([2.0 ** -127, -(2.0 ** -140), 1.5 * 2 ** -133])])
+    ref = x.to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.bf16_round(x.to(torch.float64).numpy())
+    np.testing.assert_array_equal(got, ref)
+
+
+# ----------------------------------------------------------------- transformer pieces
+def test_rmsnorm_closed_form():
+    d = 10
+    for c in (3.0, -0.02, 1e-4):
+        g = np.arange(1, d + 1, dtype=np.float64)
+        y = O.rmsnorm(np.full(d, c), g, 1e-6)
+        np.testing.assert_allclose(y, c / math.sqrt(c * c + 1e-6) * g, rtol=1e-14)
+    # scale invariance without eps
+    x = np.random.default_rng(0).standard_normal((3, d))
+    np.testing.assert_allclose(O.rmsnorm(7.5 * x, 1.0, 0.0), O.rmsnorm(x, 1.0, 0.0), rtol=1e-13)
+
+
+def test_rope_equals_complex_rotation_and_is_relative():
+    rng = np.random.default_rng(1)
+    dh, base = 16, 10000.0
+    x = rng.standard_normal((5, 3, dh))
+    pos = np.array([0, 1, 7, 100, 4095])
+    ours = O.rope(x, pos, base)
+    ref = rope_complex(torch.from_numpy(x), torch.from_numpy(pos), base).numpy()
+    np.testing.assert_allclose(ours, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(O.rope(x[:1], np.array([0]), base), x[:1])  # identity at 0
+    np.testing.assert_allclose(np.linalg.norm(ours, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-12)
+    # <rope(q, m), rope(k, n)> depends only on m - n
+    q, k = rng.standard_normal((1, 1, dh)), rng.standard_normal((1, 1, dh))
+    dots = [np.sum(O.rope(q, np.array([m + s]), base) * O.rope(k, np.array([n + s]), base))
+            for (m, n) in [(5, 2)] for s in (0, 13, 999)]
+    np.testing.assert_allclose(dots, dots[0], rtol=1e-10)
+    # first pair rotates by exactly pos radians (theta_0 = 1)
+    e = np.zeros((1, 1, dh)); e[..., 0] = 1.0
+    r = O.rope(e, np.array([2]), base)
+    assert abs(r[0, 0, 0] - math.cos(2)) < 1e-15 and abs(r[0, 0, dh // 2] - math.sin(2)) < 1e-15
+
+
+def test_silu_matches_logistic():
+    from scipy.special import expit
+    x = np.linspace(-30, 30, 101)
+    np.testing.assert_allclose(O.silu(x), x * expit(x), rtol=1e-13, atol=1e-300)
+
+
+def test_logit_summary_special_cases():
+    V = 11
+    am, mp, p2 = O.logit_summary(np.zeros((1, V)), mask_id=0)
+    assert am[0] == 1 and abs(mp[0] - 1.0 / (V - 1)) < 1e-15  # [MASK] excluded, ties -> lowest
+    z = np.full(V, -1e9); z[0] = 50.0; z[3] = 2.0; z[7] = 0.5
+    am, mp, p2 = O.logit_summary(z, mask_id=0)
+    assert am == 3
+    assert abs(mp - 1.0 / (1.0 + math.exp(-1.5))) < 1e-15       # two-way softmax closed form
+    assert abs(p2 - math.exp(-1.5) / (1.0 + math.exp(-1.5))) < 1e-15
+    z = np.array([0.0, 5.0, 5.0, 1.0])
+    assert O.logit_summary(z, 0)[0] == 1
+    from scipy.special import softmax
+    z = np.random.default_rng(2).standard_normal((4, 50)) * 20
+    am, mp, _ = O.logit_summary(z, 0)
+    zz = z.copy(); zz[:, 0] = -np.inf
+    sm = softmax(zz, axis=-1)
+    np.testing.assert_array_equal(am, sm.argmax(-1))
+    np.testing.assert_allclose(mp, sm.max(-1), rtol=1e-13)
+
+
+# --------------------------------------------------------------------------- forward
+def _oracle_branch_pass(w, shape, act, prompt, branches):
+    m = O.OracleModel(shape, w, act=act)
+    cache = O.prefill(m, prompt, len(prompt) + branches.shape[1])
+    return m, cache, O.forward(m, cache, len(prompt), branches, want_logits=True)
+
+
+@pytest.mark.parametrize("act", ["fp64", "bf16"])
+def test_forward_matches_independent_torch_forward(micro_w, act):
+    """Oracle (cache + per-branch loops) vs torch (one masked whole-sequence pass)."""
+    rng = np.random.default_rng(4)
+    B, nb, Pn = 6, 3, 9
+    prompt = rng.integers(1, MICRO.vocab, Pn)
+    branches = rng.integers(0, MICRO.vocab, (nb, B))
+    branches[rng.random((nb, B)) < 0.5] = MICRO.mask_id
+    _, cache, out = _oracle_branch_pass(micro_w, MICRO, act, prompt, branches)
+    positions, visible = block_layout(Pn, 0, B, nb)
+    toks = np.concatenate([prompt, branches.reshape(-1)])
+    z, x, ks, _ = torch_forward(micro_w, MICRO, toks, positions, visible,
+                                act="bf16" if act == "bf16" else None)
+    z = z[Pn:].numpy().reshape(nb, B, -1)
+    x = x[Pn:].numpy().reshape(nb, B, -1)
+    tol = 1e-10 if act == "fp64" else 1e-6
+    np.testing.assert_allclose(out.logits[..., 1:], z[..., 1:], rtol=tol, atol=tol)
+    np.testing.assert_allclose(out.x_final, x, rtol=tol, atol=tol)
+    np.testing.assert_allclose(cache.k[1][:Pn], ks[1][:Pn].numpy(), rtol=tol, atol=tol)
+    zz = z.copy(); zz[..., 0] = -np.inf
+    np.testing.assert_array_equal(out.am, zz.argmax(-1))
+
+
+def test_isolation_batched_equals_separate(micro_w):
+    rng = np.random.default_rng(5)
+    B, nb = 8, 4
+    prompt = rng.integers(1, MICRO.vocab, 12)
+    branches = rng.integers(1, MICRO.vocab, (nb, B))
+    branches[rng.random((nb, B)) < 0.6] = MICRO.mask_id
+    m, cache, out = _oracle_branch_pass(micro_w, MICRO, "fp64", prompt, branches)
+    for b in range(nb):
+        one = O.forward(m, cache, len(prompt), branches[b:b + 1], want_logits=True)
+        np.testing.assert_allclose(one.logits[0], out.logits[b], rtol=1e-12, atol=1e-12)
+        np.testing.assert_array_equal(one.am[0], out.am[b])
+
+
+def test_forward_without_attention_and_mlp_is_embedding_readout(micro_w):
+    """With Wo = Wd = 0 the residual stream is the embedding: logits are
+    scale * rmsnorm(E[tok]) @ Wlm^T (a closed form that skips every layer)."""
+    w = dict(micro_w)
+    for l in range(MICRO.n_layers):
+        w[f"wo.{l}"] = torch.zeros_like(w[f"wo.{l}"])
+        w[f"wd.{l}"] = torch.zeros_like(w[f"wd.{l}"])
+    tok = np.array([[5, 0, 17, 96]])
+    m = O.OracleModel(MICRO, w, act="fp64")
+    out = O.forward(m, O.KVCache.empty(MICRO, 8), 0, tok, want_logits=True)
+    E = w["embed"].double().numpy()[tok[0]]
+    h = E / np.sqrt((E ** 2).mean(-1, keepdims=True) + MICRO.rms_eps)
+    z = 20.0 * h @ w["lm_head"].double().numpy().T
+    np.testing.assert_allclose(out.logits[0], z, rtol=1e-12)
+
+
+# ---------------------------------------------------------------------- decision rules
+def _golden_cases():
+    with open(os.path.join(GOLDEN, "decision_cases.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: c["name"])
+def test_decision_rules_hand_worked(case):
+    mask = 0
+    anchor, S = O.anchor_fill(np.array(case["tok"]), case["am"], case["mp"], case["tau"], mask)
+    assert S == case["expect_filled"]
+    C = O.lookahead_candidates(anchor, case["mp"], case["k"], mask)
+    assert C == case["expect_candidates"]
+    br = O.build_branches(anchor, case["am"], C)
+    assert br.tolist() == case["expect_branches"]
+    conf = [O.branch_confidence(br[b], case["verify_mp"][b], mask) for b in range(len(br))]
+    np.testing.assert_allclose(conf, case["expect_conf"], rtol=0, atol=1e-15)
+    assert O.select_winner(conf) == case["expect_winner"]
+
+
+def test_candidates_match_counting_definition():
+    """Candidate set = remaining positions with fewer than k others ranked above them
+    (above = strictly more confident, or equally confident and lower position)."""
+    rng = np.random.default_rng(6)
+    for _ in range(300):
+        B = int(rng.integers(1, 12))
+        tok = np.where(rng.random(B) < 0.7, 0, 5)
+        mp = np.round(rng.random(B), 1)  # coarse values force ties
+        am = rng.integers(1, 9, B)
+        k = int(rng.integers(0, 6))
+        anchor, S = O.anchor_fill(tok, am, mp, 0.9, 0)
+        masked = [i for i in range(B) if tok[i] == 0]
+        if masked:
+            assert S, "at least one fill per step"
+        for i in masked:
+            assert (i in S) == (mp[i] >= 0.9) or (len(S) == 1 and all(mp[j] < 0.9 for j in masked))
+        R = [i for i in range(B) if anchor[i] == 0]
+        above = {i: sum(1 for j in R if mp[j] > mp[i] or (mp[j] == mp[i] and j < i)) for i in R}
+        want = sorted((i for i in R if above[i] < k), key=lambda i: above[i])
+        assert O.lookahead_candidates(anchor, mp, k, 0) == want
+
+
+# ------------------------------------------------------------------ whole-method pins
+def _threshold_decode(m, prompt, block, tau, gen_len):
+    """Plain confidence-driven threshold decoding, written independently of
+    lopa_step: fill all masked positions with confidence >= tau (at least the single
+    most confident one), one forward per fill round."""
+    mask = m.shape.mask_id
+    cache = O.prefill(m, prompt, len(prompt) + gen_len)
+    P, out, fw = len(prompt), [], 0
+    for _ in range(gen_len // block):
+        tok = [mask] * block
+        res = O.forward(m, cache, P, np.array([tok])); fw += 1
+        while mask in tok:
+            masked = [i for i, t in enumerate(tok) if t == mask]
+            conf, pred = res.mp[0], res.am[0]
+            fill = [i for i in masked if conf[i] >= tau]
+            if not fill:
+                fill = [max(masked, key=lambda i: (conf[i], -i))]
+            for i in fill:
+                tok[i] = int(pred[i])
+            res = O.forward(m, cache, P, np.array([tok])); fw += 1
+        for l in range(m.shape.n_layers):
+            cache.k[l][P:P + block] = res.block_k[l][0]
+            cache.v[l][P:P + block] = res.block_v[l][0]
+        out += tok
+        P += block
+    return np.array(out), fw
+
+
+def test_k0_reduces_to_threshold_decoding(micro_w):
+    m = O.OracleModel(MICRO, micro_w, act="fp64")
+    prompt = synth.make_prompt(MICRO, 10, seed=1)
+    want, fw_want = _threshold_decode(m, prompt, 8, 0.9, 24)
+    got, fw, _, _ = O.decode(m, prompt, 8, 0, 0.9, 24)
+    np.testing.assert_array_equal(got, want)
+    assert fw == fw_want
+
+
+def test_logit_reuse_and_kv_consistency(micro_w):
+    m = O.OracleModel(MICRO, micro_w, act="fp64")
+    prompt = synth.make_prompt(MICRO, 10, seed=1)
+    block, gen = 6, 18
+    toks, fw, cache, log = O.decode(m, prompt, block, 3, 0.9, gen, record=True)
+    assert len(log) > 0
+    for P, st in log:
+        w = st.winner
+        fresh = O.forward(m, cache, P, st.branches[w:w + 1])  # cache[0:P] is final
+        np.testing.assert_array_equal(fresh.am[0], st.am)
+        np.testing.assert_allclose(fresh.mp[0], st.mp, rtol=1e-12)
+        conf = [O.branch_confidence(st.branches[b], st.out.mp[b], 0) for b in range(len(st.branches))]
+        assert conf == st.conf
+    # KV cache after decoding == K/V of one block-causal pass over prompt + output
+    n_blocks = gen // block
+    positions, visible = block_layout(len(prompt), n_blocks, block, 0)
+    seq = np.concatenate([prompt, toks])
+    _, _, ks, vs = torch_forward(micro_w, MICRO, seq, positions, visible)
+    for l in range(MICRO.n_layers):
+        np.testing.assert_allclose(cache.k[l][:len(seq)], ks[l].numpy(), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(cache.v[l][:len(seq)], vs[l].numpy(), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("block", [4, 6])
+def test_exhaustive_one_extra_position_replay(micro_w, block):
+    """With k >= block every remaining position is a lookahead candidate.  At every
+    iteration, score the anchor and every one-extra-position branch with its own
+    separate forward; LoPA's winner must reach the brute-force maximum confidence."""
+    m = O.OracleModel(MICRO, micro_w, act="fp64")
+    prompt = synth.make_prompt(MICRO, 7, seed=9)
+    _, _, cache, log = O.decode(m, prompt, block, block, 0.9, 2 * block, record=True)
+    for P, st in log:
+        anchor = st.branches[0]
+        cands = [i for i in range(block) if anchor[i] == 0]
+        best = -1.0
+        for c in [None] + cands:
+            br = anchor.copy()
+            if c is not None:
+                br[c] = _greedy_token_of_step(st, c)
+            one = O.forward(m, cache, P, br[None, :])
+            rem = [i for i in range(block) if br[i] == 0]
+            conf = 1.0 if not rem else float(np.mean([one.mp[0][i] for i in rem]))
+            best = max(best, conf)
+        assert abs(st.conf[st.winner] - best) < 1e-12
+        assert sorted(st.candidates) == cands
+
+
+def _greedy_token_of_step(st, c):
+    # the lookahead branch that fills c carries the greedy token of the step's input
+    # summary at c; read it back from that branch
+    b = 1 + st.candidates.index(c)
+    return st.branches[b][c]
+
+
+# ------------------------------------------------------------- planted mistakes
+def _planted(monkeypatch, name, fn):
+    monkeypatch.setattr(OL, name, fn)
+
+
+@pytest.mark.parametrize("plant", ["rope_sign", "silu_identity", "rms_no_eps"])
+def test_pins_catch_planted_mistakes(micro_w, monkeypatch, plant):
+    real_rope, real_rms = OL.rope, OL.rmsnorm
+    if plant == "rope_sign":
+        _planted(monkeypatch, "rope", lambda x, pos, base: real_rope(x, -np.asarray(pos), base))
+    elif plant == "silu_identity":
+        _planted(monkeypatch, "silu", lambda x: x)
+    else:
+        _planted(monkeypatch, "rmsnorm", lambda x, g, eps: real_rms(x, g, 0.0))
+    with pytest.raises(AssertionError):
+        test_forward_matches_independent_torch_forward(micro_w, "fp64")
+
+
+def test_pins_catch_planted_decision_mistakes(monkeypatch):
+    cases = _golden_cases()
+    monkeypatch.setattr(OL, "select_winner", lambda conf: int(len(conf) - 1 - np.argmax(conf[::-1])))
+    with pytest.raises(AssertionError):
+        for c in cases:
+            test_decision_rules_hand_worked(c)
+    monkeypatch.undo()
+    monkeypatch.setattr(OL, "branch_confidence",
+                        lambda br, mp, mask: float(sum(mp[i] for i in range(len(br)) if br[i] == mask)))
+    with pytest.raises(AssertionError):
+        for c in cases:
+            test_decision_rules_hand_worked(c)
