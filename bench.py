@@ -1,0 +1,319 @@
+"""Benchmark of the LoPA branch-verification path on one GB300.
+
+A step is one whole single-sample decode of the workload: gen_len tokens in 32-token
+blocks, each block = one block-start forward + LoPA iterations (decide, 8-branch
+isolated verification forward, select, Commit-Winner), all inside the library's CUDA
+graphs.  Inputs (weights, prompt K/V) are resident in HBM before the timed region; each
+step rewinds the decoder to the end of the prompt and decodes again (nothing cached:
+every forward re-streams the 15 GB of weights, far larger than L2).
+
+Prints one JSON line (see the keys below).  --impl reference times the CPU oracle on
+the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes as C
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "decoded tokens/s per sample (Dream-7B-shaped, 8 branches)"
+UNIT = "tokens/s"
+# Tokens per forward of this workload, used only to turn the oracle's measured seconds
+# per verification forward into tokens/s (the oracle cannot finish a 7B decode within a
+# bounded sample).  It is the TPF the CUDA path measures on this workload; the parity
+# tests show both sides take the same decisions.
+REF_TPF = {"dream7b": 8.0, "dream7b_scaling": 8.0, "small": 4.0, "tiny": 1.5}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in self.rows if len(r) > 2 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) > 2 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows if len(r) >= 9
+                          for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+def oracle_seconds_per_forward(shape, dshape, weights, budget_s: float):
+    """Oracle (float64, bf16 storage) time of one nb x B verification forward, timed on
+    1 and 2 layers plus the LM head and extrapolated linearly to all layers."""
+    import dataclasses
+    from oracle import lopa_oracle as O
+    nb, B, P = dshape.k + 1, dshape.block, dshape.prompt_len
+    rng = np.random.default_rng(0)
+    br = rng.integers(1, shape.vocab, (nb, B))
+    br[rng.random((nb, B)) < 0.5] = shape.mask_id
+    times = {}
+    for n_l in (1, 2):
+        sh = dataclasses.replace(shape, n_layers=n_l)
+        m = O.OracleModel(sh, weights, act="bf16", cache_weights=False)
+        cache = O.KVCache.empty(sh, P + B)
+        for l in range(n_l):
+            cache.k[l][:P] = rng.standard_normal(cache.k[l][:P].shape)
+            cache.v[l][:P] = rng.standard_normal(cache.v[l][:P].shape)
+        t0 = time.perf_counter()
+        O.forward(m, cache, P, br)
+        times[n_l] = time.perf_counter() - t0
+    per_layer = max(times[2] - times[1], 1e-9)
+    fixed = max(times[1] - per_layer, 0.0)
+    return fixed + per_layer * shape.n_layers, times
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from diffusion_lookahead_decoding_gb300 import synth
+    shape, dshape = synth.WORKLOADS[args.workload]
+    weights = synth.make_weights(shape, 0)
+    tpf = REF_TPF[args.workload]
+    for _ in range(args.warmup):
+        oracle_seconds_per_forward(shape, dshape, weights, 0)
+    t0 = time.perf_counter()
+    per_fwd = []
+    for _ in range(args.steps):
+        s, _ = oracle_seconds_per_forward(shape, dshape, weights, 0)
+        per_fwd.append(s)
+    wall = time.perf_counter() - t0
+    spf = statistics.mean(per_fwd)
+    value = tpf / spf
+    cores = os.cpu_count()
+    sample = (f"oracle (numpy float64, bf16 storage) {dshape.k + 1}x{dshape.block}-token "
+              f"verification forward timed at 1 and 2 layers + LM head, extrapolated to "
+              f"{shape.n_layers} layers ({spf:.1f} s/forward); tokens/s = TPF {tpf} / that")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "prompt": dshape.prompt_len,
+                   "gen_len": dshape.gen_len, "block": dshape.block, "branches": dshape.k + 1},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def gemm_bytes(shape, T, kind):
+    """Algorithmic HBM bytes of one launch: weights once, activations in, outputs out."""
+    d, F, V = shape.d_model, shape.ffn, shape.vocab
+    if kind == 0:
+        return 2 * shape.qkv_rows * d + 2 * T * d + 4 * T * shape.qkv_rows
+    if kind == 1:
+        return 2 * d * shape.n_heads * shape.head_dim + 2 * T * shape.n_heads * shape.head_dim + 4 * T * d
+    if kind == 2:
+        return 2 * 2 * F * d + 2 * T * d + 2 * T * F
+    if kind == 3:
+        return 2 * d * F + 2 * T * F + 4 * T * d
+    return 2 * V * d + 2 * T * d + 12 * T * ((V + 255) // 256)
+
+
+def gemm_flops(shape, T, kind):
+    d, F, V = shape.d_model, shape.ffn, shape.vocab
+    n = {0: shape.qkv_rows * d, 1: d * shape.n_heads * shape.head_dim, 2: 2 * F * d, 3: d * F,
+         4: V * d}[kind]
+    return 2 * n * T
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dream7b")
+    ap.add_argument("--k", type=int, default=None, help="override the lookahead branch count")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    from diffusion_lookahead_decoding_gb300 import api, build, synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")  # replicas only: used for the barrier and the max
+    build.build()
+    shape, dshape = synth.WORKLOADS[args.workload]
+    if args.k is not None:
+        import dataclasses
+        dshape = dataclasses.replace(dshape, k=args.k)
+    B, P0, gen = dshape.block, dshape.prompt_len, dshape.gen_len
+    t_gen = time.perf_counter()
+    weights = synth.make_weights(shape, 0)
+    dev_w = api.upload_weights(shape, weights)
+    if args.no_cpu_baseline or rank != 0:
+        del weights
+        weights = None
+    t_gen = time.perf_counter() - t_gen
+    dec = api.LopaDecoder(shape, dev_w, B, dshape.k, dshape.tau, P0, P0 + gen)
+    prompt = synth.make_prompt(shape, P0, seed=1 + rank)
+    dec.prefill(prompt)
+
+    def one_step():
+        dec.rewind(P0)
+        return dec.decode(gen)
+
+    for _ in range(args.warmup):
+        one_step()
+    stats = []
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(dec.stream)
+        for _ in range(args.steps):
+            toks, st = one_step()
+            stats.append(st)
+        ev1.record(dec.stream)
+        torch.cuda.synchronize()
+        barrier()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    forwards = sum(s["forwards"] for s in stats)
+    iters = sum(s["steps"] for s in stats)
+    blocks = sum(s["blocks"] for s in stats)
+    tokens = sum(s["tokens"] for s in stats)
+    value = world * tokens / elapsed
+    tpf = tokens / forwards
+    ms_per_forward = elapsed * 1e3 / forwards
+    launches_per_forward = 8 * shape.n_layers + 3
+    gpu_launches = forwards * launches_per_forward + iters * 4
+
+    # Per-kernel timing of the projection GEMMs in the step's launch configuration.
+    T = (dshape.k + 1) * B
+    kern = {}
+    for kind, name in enumerate(["qkv", "o_proj", "gate_up_swiglu", "down", "lm_head"]):
+        iters_k = 2 * shape.n_layers if kind < 4 else 8
+        ms = dec.time_gemm(kind, iters_k)
+        by, fl = gemm_bytes(shape, T, kind), gemm_flops(shape, T, kind)
+        kern[name] = {"ms": ms, "GB/s": by / ms / 1e6, "TFLOP/s": fl / ms / 1e9}
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        peak_bw, peak_src = float(peaks["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        peak_bw, peak_src = 6800.0, "fallback"
+    dom = kern["gate_up_swiglu"]
+    roofline = {"kernel": "gemm_kernel<SWIGLU> (gate/up + SwiGLU)", "bound": "hbm",
+                "achieved": dom["GB/s"], "peak": peak_bw, "unit": "GB/s",
+                "frac": dom["GB/s"] / peak_bw, "traffic": None, "peak_source": peak_src}
+
+    # End to end through the public API with host buffers: prompt H2D, tokens D2H.
+    import torch as _t
+    pin_prompt = _t.from_numpy(prompt.astype(np.int32)).pin_memory()
+    e2e_times = []
+    for _ in range(max(1, args.e2e_steps)):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dec.prefill(pin_prompt.numpy())
+        toks_e, st_e = dec.decode(gen)
+        e2e_times.append(time.perf_counter() - t0)
+    from diffusion_lookahead_decoding_gb300 import _lib as L
+    d2h = gen * 4 + int(st_e["steps"]) * C.sizeof(L.StepResult)
+    e2e = {"value": world * gen / statistics.mean(e2e_times), "unit": UNIT,
+           "h2d_bytes_per_step": P0 * 4, "d2h_bytes_per_step": d2h,
+           "includes": "prefill of the prompt + full decode per step"}
+
+    cpu = None
+    if rank == 0 and weights is not None:
+        spf, times = oracle_seconds_per_forward(shape, dshape, weights, 20.0)
+        cpu = {"value": tpf / spf, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": (f"oracle {dshape.k + 1}x{B}-token verification forward timed at 1 "
+                          f"layer ({times[1]:.1f} s) and 2 layers ({times[2]:.1f} s) incl. LM "
+                          f"head, extrapolated to {shape.n_layers} layers = {spf:.1f} s/forward; "
+                          f"tokens/s at the measured TPF {tpf:.2f}")}
+    dec.close()
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "model": "Dream-7B-shaped (Qwen2.5-7B arch), random init",
+                       "prompt": P0, "gen_len": gen, "block": B, "branches": dshape.k + 1,
+                       "tau": dshape.tau, "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (15 GB weights re-streamed per forward)"},
+            "tpf": tpf, "ms_per_forward": ms_per_forward,
+            "lopa_iterations": iters, "blocks": blocks, "forwards": forwards,
+            "kernels": kern, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": gpu_launches, "clocks": clocks.summary(),
+            "weight_gen_s": t_gen,
+        }
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

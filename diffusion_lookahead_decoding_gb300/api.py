@@ -1,0 +1,210 @@
+"""Python face of the LoPA library: device memory and streams come from torch, every
+computation runs in liblopa.so (see include/lopa.h for the contract of each call)."""
+from __future__ import annotations
+
+import ctypes as C
+import dataclasses
+
+import numpy as np
+import torch
+
+from . import _lib as L
+
+
+def _i32p(a: np.ndarray):
+    return a.ctypes.data_as(C.POINTER(C.c_int32))
+
+
+def _f32p(a: np.ndarray):
+    return a.ctypes.data_as(C.POINTER(C.c_float))
+
+
+@dataclasses.dataclass
+class StepOutcome:
+    winner: int
+    n_filled: int
+    block_done: bool
+    n_valid_branches: int
+    forwards: int
+    prefix_len: int
+    conf: np.ndarray
+    filled_pos: np.ndarray
+    filled_tok: np.ndarray
+
+
+def upload_weights(shape, weights: dict, device="cuda") -> dict:
+    """Moves generated CPU weights to the device in the library's fused layouts:
+    wqkv = [wq; wk; wv] and wgu = [wg; wu] (row-concatenated)."""
+    dev = {}
+    bf = torch.bfloat16
+
+    def put(t):
+        return t.to(device=device, dtype=bf).contiguous()
+
+    dev["embed"] = put(weights["embed"])
+    dev["lm_head"] = put(weights["lm_head"])
+    dev["final_norm"] = put(weights["final_norm"])
+    for l in range(shape.n_layers):
+        dev[f"wqkv.{l}"] = torch.cat([put(weights[f"wq.{l}"]), put(weights[f"wk.{l}"]),
+                                      put(weights[f"wv.{l}"])], dim=0).contiguous()
+        dev[f"wo.{l}"] = put(weights[f"wo.{l}"])
+        dev[f"wgu.{l}"] = torch.cat([put(weights[f"wg.{l}"]), put(weights[f"wu.{l}"])],
+                                    dim=0).contiguous()
+        dev[f"wd.{l}"] = put(weights[f"wd.{l}"])
+        dev[f"attn_norm.{l}"] = put(weights[f"attn_norm.{l}"])
+        dev[f"mlp_norm.{l}"] = put(weights[f"mlp_norm.{l}"])
+    return dev
+
+
+class LopaDecoder:
+    """One decoding context: static KV cache, branch scratch, state, captured graphs."""
+
+    def __init__(self, shape, dev_weights: dict, block: int, k: int, tau: float,
+                 max_prompt: int, max_seq: int, stream: torch.cuda.Stream | None = None):
+        self.lib = L.load()
+        self.shape = shape
+        self.block = block
+        self.k = k
+        self.w = dev_weights  # keep the borrowed tensors alive
+        self.stream = stream or torch.cuda.Stream()
+        mc = L.ModelConfig(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads,
+                           shape.head_dim, shape.ffn, shape.vocab, shape.mask_id, max_seq,
+                           shape.rope_base, shape.rms_eps, shape.logit_scale)
+        n = shape.n_layers
+        arr = lambda key: (C.c_void_p * n)(*[dev_weights[f"{key}.{l}"].data_ptr() for l in range(n)])
+        self._arrays = {k_: arr(k_) for k_ in ("attn_norm", "wqkv", "wo", "mlp_norm", "wgu", "wd")}
+        cast = lambda a: C.cast(a, C.POINTER(C.c_void_p))
+        w = L.Weights(dev_weights["embed"].data_ptr(), dev_weights["lm_head"].data_ptr(),
+                      dev_weights["final_norm"].data_ptr(), cast(self._arrays["attn_norm"]),
+                      cast(self._arrays["wqkv"]), cast(self._arrays["wo"]),
+                      cast(self._arrays["mlp_norm"]), cast(self._arrays["wgu"]),
+                      cast(self._arrays["wd"]))
+        dc = L.DecodeConfig(block, k, tau, max_prompt)
+        ctx = C.c_void_p()
+        torch.cuda.synchronize()
+        L.check(self.lib.lopa_init_model(C.byref(mc), C.byref(w), C.byref(dc),
+                                         C.c_void_p(self.stream.cuda_stream), C.byref(ctx)))
+        self.ctx = ctx
+
+    # -- decoding -------------------------------------------------------------------
+    def prefill(self, prompt: np.ndarray):
+        p = np.ascontiguousarray(prompt, dtype=np.int32)
+        L.check(self.lib.lopa_prefill(self.ctx, _i32p(p), len(p)), self.ctx)
+
+    def step(self) -> StepOutcome:
+        r = L.StepResult()
+        L.check(self.lib.lopa_step(self.ctx, C.byref(r)), self.ctx)
+        nf = r.n_filled
+        return StepOutcome(r.winner, nf, bool(r.block_done), r.n_valid_branches, r.forwards,
+                           r.prefix_len, np.array(r.conf[:]), np.array(r.filled_pos[:nf]),
+                           np.array(r.filled_tok[:nf]))
+
+    def decode(self, gen_len: int):
+        out = np.zeros(gen_len, dtype=np.int32)
+        st = L.Stats()
+        L.check(self.lib.lopa_decode(self.ctx, gen_len, _i32p(out), C.byref(st)), self.ctx)
+        return out, {"tokens": st.tokens, "forwards": st.forwards, "steps": st.steps,
+                     "blocks": st.blocks, "seconds": st.seconds}
+
+    def rewind(self, pos: int):
+        L.check(self.lib.lopa_rewind(self.ctx, pos), self.ctx)
+
+    def time_gemm(self, kind: int, iters: int) -> float:
+        ms = C.c_float()
+        L.check(self.lib.lopa_time_gemm(self.ctx, kind, iters, C.byref(ms)), self.ctx)
+        return ms.value
+
+    # -- inspection -----------------------------------------------------------------
+    def get_block_state(self):
+        B = self.block
+        tok = np.zeros(B, np.int32)
+        am = np.zeros(B, np.int32)
+        mp = np.zeros(B, np.float32)
+        P = C.c_int()
+        L.check(self.lib.lopa_get_block_state(self.ctx, _i32p(tok), _i32p(am), _f32p(mp),
+                                              C.byref(P)), self.ctx)
+        return tok, am, mp, P.value
+
+    def set_block_state(self, tok, am, mp):
+        tok = np.ascontiguousarray(tok, np.int32)
+        am = np.ascontiguousarray(am, np.int32)
+        mp = np.ascontiguousarray(mp, np.float32)
+        L.check(self.lib.lopa_set_block_state(self.ctx, _i32p(tok), _i32p(am), _f32p(mp)),
+                self.ctx)
+
+    def verify_forward(self, branches: np.ndarray, want_hidden=False):
+        br = np.ascontiguousarray(branches, np.int32)
+        nb = br.shape[0]
+        am = np.zeros(br.shape, np.int32)
+        mp = np.zeros(br.shape, np.float32)
+        hid = np.zeros((nb, self.block, self.shape.d_model), np.float32) if want_hidden else None
+        L.check(self.lib.lopa_verify_forward(
+            self.ctx, _i32p(br), nb, _i32p(am), _f32p(mp),
+            _f32p(hid) if want_hidden else None), self.ctx)
+        return am, mp, hid
+
+    def read_kv(self, layer: int, pos0: int, n: int):
+        shp = (n, self.shape.n_kv_heads, self.shape.head_dim)
+        k = np.zeros(shp, np.uint16)
+        v = np.zeros(shp, np.uint16)
+        L.check(self.lib.lopa_read_kv(self.ctx, layer, pos0, n,
+                                      k.ctypes.data_as(C.POINTER(C.c_uint16)),
+                                      v.ctypes.data_as(C.POINTER(C.c_uint16))), self.ctx)
+        return bf16_words_to_f64(k), bf16_words_to_f64(v)
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            self.lib.lopa_free(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def bf16_words_to_f64(words: np.ndarray) -> np.ndarray:
+    return (words.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# -- kernel-level calls (device tensors, current torch stream) ---------------------------
+def _stream_ptr():
+    return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def linear_accumulate(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor):
+    """y += x @ w.T  (x [T,K] bf16, w [N,K] bf16, y [T,N] fp32, all contiguous on cuda)."""
+    T, K = x.shape
+    N = w.shape[0]
+    assert y.shape == (T, N) and y.dtype == torch.float32
+    L.check(L.load().lopa_linear_accumulate(x.data_ptr(), w.data_ptr(), y.data_ptr(), T, N, K,
+                                            _stream_ptr()))
+    return y
+
+
+def lmhead_argmax(hidden: torch.Tensor, lm_head: torch.Tensor, logit_scale: float, mask_id: int):
+    rows, d = hidden.shape
+    V = lm_head.shape[0]
+    lib = L.load()
+    ws = torch.empty(lib.lopa_lmhead_workspace_bytes(rows, V), dtype=torch.uint8,
+                     device=hidden.device)
+    am = torch.empty(rows, dtype=torch.int32, device=hidden.device)
+    mp = torch.empty(rows, dtype=torch.float32, device=hidden.device)
+    L.check(lib.lopa_lmhead_argmax(hidden.data_ptr(), lm_head.data_ptr(), rows, d, V,
+                                   logit_scale, mask_id, ws.data_ptr(), ws.numel(),
+                                   am.data_ptr(), mp.data_ptr(), _stream_ptr()))
+    return am, mp
+
+
+def branch_attention(q, k_prefix, v_prefix, k_block, v_block):
+    """q [nb*B, H, dh], k/v_prefix [P, Hk, dh], k/v_block [nb, B, Hk, dh] (bf16, cuda)."""
+    nb, B, Hk, dh = k_block.shape
+    H = q.shape[1]
+    P = k_prefix.shape[0]
+    out = torch.empty(nb * B, H * dh, dtype=torch.bfloat16, device=q.device)
+    L.check(L.load().lopa_branch_attention(
+        q.data_ptr(), k_prefix.data_ptr() if P else None, v_prefix.data_ptr() if P else None, P,
+        k_block.data_ptr(), v_block.data_ptr(), nb, B, H, Hk, dh, out.data_ptr(),
+        _stream_ptr()))
+    return out

@@ -1,0 +1,226 @@
+// Decision and commit kernels of one LoPA iteration ("SJTU x Huawei Xiaoyi release
+// LoPA", sections "Core design of LoPA" and "LoPA-Dist"):
+//   decide   : anchor fill (confidence-driven greedy, threshold tau, at least one fill)
+//              and the k lookahead branches (one extra fill each, at the k most
+//              confident positions still masked);
+//   select   : branch confidence = mean max-probability over the branch's remaining
+//              masked positions, winner = highest confidence (ties -> lowest branch),
+//              then the winner's tokens and logit summary become the state (logit reuse);
+//   commit   : Commit-Winner-Cache - copy the winner's pre-written block K/V from the
+//              branch scratch into the static cache;
+//   finalize : when the block has no [MASK] left, emit it and advance the prefix.
+// Blocks are at most 64 positions, so each decision runs in one CTA.
+#include "common.cuh"
+#include "internal.h"
+
+namespace lopa {
+
+namespace {
+
+__global__ void decide_kernel(DevState* st, int B, int k, float tau, int mask_id,
+                              int* __restrict__ branch_tok, int* __restrict__ valid) {
+  __shared__ float s_mp[LOPA_MAX_BLOCK];
+  __shared__ int s_rem[LOPA_MAX_BLOCK];
+  __shared__ int s_cand[LOPA_MAX_BRANCHES];
+  __shared__ int s_best;
+  const int i = threadIdx.x;  // blockDim.x == LOPA_MAX_BLOCK
+  const int nb = k + 1;
+  const int tok = i < B ? st->tok[i] : 0;
+  const int am = i < B ? st->am[i] : 0;
+  const float mp = i < B ? st->mp[i] : 0.f;
+  const bool masked = i < B && tok == mask_id;
+  bool fill = masked && mp >= tau;
+  s_mp[i] = mp;
+  if (i < LOPA_MAX_BRANCHES) s_cand[i] = -1;
+  if (i == 0) s_best = -1;
+  const int any_fill = __syncthreads_or(fill);
+  if (!any_fill) {
+    // Fill the single most confident masked position (lowest position on ties).
+    if (i == 0) {
+      int best = -1;
+      for (int j = 0; j < B; ++j) {
+        if (st->tok[j] != mask_id) continue;
+        if (best < 0 || s_mp[j] > s_mp[best]) best = j;
+      }
+      s_best = best;
+    }
+    __syncthreads();
+    fill = (i == s_best);
+  }
+  const int anchor = fill ? am : tok;
+  const bool rem = masked && !fill;
+  s_rem[i] = rem;
+  const int nrem = __syncthreads_count(rem);
+  const int nl = nrem < k ? nrem : k;
+  if (rem) {
+    // Rank among the remaining positions: more confident first, then lower position.
+    int rank = 0;
+    for (int j = 0; j < B; ++j)
+      if (s_rem[j] && (s_mp[j] > mp || (s_mp[j] == mp && j < i))) ++rank;
+    if (rank < nl) s_cand[rank] = i;
+  }
+  __syncthreads();
+  if (i < B) {
+    for (int b = 0; b < nb; ++b) {
+      const bool extra = b >= 1 && s_cand[b - 1] == i;
+      branch_tok[b * B + i] = extra ? am : anchor;
+    }
+  }
+  if (i < nb) valid[i] = (i == 0) || (i - 1 < nl);
+  if (i < LOPA_MAX_BRANCHES) st->cand[i] = s_cand[i];
+  if (i == 0) st->n_valid = 1 + nl;
+}
+
+__global__ void select_kernel(DevState* st, int B, int nb, int mask_id,
+                              const int* __restrict__ branch_tok, const int* __restrict__ valid,
+                              const int* __restrict__ am_b, const float* __restrict__ mp_b) {
+  __shared__ float s_conf[LOPA_MAX_BRANCHES];
+  __shared__ int s_w;
+  __shared__ int s_old[LOPA_MAX_BLOCK];
+  __shared__ int s_new[LOPA_MAX_BLOCK];
+  const int i = threadIdx.x;  // blockDim.x == LOPA_MAX_BLOCK
+  if (i < nb) {
+    float c = -INFINITY;
+    if (valid[i]) {
+      float sum = 0.f;
+      int cnt = 0;
+      for (int j = 0; j < B; ++j) {
+        if (branch_tok[i * B + j] == mask_id) {
+          sum += mp_b[i * B + j];
+          ++cnt;
+        }
+      }
+      c = cnt ? sum / (float)cnt : 1.0f;
+    }
+    s_conf[i] = c;
+  }
+  if (i < B) s_old[i] = st->tok[i];
+  __syncthreads();
+  if (i == 0) {
+    int w = 0;
+    for (int b = 1; b < nb; ++b)
+      if (s_conf[b] > s_conf[w]) w = b;
+    s_w = w;
+  }
+  __syncthreads();
+  const int w = s_w;
+  if (i < B) {
+    const int nt = branch_tok[w * B + i];
+    s_new[i] = nt;
+    st->tok[i] = nt;
+    st->am[i] = am_b[w * B + i];
+    st->mp[i] = mp_b[w * B + i];
+  }
+  __syncthreads();
+  if (i == 0) {
+    lopa_step_result& r = st->res;
+    int nf = 0, done = 1;
+    for (int j = 0; j < B; ++j) {
+      if (s_old[j] == mask_id && s_new[j] != mask_id) {
+        r.filled_pos[nf] = j;
+        r.filled_tok[nf] = s_new[j];
+        ++nf;
+      }
+      if (s_new[j] == mask_id) done = 0;
+    }
+    for (int b = 0; b < LOPA_MAX_BRANCHES; ++b) r.conf[b] = b < nb ? s_conf[b] : -INFINITY;
+    r.winner = w;
+    r.n_filled = nf;
+    r.block_done = done;
+    r.n_valid_branches = st->n_valid;
+    r.prefix_len = st->P;
+    r.device_error = st->err;
+    r.forwards = 1;
+    st->winner = w;
+    st->block_done = done;
+  }
+}
+
+// grid: (L, 2 [K, V], chunks); copies B rows of row_elems bf16 of the winner's branch.
+__global__ void commit_kv_kernel(const DevState* st, const bf16* __restrict__ ks,
+                                 const bf16* __restrict__ vs, bf16* __restrict__ kc,
+                                 bf16* __restrict__ vc, int B, int row_elems,
+                                 size_t layer_stride_cache, size_t layer_stride_scr) {
+  const int l = blockIdx.x;
+  const int w = st->winner;
+  const int P = st->P;
+  const bf16* src = (blockIdx.y == 0 ? ks : vs) + (size_t)l * layer_stride_scr +
+                    (size_t)w * B * row_elems;
+  bf16* dst = (blockIdx.y == 0 ? kc : vc) + (size_t)l * layer_stride_cache + (size_t)P * row_elems;
+  const int n16 = B * row_elems / 8;
+  for (int e = blockIdx.z * blockDim.x + threadIdx.x; e < n16; e += gridDim.z * blockDim.x)
+    reinterpret_cast<uint4*>(dst)[e] = reinterpret_cast<const uint4*>(src)[e];
+}
+
+__global__ void finalize_kernel(DevState* st, int B, int mask_id, int* __restrict__ out_tokens) {
+  const int i = threadIdx.x;
+  const int P = st->P, P0 = st->P0;
+  const int done = st->block_done;
+  __syncthreads();
+  if (!done) return;
+  if (i < B) {
+    out_tokens[P - P0 + i] = st->tok[i];
+    st->tok[i] = mask_id;
+  }
+  if (i == 0) st->P = P + B;
+}
+
+__global__ void state_reset_kernel(DevState* st, int P, int B, int mask_id) {
+  const int i = threadIdx.x;
+  if (i < LOPA_MAX_BLOCK) {
+    st->tok[i] = i < B ? mask_id : 0;
+    st->am[i] = 0;
+    st->mp[i] = 0.f;
+  }
+  if (i < LOPA_MAX_BRANCHES) st->cand[i] = -1;
+  if (i == 0) {
+    st->P = P;
+    st->P0 = P;
+    st->winner = 0;
+    st->block_done = 0;
+    st->err = 0;
+    st->n_valid = 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decide(void* st, int B, int k, float tau, int mask_id, int* branch_tok,
+                          int* valid, cudaStream_t s) {
+  decide_kernel<<<1, LOPA_MAX_BLOCK, 0, s>>>(static_cast<DevState*>(st), B, k, tau, mask_id,
+                                             branch_tok, valid);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select(void* st, int B, int nb, int mask_id, const int* branch_tok,
+                          const int* valid, const int* am_b, const float* mp_b,
+                          cudaStream_t s) {
+  select_kernel<<<1, LOPA_MAX_BLOCK, 0, s>>>(static_cast<DevState*>(st), B, nb, mask_id,
+                                             branch_tok, valid, am_b, mp_b);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_commit_kv(const void* st, const bf16* ks, const bf16* vs, bf16* kc,
+                             bf16* vc, int L, int nb, int B, int row_elems,
+                             size_t layer_stride_cache, size_t layer_stride_scr,
+                             cudaStream_t s) {
+  (void)nb;
+  const int n16 = B * row_elems / 8;
+  const int chunks = (n16 + 255) / 256 < 8 ? (n16 + 255) / 256 : 8;
+  commit_kv_kernel<<<dim3(L, 2, chunks), 256, 0, s>>>(static_cast<const DevState*>(st), ks, vs, kc,
+                                                       vc, B, row_elems, layer_stride_cache,
+                                                       layer_stride_scr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(void* st, int B, int mask_id, int* out_tokens, cudaStream_t s) {
+  finalize_kernel<<<1, LOPA_MAX_BLOCK, 0, s>>>(static_cast<DevState*>(st), B, mask_id, out_tokens);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_state_reset(void* st, int P, int B, int mask_id, cudaStream_t s) {
+  state_reset_kernel<<<1, LOPA_MAX_BLOCK, 0, s>>>(static_cast<DevState*>(st), P, B, mask_id);
+  return cudaGetLastError();
+}
+
+}  // namespace lopa

@@ -1,0 +1,119 @@
+// Host-side interfaces between the translation units of the LoPA library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/lopa.h"
+
+namespace lopa {
+
+typedef __nv_bfloat16 bf16;
+
+// ------------------------------------------------------------------ GEMM (tcgen05)
+enum GemmMode : int {
+  GEMM_RED_ADD = 0,  // out_f32[t][n] += sum_k act[t][k] * w[n][k]   (weights on M, tokens on N)
+  GEMM_SWIGLU = 1,   // out_bf16[t][f] = silu(gate) * up             (weights on M, tokens on N)
+  GEMM_LMSTATS = 2,  // per (vocab tile, token): max, sum exp, argmax  (tokens on M, vocab on N)
+};
+
+struct GemmArgs {
+  int mode;
+  int na;            // A tiles (128 rows each) per CTA: 1 or 2
+  int nbox;          // rows of the B tile = MMA N (16..256, multiple of 16)
+  int a_rows;        // rows of the A tensor (tiles at or beyond are skipped)
+  int k_blocks;      // K / 64
+  int splits;        // split-K factor (grid.y)
+  int stages;        // smem pipeline depth
+  uint32_t a_tile_bytes, stage_bytes;
+  int T;             // valid token rows
+  int F;             // SWIGLU: row offset of the up half in [2F][K]
+  int V, mask_id;    // LMSTATS
+  float scale;       // LMSTATS logit scale
+  float* out_f32;    int ldo;
+  bf16* out_bf16;    int ldh;
+  float* part_m; float* part_s; int* part_i; int part_ld;
+  int* err;
+};
+
+struct GemmLaunch {
+  CUtensorMap mapA, mapB;
+  GemmArgs args;
+  dim3 grid;
+  size_t smem;
+};
+
+// Encodes a 2-D bf16 tensor map over a row-major [rows][cols] matrix with a box of
+// box_rows x 64 columns and 128-byte swizzle.  Returns false on failure.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows, char* errbuf, size_t errlen);
+
+// Fills `L` for one GEMM.  Returns an empty string on success, else a reason.
+const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_alloc, int T,
+                      const void* w, int n_rows_w, int K, int na, int splits, int tok_box,
+                      int num_sms);
+cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s);
+cudaError_t gemm_set_smem_limits();
+int gemm_max_smem();
+
+// ------------------------------------------------------------------ attention
+struct AttnArgs {
+  const bf16* q;       // [nbq*Bq][H][dh]
+  bf16* out;           // [nbq*Bq][H*dh]
+  const bf16* kc;      // prefix keys   [*][Hk][dh]
+  const bf16* vc;
+  const bf16* kb;      // block keys    [nbq][Bk_stride][Hk][dh]
+  const bf16* vb;
+  const int* dP;       // device prefix length (may be null -> 0)
+  int pk_add;          // prefix keys = *dP + pk_add
+  int Bq, Bk, Bk_stride, nbq, H, Hk;
+};
+cudaError_t launch_attention(const AttnArgs& a, int dh, cudaStream_t s);
+
+// ------------------------------------------------------------------ pointwise
+cudaError_t launch_embed_norm(const int* tok, int T, const bf16* E, const bf16* g, float* x,
+                              bf16* n, int d, float eps, cudaStream_t s);
+cudaError_t launch_rmsnorm(const float* x, const bf16* g, bf16* n, int T, int d, float eps,
+                           cudaStream_t s);
+cudaError_t launch_rope_prewrite(float* qkv, int T, int H, int Hk, int dh, bf16* q,
+                                 bf16* kdst, bf16* vdst, int kv_to_cache, int Bq,
+                                 const float* cos_t, const float* sin_t, const int* dP,
+                                 cudaStream_t s);
+cudaError_t launch_lm_merge(const float* pm, const float* ps, const int* pi, int nvt,
+                            int part_ld, int T, int* am, float* mp, cudaStream_t s);
+cudaError_t launch_rope_table(float* cos_t, float* sin_t, int S, int dh, double base,
+                              cudaStream_t s);
+
+// ------------------------------------------------------------------ decision / commit
+// Decoding state kept in device memory so that one captured graph serves every
+// iteration and every block position.
+struct DevState {
+  int P;            // committed prefix length = absolute position of the current block
+  int P0;           // prompt length
+  int winner;       // winner of the last iteration
+  int block_done;   // 1 when the last iteration completed the block
+  int err;          // device error word (DeviceError)
+  int n_valid;      // 1 + number of lookahead branches built by the last decide
+  int pad[2];
+  int tok[LOPA_MAX_BLOCK];   // current block tokens ([MASK] where unfilled)
+  int am[LOPA_MAX_BLOCK];    // greedy token of the logits that produced `tok`
+  float mp[LOPA_MAX_BLOCK];  // its probability
+  int cand[LOPA_MAX_BRANCHES];  // lookahead candidate of branch b+1 (-1 if none)
+  lopa_step_result res;
+};
+
+cudaError_t launch_decide(void* st, int B, int k, float tau, int mask_id, int* branch_tok,
+                          int* valid, cudaStream_t s);
+cudaError_t launch_select(void* st, int B, int nb, int mask_id, const int* branch_tok,
+                          const int* valid, const int* am_b, const float* mp_b,
+                          cudaStream_t s);
+cudaError_t launch_commit_kv(const void* st, const bf16* ks, const bf16* vs, bf16* kc,
+                             bf16* vc, int L, int nb, int B, int row_elems,
+                             size_t layer_stride_cache, size_t layer_stride_scr,
+                             cudaStream_t s);
+cudaError_t launch_finalize(void* st, int B, int mask_id, int* out_tokens, cudaStream_t s);
+cudaError_t launch_state_reset(void* st, int P, int B, int mask_id, cudaStream_t s);
+
+}  // namespace lopa

@@ -1,0 +1,723 @@
+// Host orchestrator and C ABI of the LoPA branch-verification library.
+//
+// One context owns the static KV cache, the per-branch Pre-Write scratch, activations
+// and the decoding state (in device memory), and two captured CUDA graphs:
+//   start graph : the block-start forward of a fresh all-[MASK] block (1 branch), whose
+//                 logit summary seeds the first LoPA iteration;
+//   step graph  : one LoPA iteration - decide (anchor + lookahead branches), the
+//                 isolated verification forward of all 1+k branches, select (branch
+//                 confidence, winner, logit reuse), Commit-Winner of the winner's K/V,
+//                 finalize.
+// Every graph reads the block position from device memory, so one capture serves the
+// whole decode ("Decoding-efficiency revolution" blog, section 5.2: without CUDA graphs
+// kernel-launch overhead dominates).
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace lopa;
+
+namespace {
+
+thread_local std::string g_init_error;
+
+struct Plan {
+  int nb = 0, Bq = 0, T = 0, tok_box = 0, kv_to_cache = 0;
+  bool lm = false;
+  const int* tok = nullptr;
+  int* am_out = nullptr;
+  float* mp_out = nullptr;
+  std::vector<GemmLaunch> qkv, o, gu, dn;
+  GemmLaunch lmh;
+};
+
+}  // namespace
+
+struct lopa_ctx {
+  lopa_model_config mc{};
+  lopa_decode_config dc{};
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+  int num_sms = 0;
+  // borrowed weights
+  const bf16 *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
+  std::vector<const bf16*> attn_norm, wqkv, wo, mlp_norm, wgu, wd;
+  // owned device memory
+  std::vector<void*> allocs;
+  bf16 *kc = nullptr, *vc = nullptr, *ks = nullptr, *vs = nullptr;
+  float* x = nullptr;
+  bf16* n = nullptr;
+  float* qkv = nullptr;
+  bf16 *q = nullptr, *attn = nullptr, *hm = nullptr;
+  float *pm = nullptr, *ps = nullptr;
+  int* pi = nullptr;
+  int nvt = 0, part_ld = 0;
+  float *cos_t = nullptr, *sin_t = nullptr;
+  int *branch_tok = nullptr, *valid = nullptr, *am_b = nullptr, *tok_rows = nullptr;
+  float* mp_b = nullptr;
+  int* out_tokens = nullptr;
+  DevState* st = nullptr;
+  int Tmax = 0, nbmax = 0, qkv_rows = 0;
+  size_t cache_layer = 0, scr_layer = 0;
+  // graphs
+  Plan step_plan, start_plan;
+  cudaGraphExec_t step_exec = nullptr, start_exec = nullptr;
+  cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+  lopa_step_result* h_res = nullptr;  // pinned
+  // host-side view of the decode
+  bool prefilled = false, block_fresh = true;
+  int P = 0, P0 = 0;
+  std::string err;
+};
+
+namespace {
+
+int fail(lopa_ctx* c, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (c)
+    c->err = buf;
+  else
+    g_init_error = buf;
+  return code;
+}
+
+#define CK(call)                                                                        \
+  do {                                                                                  \
+    cudaError_t e_ = (call);                                                            \
+    if (e_ != cudaSuccess)                                                              \
+      return fail(ctx, LOPA_ERR_CUDA, "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), \
+                  __FILE__, __LINE__);                                                  \
+  } while (0)
+
+template <typename T>
+int dalloc(lopa_ctx* ctx, T** p, size_t count) {
+  void* v = nullptr;
+  const size_t bytes = std::max<size_t>(count * sizeof(T), 256);
+  if (cudaMalloc(&v, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(ctx, LOPA_ERR_OOM, "cudaMalloc of %zu bytes failed", bytes);
+  }
+  ctx->allocs.push_back(v);
+  *p = static_cast<T*>(v);
+  return 0;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int round16(int v) { return (v + 15) / 16 * 16; }
+
+// Split-K factor that fills the GPU with roughly one CTA per SM.
+int pick_splits(int tiles, int k_blocks, int num_sms) {
+  int s = num_sms / std::max(tiles, 1);
+  s = std::min(s, std::max(k_blocks / 2, 1));
+  return std::max(s, 1);
+}
+
+int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm, const int* tok,
+               int* am_out, float* mp_out) {
+  const lopa_model_config& m = ctx->mc;
+  const int L = m.n_layers, d = m.d_model, H = m.n_heads, dh = m.head_dim, F = m.ffn;
+  p.nb = nb;
+  p.Bq = Bq;
+  p.T = nb * Bq;
+  p.tok_box = std::min(256, round16(p.T));
+  p.kv_to_cache = kv_to_cache;
+  p.lm = lm;
+  p.tok = tok;
+  p.am_out = am_out;
+  p.mp_out = mp_out;
+  p.qkv.resize(L);
+  p.o.resize(L);
+  p.gu.resize(L);
+  p.dn.resize(L);
+  const int zt = (p.T + p.tok_box - 1) / p.tok_box;
+  auto plan = [&](GemmLaunch& G, int mode, const void* act, int K, const void* w, int nrows,
+                  const char* what) -> int {
+    int na = (mode == GEMM_RED_ADD && nrows >= 256) ? 2 : 1;
+    const int tiles = ((nrows + na * 128 - 1) / (na * 128)) * zt;
+    const int splits = mode == GEMM_RED_ADD ? pick_splits(tiles, K / 64, ctx->num_sms) : 1;
+    const char* e = plan_gemm(&G, mode, act, ctx->Tmax, p.T, w, nrows, K, na, splits, p.tok_box,
+                              ctx->num_sms);
+    if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s GEMM: %s", what, e);
+    G.args.err = &ctx->st->err;
+    return 0;
+  };
+  for (int l = 0; l < L; ++l) {
+    int r;
+    if ((r = plan(p.qkv[l], GEMM_RED_ADD, ctx->n, d, ctx->wqkv[l], ctx->qkv_rows, "qkv"))) return r;
+    p.qkv[l].args.out_f32 = ctx->qkv;
+    p.qkv[l].args.ldo = ctx->qkv_rows;
+    if ((r = plan(p.o[l], GEMM_RED_ADD, ctx->attn, H * dh, ctx->wo[l], d, "o"))) return r;
+    p.o[l].args.out_f32 = ctx->x;
+    p.o[l].args.ldo = d;
+    if ((r = plan(p.gu[l], GEMM_SWIGLU, ctx->n, d, ctx->wgu[l], 2 * F, "gate/up"))) return r;
+    p.gu[l].args.out_bf16 = ctx->hm;
+    p.gu[l].args.ldh = F;
+    if ((r = plan(p.dn[l], GEMM_RED_ADD, ctx->hm, F, ctx->wd[l], d, "down"))) return r;
+    p.dn[l].args.out_f32 = ctx->x;
+    p.dn[l].args.ldo = d;
+  }
+  if (lm) {
+    const int na = p.T > 128 ? 2 : 1;
+    const char* e = plan_gemm(&p.lmh, GEMM_LMSTATS, ctx->n, ctx->Tmax, p.T, ctx->lm_head, m.vocab,
+                              d, na, 1, 0, ctx->num_sms);
+    if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "lm-head GEMM: %s", e);
+    GemmArgs& a = p.lmh.args;
+    a.V = m.vocab;
+    a.mask_id = m.mask_id;
+    a.scale = m.logit_scale;
+    a.part_m = ctx->pm;
+    a.part_s = ctx->ps;
+    a.part_i = ctx->pi;
+    a.part_ld = ctx->part_ld;
+    a.err = &ctx->st->err;
+  }
+  return 0;
+}
+
+// Enqueues one forward of plan p on the context stream (also used inside capture).
+int enqueue_forward(lopa_ctx* ctx, const Plan& p) {
+  const lopa_model_config& m = ctx->mc;
+  const int L = m.n_layers, d = m.d_model, H = m.n_heads, Hk = m.n_kv_heads, dh = m.head_dim;
+  cudaStream_t s = ctx->stream;
+  CK(launch_embed_norm(p.tok, p.T, ctx->embed, ctx->attn_norm[0], ctx->x, ctx->n, d, m.rms_eps, s));
+  for (int l = 0; l < L; ++l) {
+    bf16* kcl = ctx->kc + (size_t)l * ctx->cache_layer;
+    bf16* vcl = ctx->vc + (size_t)l * ctx->cache_layer;
+    bf16* ksl = ctx->ks + (size_t)l * ctx->scr_layer;
+    bf16* vsl = ctx->vs + (size_t)l * ctx->scr_layer;
+    CK(launch_gemm(p.qkv[l], s));
+    CK(launch_rope_prewrite(ctx->qkv, p.T, H, Hk, dh, ctx->q, p.kv_to_cache ? kcl : ksl,
+                            p.kv_to_cache ? vcl : vsl, p.kv_to_cache, p.Bq, ctx->cos_t, ctx->sin_t,
+                            &ctx->st->P, s));
+    AttnArgs aa;
+    aa.q = ctx->q;
+    aa.out = ctx->attn;
+    aa.kc = kcl;
+    aa.vc = vcl;
+    aa.kb = ksl;
+    aa.vb = vsl;
+    aa.dP = &ctx->st->P;
+    aa.pk_add = p.kv_to_cache ? p.T : 0;
+    aa.Bq = p.Bq;
+    aa.Bk = p.kv_to_cache ? 0 : p.Bq;
+    aa.Bk_stride = p.Bq;
+    aa.nbq = p.nb;
+    aa.H = H;
+    aa.Hk = Hk;
+    CK(launch_attention(aa, dh, s));
+    CK(launch_gemm(p.o[l], s));
+    CK(launch_rmsnorm(ctx->x, ctx->mlp_norm[l], ctx->n, p.T, d, m.rms_eps, s));
+    CK(launch_gemm(p.gu[l], s));
+    CK(launch_gemm(p.dn[l], s));
+    CK(launch_rmsnorm(ctx->x, l + 1 < L ? ctx->attn_norm[l + 1] : ctx->final_norm, ctx->n, p.T, d,
+                      m.rms_eps, s));
+  }
+  if (p.lm) {
+    CK(launch_gemm(p.lmh, s));
+    CK(launch_lm_merge(ctx->pm, ctx->ps, ctx->pi, ctx->nvt, ctx->part_ld, p.T, p.am_out, p.mp_out,
+                       s));
+  }
+  return 0;
+}
+
+int enqueue_step(lopa_ctx* ctx) {
+  const int B = ctx->dc.block, nb = ctx->nbmax, mask = ctx->mc.mask_id;
+  cudaStream_t s = ctx->stream;
+  CK(launch_decide(ctx->st, B, ctx->dc.k, ctx->dc.tau, mask, ctx->branch_tok, ctx->valid, s));
+  int r = enqueue_forward(ctx, ctx->step_plan);
+  if (r) return r;
+  CK(launch_select(ctx->st, B, nb, mask, ctx->branch_tok, ctx->valid, ctx->am_b, ctx->mp_b, s));
+  CK(launch_commit_kv(ctx->st, ctx->ks, ctx->vs, ctx->kc, ctx->vc, ctx->mc.n_layers, nb, B,
+                      ctx->mc.n_kv_heads * ctx->mc.head_dim, ctx->cache_layer, ctx->scr_layer, s));
+  CK(launch_finalize(ctx->st, B, mask, ctx->out_tokens, s));
+  return 0;
+}
+
+int capture(lopa_ctx* ctx, int (*fn)(lopa_ctx*), cudaGraphExec_t* exec) {
+  cudaGraph_t g = nullptr;
+  CK(cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeThreadLocal));
+  int r = fn(ctx);
+  cudaError_t e = cudaStreamEndCapture(ctx->stream, &g);
+  if (r) {
+    if (g) cudaGraphDestroy(g);
+    return r;
+  }
+  if (e != cudaSuccess) return fail(ctx, LOPA_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
+  e = cudaGraphInstantiate(exec, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess)
+    return fail(ctx, LOPA_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+  return 0;
+}
+
+int start_fn(lopa_ctx* ctx) { return enqueue_forward(ctx, ctx->start_plan); }
+
+int check_device_error(lopa_ctx* ctx) {
+  int e = 0;
+  CK(cudaMemcpyAsync(&e, &ctx->st->err, sizeof(int), cudaMemcpyDeviceToHost, ctx->stream));
+  CK(cudaStreamSynchronize(ctx->stream));
+  if (e) return fail(ctx, LOPA_ERR_DEVICE_TIMEOUT, "device-side wait gave up (code %d)", e);
+  return 0;
+}
+
+int validate(const lopa_model_config* c, const lopa_decode_config* d) {
+  lopa_ctx* ctx = nullptr;
+  if (!c || !d) return fail(ctx, LOPA_ERR_INVALID_ARG, "null config");
+  if (c->n_layers < 1 || c->d_model < 1 || c->n_heads < 1 || c->n_kv_heads < 1 || c->vocab < 2 ||
+      c->ffn < 1 || c->max_seq < 1)
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "model dimensions must be positive");
+  if (c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128)
+    return fail(ctx, LOPA_ERR_UNSUPPORTED, "head_dim must be 32, 64 or 128");
+  if (c->n_heads % c->n_kv_heads) return fail(ctx, LOPA_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads");
+  if (c->d_model % 128 || c->ffn % 128 || ((c->n_heads + 2 * c->n_kv_heads) * c->head_dim) % 128 ||
+      (c->n_heads * c->head_dim) % 64)
+    return fail(ctx, LOPA_ERR_UNSUPPORTED, "d_model, ffn and q/k/v rows must be multiples of 128");
+  if (c->mask_id < 0 || c->mask_id >= c->vocab) return fail(ctx, LOPA_ERR_INVALID_ARG, "mask_id out of range");
+  if (!(c->rms_eps >= 0.f) || !(c->rope_base > 0.f) || !std::isfinite(c->logit_scale))
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "bad rms_eps / rope_base / logit_scale");
+  if (d->block < 16 || d->block > LOPA_MAX_BLOCK || d->block % 16)
+    return fail(ctx, LOPA_ERR_UNSUPPORTED, "block must be 16..%d and a multiple of 16", LOPA_MAX_BLOCK);
+  if (d->k < 0 || d->k >= LOPA_MAX_BRANCHES) return fail(ctx, LOPA_ERR_INVALID_ARG, "k must be 0..%d", LOPA_MAX_BRANCHES - 1);
+  if (d->max_prompt < 1 || d->max_prompt + d->block > c->max_seq)
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "need 1 <= max_prompt and max_prompt + block <= max_seq");
+  if (!std::isfinite(d->tau)) return fail(ctx, LOPA_ERR_INVALID_ARG, "tau must be finite");
+  return 0;
+}
+
+int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
+  const lopa_model_config& m = ctx->mc;
+  const int L = m.n_layers, d = m.d_model, H = m.n_heads, Hk = m.n_kv_heads, dh = m.head_dim;
+  const int F = m.ffn, V = m.vocab, B = ctx->dc.block;
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  CK(cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, dev));
+  int major = 0, minor = 0;
+  CK(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+  CK(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+  if (major != 10) return fail(ctx, LOPA_ERR_UNSUPPORTED, "needs an sm_10x GPU (found sm_%d%d)", major, minor);
+  CK(gemm_set_smem_limits());
+  if (!ctx->stream) {
+    CK(cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking));
+    ctx->own_stream = true;
+  }
+  // weights
+  if (!aligned16(w->embed) || !aligned16(w->lm_head) || !aligned16(w->final_norm) || !w->attn_norm ||
+      !w->wqkv || !w->wo || !w->mlp_norm || !w->wgu || !w->wd)
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "weight pointers must be non-null and 16-byte aligned");
+  ctx->embed = static_cast<const bf16*>(w->embed);
+  ctx->lm_head = static_cast<const bf16*>(w->lm_head);
+  ctx->final_norm = static_cast<const bf16*>(w->final_norm);
+  for (int l = 0; l < L; ++l) {
+    const void* ps[6] = {w->attn_norm[l], w->wqkv[l], w->wo[l], w->mlp_norm[l], w->wgu[l], w->wd[l]};
+    for (const void* p : ps)
+      if (!aligned16(p)) return fail(ctx, LOPA_ERR_INVALID_ARG, "layer %d weight pointer null or unaligned", l);
+    ctx->attn_norm.push_back(static_cast<const bf16*>(w->attn_norm[l]));
+    ctx->wqkv.push_back(static_cast<const bf16*>(w->wqkv[l]));
+    ctx->wo.push_back(static_cast<const bf16*>(w->wo[l]));
+    ctx->mlp_norm.push_back(static_cast<const bf16*>(w->mlp_norm[l]));
+    ctx->wgu.push_back(static_cast<const bf16*>(w->wgu[l]));
+    ctx->wd.push_back(static_cast<const bf16*>(w->wd[l]));
+  }
+  // buffers
+  ctx->nbmax = ctx->dc.k + 1;
+  ctx->Tmax = std::max(ctx->nbmax * B, ctx->dc.max_prompt);
+  ctx->qkv_rows = (H + 2 * Hk) * dh;
+  ctx->cache_layer = (size_t)m.max_seq * Hk * dh;
+  ctx->scr_layer = (size_t)ctx->nbmax * B * Hk * dh;
+  ctx->nvt = (V + 255) / 256;
+  ctx->part_ld = ctx->nbmax * B;
+  const size_t T = ctx->Tmax;
+  int r;
+  if ((r = dalloc(ctx, &ctx->kc, ctx->cache_layer * L)) || (r = dalloc(ctx, &ctx->vc, ctx->cache_layer * L)) ||
+      (r = dalloc(ctx, &ctx->ks, ctx->scr_layer * L)) || (r = dalloc(ctx, &ctx->vs, ctx->scr_layer * L)) ||
+      (r = dalloc(ctx, &ctx->x, T * d)) || (r = dalloc(ctx, &ctx->n, T * d)) ||
+      (r = dalloc(ctx, &ctx->qkv, T * ctx->qkv_rows)) || (r = dalloc(ctx, &ctx->q, T * H * dh)) ||
+      (r = dalloc(ctx, &ctx->attn, T * H * dh)) || (r = dalloc(ctx, &ctx->hm, T * F)) ||
+      (r = dalloc(ctx, &ctx->pm, (size_t)ctx->nvt * ctx->part_ld)) ||
+      (r = dalloc(ctx, &ctx->ps, (size_t)ctx->nvt * ctx->part_ld)) ||
+      (r = dalloc(ctx, &ctx->pi, (size_t)ctx->nvt * ctx->part_ld)) ||
+      (r = dalloc(ctx, &ctx->cos_t, (size_t)m.max_seq * dh / 2)) ||
+      (r = dalloc(ctx, &ctx->sin_t, (size_t)m.max_seq * dh / 2)) ||
+      (r = dalloc(ctx, &ctx->branch_tok, (size_t)ctx->nbmax * B)) ||
+      (r = dalloc(ctx, &ctx->valid, (size_t)LOPA_MAX_BRANCHES)) ||
+      (r = dalloc(ctx, &ctx->am_b, (size_t)ctx->nbmax * B)) ||
+      (r = dalloc(ctx, &ctx->mp_b, (size_t)ctx->nbmax * B)) ||
+      (r = dalloc(ctx, &ctx->tok_rows, T)) || (r = dalloc(ctx, &ctx->out_tokens, (size_t)m.max_seq)) ||
+      (r = dalloc(ctx, &ctx->st, 1)))
+    return r;
+  cudaStream_t s = ctx->stream;
+  CK(cudaMemsetAsync(ctx->qkv, 0, T * ctx->qkv_rows * sizeof(float), s));
+  CK(cudaMemsetAsync(ctx->kc, 0, ctx->cache_layer * L * sizeof(bf16), s));
+  CK(cudaMemsetAsync(ctx->vc, 0, ctx->cache_layer * L * sizeof(bf16), s));
+  CK(cudaMemsetAsync(ctx->st, 0, sizeof(DevState), s));
+  CK(cudaMemsetAsync(ctx->out_tokens, 0, (size_t)m.max_seq * sizeof(int), s));
+  CK(launch_rope_table(ctx->cos_t, ctx->sin_t, m.max_seq, dh, (double)m.rope_base, s));
+  CK(launch_state_reset(ctx->st, 0, B, m.mask_id, s));
+  CK(cudaEventCreate(&ctx->ev0));
+  CK(cudaEventCreate(&ctx->ev1));
+  CK(cudaMallocHost(&ctx->h_res, sizeof(lopa_step_result)));
+  // plans and graphs
+  if ((r = build_plan(ctx, ctx->step_plan, ctx->nbmax, B, 0, true, ctx->branch_tok, ctx->am_b, ctx->mp_b)))
+    return r;
+  if ((r = build_plan(ctx, ctx->start_plan, 1, B, 0, true, ctx->st->tok, ctx->st->am, ctx->st->mp)))
+    return r;
+  CK(cudaStreamSynchronize(s));
+  if ((r = capture(ctx, enqueue_step, &ctx->step_exec))) return r;
+  if ((r = capture(ctx, start_fn, &ctx->start_exec))) return r;
+  return 0;
+}
+
+void destroy(lopa_ctx* ctx) {
+  if (!ctx) return;
+  if (ctx->stream) cudaStreamSynchronize(ctx->stream);
+  if (ctx->step_exec) cudaGraphExecDestroy(ctx->step_exec);
+  if (ctx->start_exec) cudaGraphExecDestroy(ctx->start_exec);
+  if (ctx->ev0) cudaEventDestroy(ctx->ev0);
+  if (ctx->ev1) cudaEventDestroy(ctx->ev1);
+  if (ctx->h_res) cudaFreeHost(ctx->h_res);
+  for (void* p : ctx->allocs) cudaFree(p);
+  if (ctx->own_stream) cudaStreamDestroy(ctx->stream);
+  delete ctx;
+}
+
+// Runs one iteration (plus the block-start forward when the block is fresh).
+int step_impl(lopa_ctx* ctx, lopa_step_result* out) {
+  if (!ctx->prefilled) return fail(ctx, LOPA_ERR_BAD_STATE, "lopa_step before lopa_prefill");
+  int fwd = 0;
+  if (ctx->block_fresh) {
+    if (ctx->P + ctx->dc.block > ctx->mc.max_seq)
+      return fail(ctx, LOPA_ERR_BAD_STATE, "KV cache full: next block would end at %d > max_seq %d",
+                  ctx->P + ctx->dc.block, ctx->mc.max_seq);
+    CK(cudaGraphLaunch(ctx->start_exec, ctx->stream));
+    fwd = 1;
+  }
+  CK(cudaGraphLaunch(ctx->step_exec, ctx->stream));
+  CK(cudaMemcpyAsync(ctx->h_res, &ctx->st->res, sizeof(lopa_step_result), cudaMemcpyDeviceToHost,
+                     ctx->stream));
+  CK(cudaStreamSynchronize(ctx->stream));
+  lopa_step_result& r = *ctx->h_res;
+  r.forwards = 1 + fwd;
+  if (r.device_error) return fail(ctx, LOPA_ERR_DEVICE_TIMEOUT, "device-side wait gave up (code %d)", r.device_error);
+  ctx->block_fresh = r.block_done != 0;
+  if (r.block_done) ctx->P += ctx->dc.block;
+  if (out) *out = r;
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lopa_version(void) { return 100; }
+
+const char* lopa_last_error(const lopa_ctx* ctx) {
+  return ctx ? ctx->err.c_str() : g_init_error.c_str();
+}
+
+int lopa_init_model(const lopa_model_config* cfg, const lopa_weights* w, const lopa_decode_config* dcfg,
+                    void* stream, lopa_ctx** out) {
+  if (!out) return fail(nullptr, LOPA_ERR_INVALID_ARG, "out is null");
+  *out = nullptr;
+  if (!w) return fail(nullptr, LOPA_ERR_INVALID_ARG, "weights are null");
+  int r = validate(cfg, dcfg);
+  if (r) return r;
+  lopa_ctx* ctx = new lopa_ctx();
+  ctx->mc = *cfg;
+  ctx->dc = *dcfg;
+  ctx->stream = static_cast<cudaStream_t>(stream);
+  r = init_impl(ctx, w);
+  if (r) {
+    g_init_error = ctx->err;
+    destroy(ctx);
+    return r;
+  }
+  *out = ctx;
+  return 0;
+}
+
+void lopa_free(lopa_ctx* ctx) { destroy(ctx); }
+
+int lopa_prefill(lopa_ctx* ctx, const int32_t* prompt, int n) {
+  if (!ctx) return fail(nullptr, LOPA_ERR_INVALID_ARG, "ctx is null");
+  if (!prompt || n < 1 || n > ctx->dc.max_prompt)
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "prompt length %d outside [1, %d]", n, ctx->dc.max_prompt);
+  for (int i = 0; i < n; ++i)
+    if (prompt[i] < 0 || prompt[i] >= ctx->mc.vocab)
+      return fail(ctx, LOPA_ERR_INVALID_ARG, "prompt token %d at %d out of range", prompt[i], i);
+  cudaStream_t s = ctx->stream;
+  CK(cudaMemcpyAsync(ctx->tok_rows, prompt, sizeof(int) * n, cudaMemcpyHostToDevice, s));
+  CK(launch_state_reset(ctx->st, 0, ctx->dc.block, ctx->mc.mask_id, s));
+  Plan p;
+  int r = build_plan(ctx, p, 1, n, 1, false, ctx->tok_rows, nullptr, nullptr);
+  if (r) return r;
+  if ((r = enqueue_forward(ctx, p))) return r;
+  CK(launch_state_reset(ctx->st, n, ctx->dc.block, ctx->mc.mask_id, s));
+  if ((r = check_device_error(ctx))) return r;
+  ctx->prefilled = true;
+  ctx->block_fresh = true;
+  ctx->P = ctx->P0 = n;
+  return 0;
+}
+
+int lopa_step(lopa_ctx* ctx, lopa_step_result* out) {
+  if (!ctx) return fail(nullptr, LOPA_ERR_INVALID_ARG, "ctx is null");
+  return step_impl(ctx, out);
+}
+
+int lopa_decode(lopa_ctx* ctx, int gen_len, int32_t* out_tokens, lopa_stats* out) {
+  if (!ctx) return fail(nullptr, LOPA_ERR_INVALID_ARG, "ctx is null");
+  if (!ctx->prefilled) return fail(ctx, LOPA_ERR_BAD_STATE, "lopa_decode before lopa_prefill");
+  const int B = ctx->dc.block;
+  if (gen_len < 0 || gen_len % B) return fail(ctx, LOPA_ERR_INVALID_ARG, "gen_len must be a multiple of %d", B);
+  if (!ctx->block_fresh) return fail(ctx, LOPA_ERR_BAD_STATE, "a block is in progress; finish it with lopa_step");
+  if (ctx->P + gen_len > ctx->mc.max_seq)
+    return fail(ctx, LOPA_ERR_BAD_STATE, "decode would end at %d > max_seq %d", ctx->P + gen_len, ctx->mc.max_seq);
+  const int start = ctx->P - ctx->P0;
+  lopa_stats st{};
+  CK(cudaEventRecord(ctx->ev0, ctx->stream));
+  for (int b = 0; b < gen_len / B; ++b) {
+    int iters = 0;
+    while (true) {
+      lopa_step_result r;
+      int rc = step_impl(ctx, &r);
+      if (rc) return rc;
+      st.forwards += r.forwards;
+      st.steps += 1;
+      if (r.block_done) break;
+      if (++iters > B)
+        return fail(ctx, LOPA_ERR_BAD_STATE, "block did not finish within %d iterations", B);
+    }
+    st.blocks += 1;
+    st.tokens += B;
+  }
+  CK(cudaEventRecord(ctx->ev1, ctx->stream));
+  CK(cudaEventSynchronize(ctx->ev1));
+  float ms = 0.f;
+  CK(cudaEventElapsedTime(&ms, ctx->ev0, ctx->ev1));
+  st.seconds = ms * 1e-3;
+  if (out_tokens && gen_len > 0) {
+    CK(cudaMemcpyAsync(out_tokens, ctx->out_tokens + start, sizeof(int) * gen_len,
+                       cudaMemcpyDeviceToHost, ctx->stream));
+    CK(cudaStreamSynchronize(ctx->stream));
+  }
+  if (out) *out = st;
+  return 0;
+}
+
+int lopa_rewind(lopa_ctx* ctx, int pos) {
+  if (!ctx) return fail(nullptr, LOPA_ERR_INVALID_ARG, "ctx is null");
+  if (!ctx->prefilled) return fail(ctx, LOPA_ERR_BAD_STATE, "rewind before lopa_prefill");
+  const int B = ctx->dc.block;
+  const int committed = ctx->P;
+  if (pos < ctx->P0 || pos > committed || (pos - ctx->P0) % B)
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "rewind position %d must be in [%d, %d] on a block boundary",
+                pos, ctx->P0, committed);
+  CK(launch_state_reset(ctx->st, pos, B, ctx->mc.mask_id, ctx->stream));
+  // state_reset sets P0 = pos too; put the prompt length back.
+  CK(cudaMemcpyAsync(&ctx->st->P0, &ctx->P0, sizeof(int), cudaMemcpyHostToDevice, ctx->stream));
+  CK(cudaStreamSynchronize(ctx->stream));
+  ctx->P = pos;
+  ctx->block_fresh = true;
+  return 0;
+}
+
+int lopa_time_gemm(lopa_ctx* ctx, int kind, int iters, float* avg_ms) {
+  if (!ctx) return fail(nullptr, LOPA_ERR_INVALID_ARG, "ctx is null");
+  if (kind < 0 || kind > 4 || iters < 1 || !avg_ms) return fail(ctx, LOPA_ERR_INVALID_ARG, "bad kind/iters");
+  const Plan& p = ctx->step_plan;
+  const int L = ctx->mc.n_layers;
+  cudaStream_t s = ctx->stream;
+  CK(cudaEventRecord(ctx->ev0, s));
+  for (int i = 0; i < iters; ++i) {
+    const int l = i % L;
+    const GemmLaunch& G = kind == 0 ? p.qkv[l] : kind == 1 ? p.o[l] : kind == 2 ? p.gu[l]
+                        : kind == 3 ? p.dn[l] : p.lmh;
+    CK(launch_gemm(G, s));
+  }
+  CK(cudaEventRecord(ctx->ev1, s));
+  CK(cudaEventSynchronize(ctx->ev1));
+  float ms = 0.f;
+  CK(cudaEventElapsedTime(&ms, ctx->ev0, ctx->ev1));
+  *avg_ms = ms / iters;
+  // The q/k/v accumulator must start at zero for the next forward.
+  CK(cudaMemsetAsync(ctx->qkv, 0, (size_t)ctx->Tmax * ctx->qkv_rows * sizeof(float), s));
+  return check_device_error(ctx);
+}
+
+int lopa_get_block_state(lopa_ctx* ctx, int32_t* tok, int32_t* am, float* mp, int* prefix_len) {
+  if (!ctx) return fail(nullptr, LOPA_ERR_INVALID_ARG, "ctx is null");
+  const int B = ctx->dc.block;
+  cudaStream_t s = ctx->stream;
+  if (tok) CK(cudaMemcpyAsync(tok, ctx->st->tok, sizeof(int) * B, cudaMemcpyDeviceToHost, s));
+  if (am) CK(cudaMemcpyAsync(am, ctx->st->am, sizeof(int) * B, cudaMemcpyDeviceToHost, s));
+  if (mp) CK(cudaMemcpyAsync(mp, ctx->st->mp, sizeof(float) * B, cudaMemcpyDeviceToHost, s));
+  if (prefix_len) CK(cudaMemcpyAsync(prefix_len, &ctx->st->P, sizeof(int), cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  return 0;
+}
+
+int lopa_set_block_state(lopa_ctx* ctx, const int32_t* tok, const int32_t* am, const float* mp) {
+  if (!ctx) return fail(nullptr, LOPA_ERR_INVALID_ARG, "ctx is null");
+  if (!ctx->prefilled) return fail(ctx, LOPA_ERR_BAD_STATE, "set_block_state before lopa_prefill");
+  if (!tok || !am || !mp) return fail(ctx, LOPA_ERR_INVALID_ARG, "null state array");
+  const int B = ctx->dc.block;
+  bool any_mask = false;
+  for (int i = 0; i < B; ++i) {
+    if (tok[i] < 0 || tok[i] >= ctx->mc.vocab || am[i] < 0 || am[i] >= ctx->mc.vocab)
+      return fail(ctx, LOPA_ERR_INVALID_ARG, "token out of range at %d", i);
+    any_mask |= tok[i] == ctx->mc.mask_id;
+  }
+  if (!any_mask) return fail(ctx, LOPA_ERR_INVALID_ARG, "state must have at least one [MASK]");
+  if (ctx->P + B > ctx->mc.max_seq) return fail(ctx, LOPA_ERR_BAD_STATE, "KV cache full");
+  cudaStream_t s = ctx->stream;
+  CK(cudaMemcpyAsync(ctx->st->tok, tok, sizeof(int) * B, cudaMemcpyHostToDevice, s));
+  CK(cudaMemcpyAsync(ctx->st->am, am, sizeof(int) * B, cudaMemcpyHostToDevice, s));
+  CK(cudaMemcpyAsync(ctx->st->mp, mp, sizeof(float) * B, cudaMemcpyHostToDevice, s));
+  CK(cudaStreamSynchronize(s));
+  ctx->block_fresh = false;
+  return 0;
+}
+
+int lopa_verify_forward(lopa_ctx* ctx, const int32_t* branch_tok, int nb, int32_t* am, float* mp,
+                        float* hidden) {
+  if (!ctx) return fail(nullptr, LOPA_ERR_INVALID_ARG, "ctx is null");
+  if (!ctx->prefilled) return fail(ctx, LOPA_ERR_BAD_STATE, "verify_forward before lopa_prefill");
+  if (!branch_tok || nb < 1 || nb > ctx->nbmax)
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "nb must be 1..%d", ctx->nbmax);
+  const int B = ctx->dc.block, T = nb * B, d = ctx->mc.d_model;
+  if (ctx->P + B > ctx->mc.max_seq) return fail(ctx, LOPA_ERR_BAD_STATE, "KV cache full");
+  for (int i = 0; i < T; ++i)
+    if (branch_tok[i] < 0 || branch_tok[i] >= ctx->mc.vocab)
+      return fail(ctx, LOPA_ERR_INVALID_ARG, "branch token out of range at %d", i);
+  cudaStream_t s = ctx->stream;
+  CK(cudaMemcpyAsync(ctx->tok_rows, branch_tok, sizeof(int) * T, cudaMemcpyHostToDevice, s));
+  Plan p;
+  int r = build_plan(ctx, p, nb, B, 0, true, ctx->tok_rows, ctx->am_b, ctx->mp_b);
+  if (r) return r;
+  if ((r = enqueue_forward(ctx, p))) return r;
+  if (am) CK(cudaMemcpyAsync(am, ctx->am_b, sizeof(int) * T, cudaMemcpyDeviceToHost, s));
+  if (mp) CK(cudaMemcpyAsync(mp, ctx->mp_b, sizeof(float) * T, cudaMemcpyDeviceToHost, s));
+  if (hidden) CK(cudaMemcpyAsync(hidden, ctx->x, sizeof(float) * T * d, cudaMemcpyDeviceToHost, s));
+  return check_device_error(ctx);
+}
+
+int lopa_read_kv(lopa_ctx* ctx, int layer, int pos0, int n, uint16_t* k, uint16_t* v) {
+  if (!ctx) return fail(nullptr, LOPA_ERR_INVALID_ARG, "ctx is null");
+  if (layer < 0 || layer >= ctx->mc.n_layers || pos0 < 0 || n < 0 || pos0 + n > ctx->mc.max_seq)
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "layer/position range out of bounds");
+  const size_t row = (size_t)ctx->mc.n_kv_heads * ctx->mc.head_dim;
+  const size_t off = (size_t)layer * ctx->cache_layer + (size_t)pos0 * row;
+  cudaStream_t s = ctx->stream;
+  if (k) CK(cudaMemcpyAsync(k, ctx->kc + off, n * row * 2, cudaMemcpyDeviceToHost, s));
+  if (v) CK(cudaMemcpyAsync(v, ctx->vc + off, n * row * 2, cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  return 0;
+}
+
+// ---------------------------------------------------------------- kernel-level calls
+
+int lopa_linear_accumulate(const void* x, const void* w, float* y, int T, int N, int K, void* stream) {
+  lopa_ctx* ctx = nullptr;
+  if (!aligned16(x) || !aligned16(w) || !y) return fail(ctx, LOPA_ERR_INVALID_ARG, "null or unaligned pointer");
+  if (T < 1 || N < 128 || N % 128 || K < 64 || K % 64)
+    return fail(ctx, LOPA_ERR_UNSUPPORTED, "need T >= 1, N % 128 == 0, K % 64 == 0");
+  CK(gemm_set_smem_limits());
+  int dev = 0, sms = 0;
+  CK(cudaGetDevice(&dev));
+  CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int tok_box = std::min(256, round16(T));
+  const int na = N >= 256 ? 2 : 1;
+  const int tiles = ((N + na * 128 - 1) / (na * 128)) * ((T + tok_box - 1) / tok_box);
+  GemmLaunch G;
+  const char* e = plan_gemm(&G, GEMM_RED_ADD, x, T, T, w, N, K, na, pick_splits(tiles, K / 64, sms),
+                            tok_box, sms);
+  if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s", e);
+  G.args.out_f32 = y;
+  G.args.ldo = N;
+  CK(launch_gemm(G, static_cast<cudaStream_t>(stream)));
+  return 0;
+}
+
+size_t lopa_lmhead_workspace_bytes(int rows, int vocab) {
+  if (rows < 1 || vocab < 1) return 0;
+  return (size_t)((vocab + 255) / 256) * rows * 12 + 256;
+}
+
+int lopa_lmhead_argmax(const void* hidden, const void* lm_head, int rows, int d_model, int vocab,
+                       float logit_scale, int mask_id, void* workspace, size_t workspace_bytes,
+                       int32_t* argmax_out, float* maxp_out, void* stream) {
+  lopa_ctx* ctx = nullptr;
+  if (!aligned16(hidden) || !aligned16(lm_head) || !aligned16(workspace) || !argmax_out || !maxp_out)
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "null or unaligned pointer");
+  if (rows < 1 || vocab < 2 || d_model < 64 || d_model % 64 || mask_id < 0 || mask_id >= vocab)
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "bad shape");
+  if (workspace_bytes < lopa_lmhead_workspace_bytes(rows, vocab))
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "workspace too small");
+  CK(gemm_set_smem_limits());
+  const int nvt = (vocab + 255) / 256;
+  float* pm = static_cast<float*>(workspace);
+  float* ps = pm + (size_t)nvt * rows;
+  int* pi = reinterpret_cast<int*>(ps + (size_t)nvt * rows);
+  GemmLaunch G;
+  const char* e = plan_gemm(&G, GEMM_LMSTATS, hidden, rows, rows, lm_head, vocab, d_model,
+                            rows > 128 ? 2 : 1, 1, 0, 0);
+  if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s", e);
+  GemmArgs& a = G.args;
+  a.V = vocab;
+  a.mask_id = mask_id;
+  a.scale = logit_scale;
+  a.part_m = pm;
+  a.part_s = ps;
+  a.part_i = pi;
+  a.part_ld = rows;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CK(launch_gemm(G, s));
+  CK(launch_lm_merge(pm, ps, pi, nvt, rows, rows, argmax_out, maxp_out, s));
+  return 0;
+}
+
+int lopa_branch_attention(const void* q, const void* k_prefix, const void* v_prefix, int prefix_len,
+                          const void* k_block, const void* v_block, int n_branches, int block,
+                          int n_heads, int n_kv_heads, int head_dim, void* out, void* stream) {
+  lopa_ctx* ctx = nullptr;
+  if (!aligned16(q) || !aligned16(k_block) || !aligned16(v_block) || !aligned16(out))
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "null or unaligned pointer");
+  if (prefix_len < 0 || (prefix_len > 0 && (!aligned16(k_prefix) || !aligned16(v_prefix))))
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "bad prefix");
+  if (n_branches < 1 || block < 1 || block > 4096 || n_heads < 1 || n_kv_heads < 1 ||
+      n_heads % n_kv_heads)
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "bad shape");
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128)
+    return fail(ctx, LOPA_ERR_UNSUPPORTED, "head_dim must be 32, 64 or 128");
+  AttnArgs a;
+  a.q = static_cast<const bf16*>(q);
+  a.out = static_cast<bf16*>(out);
+  a.kc = static_cast<const bf16*>(k_prefix);
+  a.vc = static_cast<const bf16*>(v_prefix);
+  a.kb = static_cast<const bf16*>(k_block);
+  a.vb = static_cast<const bf16*>(v_block);
+  a.dP = nullptr;
+  a.pk_add = prefix_len;
+  a.Bq = block;
+  a.Bk = block;
+  a.Bk_stride = block;
+  a.nbq = n_branches;
+  a.H = n_heads;
+  a.Hk = n_kv_heads;
+  CK(launch_attention(a, head_dim, static_cast<cudaStream_t>(stream)));
+  return 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,217 @@
+/*
+ * lopa.h - C ABI of the GB300 (sm_103a) LoPA branch-verification library.
+ *
+ * LoPA (Lookahead Parallel Decoding, arXiv 2512.16229) decodes a diffusion LM block by
+ * block.  In every iteration it keeps the anchor branch (standard confidence-driven
+ * greedy fill), adds k lookahead branches (each fills one more of the k most confident
+ * masked positions), verifies all 1+k branches in ONE forward pass with attention
+ * isolated per branch, scores each branch by the mean max-probability of its remaining
+ * masked positions, keeps the winner and reuses the winner's logits for the next fill.
+ * Sources: "SJTU x Huawei Xiaoyi release LoPA: 7B diffusion LM, 1000+ tokens/s single
+ * sample" - sections "Core design of LoPA" (the iteration) and "LoPA-Dist" (static KV
+ * cache with the two-phase Pre-Write / Commit-Winner-Cache update).
+ *
+ * Conventions for every call:
+ *   - Return 0 (LOPA_OK) on success or a negative LOPA_ERR_* code.  A failed call
+ *     leaves the decoding state as it was, and lopa_last_error() holds a message.
+ *     No call aborts the process or traps the device: device-side waits are bounded
+ *     and report LOPA_ERR_DEVICE_TIMEOUT.
+ *   - "device" pointers are CUDA global-memory pointers on the current device;
+ *     "host" pointers are ordinary CPU memory.  bf16 = IEEE bfloat16 stored as
+ *     16-bit words.  All matrices are row-major.
+ *   - Work is enqueued on the caller's CUDA stream (a cudaStream_t passed as void*;
+ *     NULL = legacy default stream).  Calls that return results to host memory
+ *     synchronize that stream before returning.
+ *   - A lopa_ctx is not thread-safe; use one per thread or serialize calls.
+ */
+#ifndef LOPA_H
+#define LOPA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LOPA_MAX_BRANCHES 16 /* 1 anchor + up to 15 lookahead branches */
+#define LOPA_MAX_BLOCK 64    /* block length B */
+
+enum {
+  LOPA_OK = 0,
+  LOPA_ERR_INVALID_ARG = -1,    /* bad pointer, size, shape or config */
+  LOPA_ERR_BAD_STATE = -2,      /* call out of order (e.g. step before prefill) or cache full */
+  LOPA_ERR_CUDA = -3,           /* a CUDA runtime call failed */
+  LOPA_ERR_OOM = -4,            /* device allocation failed */
+  LOPA_ERR_DEVICE_TIMEOUT = -5, /* a bounded device-side wait gave up */
+  LOPA_ERR_UNSUPPORTED = -6     /* shape outside what the kernels implement */
+};
+
+typedef struct lopa_ctx lopa_ctx; /* opaque; owned by the library */
+
+/* Decoder-only transformer of the Qwen2.5 family (pre-norm RMSNorm, RoPE with the
+ * rotate-half convention, grouped-query attention, SwiGLU MLP, untied LM head).
+ * Kernel limits: head_dim in {32, 64, 128}; d_model, n_heads*head_dim and ffn
+ * multiples of 64; (n_heads + 2*n_kv_heads)*head_dim, d_model and ffn multiples of
+ * 128; n_heads a multiple of n_kv_heads. */
+typedef struct {
+  int n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab;
+  int mask_id;       /* token id of [MASK]; it is never predicted */
+  int max_seq;       /* capacity of the static KV cache in tokens (prompt + output) */
+  float rope_base;   /* RoPE theta base */
+  float rms_eps;     /* RMSNorm epsilon */
+  float logit_scale; /* logits = logit_scale * (final_hidden . lm_head_row) */
+} lopa_model_config;
+
+/* Borrowed device pointers (bf16), which must outlive the context.  Per-layer entries
+ * are HOST arrays of n_layers device pointers; the arrays themselves are copied at
+ * init and need not outlive the call. */
+typedef struct {
+  const void* embed;              /* [vocab][d_model] */
+  const void* lm_head;            /* [vocab][d_model] */
+  const void* final_norm;         /* [d_model] */
+  const void* const* attn_norm;   /* [L] -> [d_model] */
+  const void* const* wqkv;        /* [L] -> [(H + 2*Hk)*dh][d_model]: q rows (head-major), then k, then v */
+  const void* const* wo;          /* [L] -> [d_model][H*dh] */
+  const void* const* mlp_norm;    /* [L] -> [d_model] */
+  const void* const* wgu;         /* [L] -> [2*ffn][d_model]: gate rows, then up rows */
+  const void* const* wd;          /* [L] -> [d_model][ffn] */
+} lopa_weights;
+
+typedef struct {
+  int block;      /* block length B, 16 <= B <= LOPA_MAX_BLOCK, multiple of 16 */
+  int k;          /* lookahead branches, 0 <= k < LOPA_MAX_BRANCHES */
+  float tau;      /* confidence threshold of the anchor fill (fill when maxp >= tau) */
+  int max_prompt; /* longest prompt lopa_prefill will accept */
+} lopa_decode_config;
+
+/* Outcome of one LoPA iteration (one verification forward). */
+typedef struct {
+  int winner;            /* winning branch, 0 = anchor */
+  int n_filled;          /* positions filled by this iteration (anchor fills + lookahead fill of the winner) */
+  int block_done;        /* 1 when the block has no [MASK] left; it is then committed */
+  int n_valid_branches;  /* 1 + min(k, masked positions left after the anchor fill) */
+  int forwards;          /* forward passes run by this call (1, or 2 when a block-start forward ran) */
+  int prefix_len;        /* committed prefix length P when the iteration ran */
+  int device_error;      /* 0, or a device-side error code */
+  float conf[LOPA_MAX_BRANCHES]; /* branch confidences; -inf for padded (invalid) branches */
+  int filled_pos[LOPA_MAX_BLOCK]; /* first n_filled entries: positions in the block, ascending */
+  int filled_tok[LOPA_MAX_BLOCK]; /* tokens written at those positions */
+} lopa_step_result;
+
+typedef struct {
+  long long tokens;   /* generated tokens */
+  long long forwards; /* forward passes (block-start + one per iteration; prefill excluded) */
+  long long steps;    /* LoPA iterations */
+  long long blocks;   /* completed blocks */
+  double seconds;     /* device time of the decode (CUDA events), prefill excluded */
+} lopa_stats;
+
+/* Validates the configs, records the borrowed weight pointers, allocates the static KV
+ * cache [L][max_seq][Hk][dh] (K and V), the per-branch Pre-Write scratch, activations
+ * and state, precomputes RoPE tables and captures the iteration into CUDA graphs.
+ * stream: cudaStream_t to enqueue on (borrowed).  *out receives the context. */
+int lopa_init_model(const lopa_model_config* cfg, const lopa_weights* w,
+                    const lopa_decode_config* dcfg, void* stream, lopa_ctx** out);
+
+/* Runs the prompt (host int32 ids, n tokens, 1 <= n <= max_prompt) as one block that
+ * attends bidirectionally within itself, writes its K/V into cache[0:n), and resets the
+ * decoding state to an empty first output block at position n.  Synchronizes. */
+int lopa_prefill(lopa_ctx* ctx, const int32_t* prompt, int n);
+
+/* One LoPA iteration on the current block (running the block-start forward first when
+ * the block is fresh): anchor fill, lookahead branches, one isolated verification
+ * forward over all branches, confidences, winner, Commit-Winner of the winner's K/V,
+ * logit reuse.  out (host, may be NULL) receives the outcome.  Synchronizes.
+ * BAD_STATE before prefill or when the next block would exceed max_seq. */
+int lopa_step(lopa_ctx* ctx, lopa_step_result* out);
+
+/* Decodes gen_len tokens (a multiple of the block length) from a block boundary:
+ * for each block, the block-start forward then iterations until no [MASK] is left.
+ * out_tokens: host int32[gen_len] (may be NULL); out: host stats (may be NULL). */
+int lopa_decode(lopa_ctx* ctx, int gen_len, int32_t* out_tokens, lopa_stats* out);
+
+/* Discards everything decoded after absolute position pos (prompt_len <= pos <= the
+ * committed prefix, pos - prompt_len a multiple of the block length): the cache beyond
+ * pos counts as empty and the state becomes a fresh block at pos.  The prompt's K/V
+ * stay, so a new decode of the same prompt needs no second prefill. */
+int lopa_rewind(lopa_ctx* ctx, int pos);
+
+/* Message of the last failed call on ctx (or of the last failed init when ctx is NULL). */
+const char* lopa_last_error(const lopa_ctx* ctx);
+
+/* Frees everything the context owns (not the borrowed weights or stream). */
+void lopa_free(lopa_ctx* ctx);
+
+/* ---- inspection (used by parity tests) ---------------------------------------- */
+
+/* Copies the current block state to host: tok[B] (int32, [MASK] where unfilled),
+ * am[B] / mp[B] = greedy token and its probability from the logits that produced the
+ * state (the reused logits), *prefix_len = committed prefix P.  Any output may be NULL. */
+int lopa_get_block_state(lopa_ctx* ctx, int32_t* tok, int32_t* am, float* mp, int* prefix_len);
+
+/* Overwrites the current block's tok/am/mp (host arrays of B entries) so that the next
+ * lopa_step starts from that state (no block-start forward). */
+int lopa_set_block_state(lopa_ctx* ctx, const int32_t* tok, const int32_t* am, const float* mp);
+
+/* Runs one verification forward of nb branches (host int32 [nb][B], 1 <= nb <= 1+k)
+ * for the current block position without changing the state or the cache.  Outputs
+ * (host, each may be NULL): am/mp [nb][B]; hidden [nb][B][d_model] fp32 = residual
+ * stream after the last layer (before the final norm). */
+int lopa_verify_forward(lopa_ctx* ctx, const int32_t* branch_tok, int nb, int32_t* am,
+                        float* mp, float* hidden);
+
+/* Copies cache K and V for layer, positions [pos0, pos0+n) to host as bf16 words
+ * [n][Hk][dh] each (either may be NULL). */
+int lopa_read_kv(lopa_ctx* ctx, int layer, int pos0, int n, uint16_t* k, uint16_t* v);
+
+/* ---- kernel-level entry points (device pointers, caller's stream) -------------- */
+
+/* y[T][N] += x[T][K] . w[N][K]^T with bf16 inputs and fp32 accumulation on the
+ * tcgen05 tensor cores (the projection kernel of the verification forward).
+ * T >= 1, N multiple of 128, K multiple of 64; x, w 16-byte aligned; y fp32.  The
+ * update is applied with atomic adds, so y must not be written concurrently by others. */
+int lopa_linear_accumulate(const void* x, const void* w, float* y, int T, int N, int K,
+                           void* stream);
+
+/* Bytes of device workspace lopa_lmhead_argmax needs for `rows` rows. */
+size_t lopa_lmhead_workspace_bytes(int rows, int vocab);
+
+/* Fused LM head + online softmax ("SJTU x Huawei Xiaoyi release LoPA", section "Core
+ * design of LoPA": logits of the verification pass are reused, so only their greedy
+ * token and confidence are kept).  For each row r of hidden [rows][d_model] (bf16):
+ * z = logit_scale * hidden_r . lm_head^T over vocab (mask_id excluded);
+ * argmax_out[r] = argmax z (lowest id on ties), maxp_out[r] = 1 / sum exp(z - max z).
+ * Full-vocabulary logits are never written.  workspace: device buffer of at least
+ * lopa_lmhead_workspace_bytes(rows, vocab) bytes. */
+int lopa_lmhead_argmax(const void* hidden, const void* lm_head, int rows, int d_model,
+                       int vocab, float logit_scale, int mask_id, void* workspace,
+                       size_t workspace_bytes, int32_t* argmax_out, float* maxp_out,
+                       void* stream);
+
+/* Branch-isolated attention (same passage, "attention isolated between branches"):
+ * for branch b, query row (i, h) attends to the shared prefix keys [0, prefix_len)
+ * and to its own block keys [0, block) only, bidirectionally, with softmax scale
+ * 1/sqrt(head_dim) and grouped-query heads (head h uses KV head h / (n_heads/n_kv_heads)).
+ * q [nb*block][n_heads][head_dim], k_prefix/v_prefix [prefix_len][n_kv_heads][head_dim],
+ * k_block/v_block [nb][block][n_kv_heads][head_dim], out [nb*block][n_heads*head_dim];
+ * all bf16, 16-byte aligned.  head_dim in {32, 64, 128}; block <= 4096. */
+int lopa_branch_attention(const void* q, const void* k_prefix, const void* v_prefix,
+                          int prefix_len, const void* k_block, const void* v_block,
+                          int n_branches, int block, int n_heads, int n_kv_heads,
+                          int head_dim, void* out, void* stream);
+
+/* Diagnostics: launches the verification-step GEMM of one kind (0 = q/k/v, 1 = output
+ * projection, 2 = gate/up + SwiGLU, 3 = down, 4 = LM head) `iters` times on the
+ * context stream, cycling over the layers' weights, and writes the mean launch time
+ * in milliseconds (CUDA events) to *avg_ms.  The decoding state is not changed; the
+ * activation buffers hold garbage afterwards until the next forward rewrites them. */
+int lopa_time_gemm(lopa_ctx* ctx, int kind, int iters, float* avg_ms);
+
+/* Library version (major*10000 + minor*100 + patch). */
+int lopa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LOPA_H */

@@ -45,7 +45,7 @@ import math
 import numpy as np
 
 __all__ = [
-    "bf16_round", "rmsnorm", "rope", "silu", "logit_summary", "OracleModel", "prefill",
+    "bf16_round", "rmsnorm", "rope", "silu", "linear", "isolated_attention", "logit_summary", "OracleModel", "prefill",
     "forward", "anchor_fill", "lookahead_candidates", "build_branches",
     "branch_confidence", "select_winner", "lopa_step", "decode", "StepRecord",
 ]
@@ -105,6 +105,35 @@ def rope(x, pos, base):
 
 def silu(x):
     return x / (1.0 + np.exp(-x))
+
+
+def linear(x, W):
+    """x @ W^T for a weight stored [out_features, in_features]."""
+    return np.asarray(x, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T
+
+
+def isolated_attention(q, prefix_k, prefix_v, block_k, block_v):
+    """Attention of every branch over the shared prefix and its own block only.
+
+    q: [nb, B, H, dh]; prefix_k/v: [P, Hk, dh]; block_k/v: [nb, B, Hk, dh].
+    Query head h reads KV head h // (H / Hk) (grouped-query attention); softmax scale
+    1/sqrt(dh); no mask inside the block (bidirectional).  Each branch is a separate
+    loop iteration: branch b never sees another branch's keys."""
+    nb, B, H, dh = q.shape
+    Hk = block_k.shape[2]
+    group = H // Hk
+    out = np.zeros((nb, B, H, dh))
+    for b in range(nb):
+        keys = np.concatenate([prefix_k, block_k[b]], axis=0)  # [P+B, Hk, dh]
+        vals = np.concatenate([prefix_v, block_v[b]], axis=0)
+        for h in range(H):
+            g = h // group
+            s = q[b, :, h, :] @ keys[:, g, :].T / math.sqrt(dh)  # [B, P+B]
+            s = s - s.max(axis=-1, keepdims=True)
+            a = np.exp(s)
+            a /= a.sum(axis=-1, keepdims=True)
+            out[b, :, h, :] = a @ vals[:, g, :]
+    return out
 
 
 def logit_summary(z, mask_id):
@@ -194,39 +223,28 @@ def forward(model, cache, P, branches, want_logits=False):
     rnd = model.rnd
     branches = np.asarray(branches, dtype=np.int64)
     nb, B = branches.shape
-    H, Hk, dh, d = sh.n_heads, sh.n_kv_heads, sh.head_dim, sh.d_model
-    group = H // Hk
+    H, Hk, dh = sh.n_heads, sh.n_kv_heads, sh.head_dim
     pos = P + np.arange(B)
     x = model.W("embed")[branches]  # [nb, B, d]
     block_k, block_v = [], []
     for l in range(sh.n_layers):
         n = rnd(rmsnorm(x, model.W(f"attn_norm.{l}"), sh.rms_eps))
-        q = (n @ model.W(f"wq.{l}").T).reshape(nb, B, H, dh)
-        k = (n @ model.W(f"wk.{l}").T).reshape(nb, B, Hk, dh)
-        v = (n @ model.W(f"wv.{l}").T).reshape(nb, B, Hk, dh)
+        q = linear(n, model.W(f"wq.{l}")).reshape(nb, B, H, dh)
+        k = linear(n, model.W(f"wk.{l}")).reshape(nb, B, Hk, dh)
+        v = linear(n, model.W(f"wv.{l}")).reshape(nb, B, Hk, dh)
         q = rnd(np.stack([rope(q[b], pos, sh.rope_base) for b in range(nb)]))
         k = rnd(np.stack([rope(k[b], pos, sh.rope_base) for b in range(nb)]))
         v = rnd(v)
         block_k.append(k)
         block_v.append(v)
-        attn = np.zeros((nb, B, H, dh))
-        for b in range(nb):
-            keys = np.concatenate([cache.k[l][:P], k[b]], axis=0)  # [P+B, Hk, dh]
-            vals = np.concatenate([cache.v[l][:P], v[b]], axis=0)
-            for h in range(H):
-                g = h // group
-                s = q[b, :, h, :] @ keys[:, g, :].T / math.sqrt(dh)  # [B, P+B]
-                s = s - s.max(axis=-1, keepdims=True)
-                a = np.exp(s)
-                a /= a.sum(axis=-1, keepdims=True)
-                attn[b, :, h, :] = a @ vals[:, g, :]
+        attn = isolated_attention(q, cache.k[l][:P], cache.v[l][:P], k, v)
         o = rnd(attn.reshape(nb, B, H * dh))
-        x = x + o @ model.W(f"wo.{l}").T
+        x = x + linear(o, model.W(f"wo.{l}"))
         n2 = rnd(rmsnorm(x, model.W(f"mlp_norm.{l}"), sh.rms_eps))
-        hm = rnd(silu(n2 @ model.W(f"wg.{l}").T) * (n2 @ model.W(f"wu.{l}").T))
-        x = x + hm @ model.W(f"wd.{l}").T
+        hm = rnd(silu(linear(n2, model.W(f"wg.{l}"))) * linear(n2, model.W(f"wu.{l}")))
+        x = x + linear(hm, model.W(f"wd.{l}"))
     hf = rnd(rmsnorm(x, model.W("final_norm"), sh.rms_eps))
-    z = sh.logit_scale * (hf @ model.W("lm_head").T)
+    z = sh.logit_scale * linear(hf, model.W("lm_head"))
     am, mp, p2 = logit_summary(z, sh.mask_id)
     out = ForwardOut(am, mp, p2, x, block_k, block_v)
     if want_logits:

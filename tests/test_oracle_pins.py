@@ -336,3 +336,34 @@ def test_pins_catch_planted_decision_mistakes(monkeypatch):
     with pytest.raises(AssertionError):
         for c in cases:
             test_decision_rules_hand_worked(c)
+
+
+# ------------------------------------------------------------- isolated attention
+def test_isolated_attention_bruteforce_and_special_cases():
+    rng = np.random.default_rng(11)
+    nb, B, H, Hk, dh, P = 2, 3, 4, 2, 4, 5
+    q = rng.standard_normal((nb, B, H, dh))
+    kp, vp = rng.standard_normal((P, Hk, dh)), rng.standard_normal((P, Hk, dh))
+    kb, vb = rng.standard_normal((nb, B, Hk, dh)), rng.standard_normal((nb, B, Hk, dh))
+    got = O.isolated_attention(q, kp, vp, kb, vb)
+    for b in range(nb):
+        for i in range(B):
+            for h in range(H):
+                g = h // (H // Hk)
+                keys = [kp[j, g] for j in range(P)] + [kb[b, j, g] for j in range(B)]
+                vals = [vp[j, g] for j in range(P)] + [vb[b, j, g] for j in range(B)]
+                sc = [sum(q[b, i, h, e] * kk[e] for e in range(dh)) / math.sqrt(dh) for kk in keys]
+                mx = max(sc)
+                w = [math.exp(s - mx) for s in sc]
+                tot = sum(w)
+                ref = [sum(w[j] * vals[j][e] for j in range(len(vals))) / tot for e in range(dh)]
+                np.testing.assert_allclose(got[b, i, h], ref, rtol=1e-12, atol=1e-12)
+    # one key only -> its value; identical keys -> mean of the values
+    one = O.isolated_attention(q[:, :1], kp[:0], vp[:0], kb[:, :1], vb[:, :1])
+    np.testing.assert_allclose(one[:, 0], np.repeat(vb[:, 0], H // Hk, axis=1), rtol=1e-14)
+    same_k = np.ones((nb, B, Hk, dh))
+    mean = O.isolated_attention(q, kp[:0], vp[:0], same_k, vb)
+    np.testing.assert_allclose(mean[0, 1, 3], vb[0, :, 1].mean(0), rtol=1e-12)
+    # another branch's block never leaks in
+    vb2 = vb.copy(); vb2[1] += 100.0
+    np.testing.assert_array_equal(O.isolated_attention(q, kp, vp, kb, vb2)[0], got[0])
