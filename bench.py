@@ -180,8 +180,12 @@ def main():
     ap.add_argument("--k", type=int, default=None, help="override the lookahead branch count")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--profile-gemm", type=int, default=None,
+                    help="only launch this projection GEMM kind 3 times (for ncu captures)")
+    ap.add_argument("--profile-decode", action="store_true",
+                    help="prefill + warmup decodes + steps decodes, no timing (for ncu launch lists)")
     args = ap.parse_args()
-    if args.warmup < 3 and args.impl == "ours":
+    if args.warmup < 3 and args.impl == "ours" and not (args.profile_decode or args.profile_gemm is not None):
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
@@ -203,13 +207,26 @@ def main():
     t_gen = time.perf_counter()
     weights = synth.make_weights(shape, 0)
     dev_w = api.upload_weights(shape, weights)
-    if args.no_cpu_baseline or rank != 0:
+    if args.no_cpu_baseline or rank != 0 or args.profile_decode or args.profile_gemm is not None:
         del weights
         weights = None
     t_gen = time.perf_counter() - t_gen
     dec = api.LopaDecoder(shape, dev_w, B, dshape.k, dshape.tau, P0, P0 + gen)
+    if args.profile_gemm is not None:
+        ms = dec.time_gemm(args.profile_gemm, 3)
+        print(json.dumps({"profile_gemm": args.profile_gemm, "ms": ms}), flush=True)
+        dec.close()
+        return
     prompt = synth.make_prompt(shape, P0, seed=1 + rank)
     dec.prefill(prompt)
+    if args.profile_decode:
+        for _ in range(args.warmup + args.steps):
+            dec.rewind(P0)
+            _, st = dec.decode(gen)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_decode": st}), flush=True)
+        dec.close()
+        return
 
     def one_step():
         dec.rewind(P0)

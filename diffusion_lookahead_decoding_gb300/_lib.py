@@ -71,6 +71,8 @@ SIGNATURES = {
     "lopa_read_kv": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.POINTER(C.c_uint16),
                                C.POINTER(C.c_uint16)]),
     "lopa_rewind": (C.c_int, [C.c_void_p, C.c_int]),
+    "lopa_read_branch_kv": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.POINTER(C.c_uint16),
+                                      C.POINTER(C.c_uint16)]),
     "lopa_time_gemm": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.POINTER(C.c_float)]),
     "lopa_linear_accumulate": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
                                          C.c_int, C.c_void_p]),

@@ -152,6 +152,15 @@ class LopaDecoder:
                                       v.ctypes.data_as(C.POINTER(C.c_uint16))), self.ctx)
         return bf16_words_to_f64(k), bf16_words_to_f64(v)
 
+    def read_branch_kv(self, layer: int, branch: int):
+        shp = (self.block, self.shape.n_kv_heads, self.shape.head_dim)
+        k = np.zeros(shp, np.uint16)
+        v = np.zeros(shp, np.uint16)
+        L.check(self.lib.lopa_read_branch_kv(self.ctx, layer, branch,
+                                             k.ctypes.data_as(C.POINTER(C.c_uint16)),
+                                             v.ctypes.data_as(C.POINTER(C.c_uint16))), self.ctx)
+        return bf16_words_to_f64(k), bf16_words_to_f64(v)
+
     def close(self):
         if getattr(self, "ctx", None):
             self.lib.lopa_free(self.ctx)

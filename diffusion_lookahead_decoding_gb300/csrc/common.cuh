@@ -180,6 +180,35 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// ---------------------------------------------------------------- programmatic launch
+// Every kernel of the path is launched with programmatic stream serialization: it may
+// start while its predecessor is still running, does its set-up (and streams data that
+// does not depend on the predecessor, such as weights), then waits here before it reads
+// anything the predecessor wrote.  pdl_trigger lets the next kernel start early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Drops a 128-byte line from L2 without writing it back (its contents become undefined).
+// Used on split-K partial sums once they have been consumed, so that dead partials never
+// cost HBM write bandwidth.
+__device__ __forceinline__ void l2_discard128(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
+// Discards the `row_floats`-wide row at `base` of each of `nsplit` partial splits
+// (`stride` floats apart); the row must start on a 128-byte boundary and the calling CTA
+// must have finished reading it.
+__device__ __forceinline__ void discard_partial_row(const float* base, size_t stride, int nsplit,
+                                                    int row_floats) {
+  const int lines = row_floats / 32;
+  for (int e = threadIdx.x; e < lines * nsplit; e += blockDim.x) {
+    const int s = e / lines, l = e - s * lines;
+    l2_discard128(base + (size_t)s * stride + (size_t)l * 32);
+  }
+}
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -19,6 +19,8 @@ namespace {
 
 __global__ void decide_kernel(DevState* st, int B, int k, float tau, int mask_id,
                               int* __restrict__ branch_tok, int* __restrict__ valid) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float s_mp[LOPA_MAX_BLOCK];
   __shared__ int s_rem[LOPA_MAX_BLOCK];
   __shared__ int s_cand[LOPA_MAX_BRANCHES];
@@ -74,6 +76,8 @@ __global__ void decide_kernel(DevState* st, int B, int k, float tau, int mask_id
 __global__ void select_kernel(DevState* st, int B, int nb, int mask_id,
                               const int* __restrict__ branch_tok, const int* __restrict__ valid,
                               const int* __restrict__ am_b, const float* __restrict__ mp_b) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float s_conf[LOPA_MAX_BRANCHES];
   __shared__ int s_w;
   __shared__ int s_old[LOPA_MAX_BLOCK];
@@ -141,6 +145,8 @@ __global__ void commit_kv_kernel(const DevState* st, const bf16* __restrict__ ks
                                  const bf16* __restrict__ vs, bf16* __restrict__ kc,
                                  bf16* __restrict__ vc, int B, int row_elems,
                                  size_t layer_stride_cache, size_t layer_stride_scr) {
+  pdl_wait();
+  pdl_trigger();
   const int l = blockIdx.x;
   const int w = st->winner;
   const int P = st->P;
@@ -153,6 +159,8 @@ __global__ void commit_kv_kernel(const DevState* st, const bf16* __restrict__ ks
 }
 
 __global__ void finalize_kernel(DevState* st, int B, int mask_id, int* __restrict__ out_tokens) {
+  pdl_wait();
+  pdl_trigger();
   const int i = threadIdx.x;
   const int P = st->P, P0 = st->P0;
   const int done = st->block_done;
@@ -187,17 +195,15 @@ __global__ void state_reset_kernel(DevState* st, int P, int B, int mask_id) {
 
 cudaError_t launch_decide(void* st, int B, int k, float tau, int mask_id, int* branch_tok,
                           int* valid, cudaStream_t s) {
-  decide_kernel<<<1, LOPA_MAX_BLOCK, 0, s>>>(static_cast<DevState*>(st), B, k, tau, mask_id,
-                                             branch_tok, valid);
-  return cudaGetLastError();
+  return launch_pdl(decide_kernel, dim3(1), dim3(LOPA_MAX_BLOCK), 0, s, static_cast<DevState*>(st),
+                    B, k, tau, mask_id, branch_tok, valid);
 }
 
 cudaError_t launch_select(void* st, int B, int nb, int mask_id, const int* branch_tok,
                           const int* valid, const int* am_b, const float* mp_b,
                           cudaStream_t s) {
-  select_kernel<<<1, LOPA_MAX_BLOCK, 0, s>>>(static_cast<DevState*>(st), B, nb, mask_id,
-                                             branch_tok, valid, am_b, mp_b);
-  return cudaGetLastError();
+  return launch_pdl(select_kernel, dim3(1), dim3(LOPA_MAX_BLOCK), 0, s, static_cast<DevState*>(st),
+                    B, nb, mask_id, branch_tok, valid, am_b, mp_b);
 }
 
 cudaError_t launch_commit_kv(const void* st, const bf16* ks, const bf16* vs, bf16* kc,
@@ -207,15 +213,14 @@ cudaError_t launch_commit_kv(const void* st, const bf16* ks, const bf16* vs, bf1
   (void)nb;
   const int n16 = B * row_elems / 8;
   const int chunks = (n16 + 255) / 256 < 8 ? (n16 + 255) / 256 : 8;
-  commit_kv_kernel<<<dim3(L, 2, chunks), 256, 0, s>>>(static_cast<const DevState*>(st), ks, vs, kc,
-                                                       vc, B, row_elems, layer_stride_cache,
-                                                       layer_stride_scr);
-  return cudaGetLastError();
+  return launch_pdl(commit_kv_kernel, dim3(L, 2, chunks), dim3(256), 0, s,
+                    static_cast<const DevState*>(st), ks, vs, kc, vc, B, row_elems,
+                    layer_stride_cache, layer_stride_scr);
 }
 
 cudaError_t launch_finalize(void* st, int B, int mask_id, int* out_tokens, cudaStream_t s) {
-  finalize_kernel<<<1, LOPA_MAX_BLOCK, 0, s>>>(static_cast<DevState*>(st), B, mask_id, out_tokens);
-  return cudaGetLastError();
+  return launch_pdl(finalize_kernel, dim3(1), dim3(LOPA_MAX_BLOCK), 0, s,
+                    static_cast<DevState*>(st), B, mask_id, out_tokens);
 }
 
 cudaError_t launch_state_reset(void* st, int P, int B, int mask_id, cudaStream_t s) {

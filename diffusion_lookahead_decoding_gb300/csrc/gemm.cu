@@ -3,20 +3,24 @@
 // Every projection of the verification forward multiplies the (1+k)*B token rows of
 // all branches by one weight matrix ("Decoding-efficiency revolution" blog, section
 // 3.3: all branch forwards share one matmul).  The weight stream is the cost, so each
-// CTA owns a slab of weight rows and streams it once through a TMA -> shared memory ->
-// tcgen05.mma pipeline, with the whole token tile (up to 256 rows) as the MMA's N side:
+// CTA owns a slab of weight rows and streams it once through TMA -> shared memory ->
+// tcgen05.mma, with the whole token tile (up to 256 rows) on the MMA's other side:
 //
-//   RED_ADD : D[w_row][tok] = W . X^T over a K-split; the epilogue atomically adds
-//             into an fp32 [T][N] output (q/k/v accumulator, or the residual stream).
+//   RED_ADD : D[w_row][tok] = W . X^T over a K-split; the epilogue stores the split's
+//             fp32 partial [split][T][N] (summed in a fixed order by the consumer) or,
+//             for the standalone call, adds it atomically into an fp32 [T][N] output.
 //   SWIGLU  : two accumulators (gate rows f, up rows F+f) and an epilogue that writes
 //             bf16 silu(gate)*up for the down projection.
 //   LMSTATS : tokens on M (two 128-row tiles), 256 vocab rows on N; the epilogue keeps
 //             per (vocab tile, token) the max logit, its id and sum exp(z - max), so
 //             full-vocabulary logits never reach memory.
 //
-// Roles in a CTA of 192 threads: warp 0 = TMA producer, warp 1 = TMEM allocator and
-// MMA issuer, warps 2..5 = epilogue (each reads its 32 TMEM lanes).  All waits are
-// bounded (see common.cuh).
+// Weights and activations travel in two separate shared-memory rings: the weight ring
+// is deeper (weights come from HBM, activations from L2), so more weight bytes are in
+// flight per SM.  Roles in a CTA of 224 threads: warp 0 streams weights (before waiting
+// on the previous kernel, since weights never depend on it), warp 6 streams activations,
+// warp 1 allocates TMEM and issues the MMAs, warps 2..5 run the epilogue (each reads its
+// 32 TMEM lanes).  All waits are bounded (see common.cuh).
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -28,12 +32,13 @@ namespace lopa {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kMaxSmem = 227 * 1024;
+constexpr int kMaxStages = 8;
 
 struct SmemTail {
-  uint64_t full[8];
-  uint64_t empty[8];
+  uint64_t wfull[kMaxStages], wempty[kMaxStages];
+  uint64_t xfull[kMaxStages], xempty[kMaxStages];
   uint64_t accf;
   uint32_t tmem_addr;
   int abort;
@@ -46,10 +51,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  SmemTail* tail = reinterpret_cast<SmemTail*>(smem + (size_t)a.stages * a.stage_bytes);
+  uint8_t* wring = smem;
+  uint8_t* xring = smem + (size_t)a.w_stages * a.w_slot_bytes;
+  SmemTail* tail = reinterpret_cast<SmemTail*>(xring + (size_t)a.x_stages * a.x_slot_bytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int S = a.stages;
+  const int SW = a.w_stages, SX = a.x_stages;
+  // The weight operand is A (128-row tiles) except for the LM head, where it is B.
+  constexpr bool kWeightIsA = MODE != GEMM_LMSTATS;
 
   // Tile coordinates.
   int a_row[2];
@@ -77,11 +86,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb1 = (int)(((long long)(blockIdx.y + 1) * a.k_blocks) / a.splits);
   const int nk = kb1 - kb0;
   const uint32_t ncols = a.na == 2 ? 512u : 256u;
+  const uint32_t a_bytes = (a_ok[0] ? a.a_tile_bytes : 0u) + (a_ok[1] ? a.a_tile_bytes : 0u);
+  const uint32_t b_bytes = a.nbox * 128u;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&tail->full[s]), 1);
-      mbar_init(smem_u32(&tail->empty[s]), 1);
+    for (int s = 0; s < SW; ++s) {
+      mbar_init(smem_u32(&tail->wfull[s]), 1);
+      mbar_init(smem_u32(&tail->wempty[s]), 1);
+    }
+    for (int s = 0; s < SX; ++s) {
+      mbar_init(smem_u32(&tail->xfull[s]), 1);
+      mbar_init(smem_u32(&tail->xempty[s]), 1);
     }
     mbar_init(smem_u32(&tail->accf), 1);
     tail->abort = 0;
@@ -98,29 +113,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tail->tmem_addr;
   volatile int* abort = &tail->abort;
+  pdl_trigger();
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 6) {
+    // Producers: warp 0 streams the weight operand, warp 6 the activation operand.
+    const bool weights = warp == 0;
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_x = policy_evict_last();
-      // Weights are streamed once per forward; activations are re-read by every CTA.
-      const uint64_t pol_a = (MODE == GEMM_LMSTATS) ? pol_x : pol_w;
-      const uint64_t pol_b = (MODE == GEMM_LMSTATS) ? pol_w : pol_x;
-      const uint32_t bytes =
-          (a_ok[0] ? a.a_tile_bytes : 0u) + (a_ok[1] ? a.a_tile_bytes : 0u) + a.nbox * 128u;
+      if (!weights) pdl_wait();  // activations are written by the previous kernel
+      const int S = weights ? SW : SX;
+      uint8_t* ring = weights ? wring : xring;
+      const uint32_t slot = weights ? a.w_slot_bytes : a.x_slot_bytes;
+      uint64_t* full = weights ? tail->wfull : tail->xfull;
+      uint64_t* empty = weights ? tail->wempty : tail->xempty;
+      const bool is_a = weights == kWeightIsA;
+      const uint64_t pol = weights ? policy_evict_first() : policy_evict_last();
+      const uint32_t bytes = is_a ? a_bytes : b_bytes;
       for (int it = 0; it < nk; ++it) {
         const int s = it % S;
-        const uint32_t ph = (uint32_t)(it / S) & 1u;
-        if (it >= S &&
-            !mbar_wait_bounded(smem_u32(&tail->empty[s]), ph ^ 1u, abort, a.err, DEV_TIMEOUT_PRODUCER))
+        if (it >= S && !mbar_wait_bounded(smem_u32(&empty[s]), ((uint32_t)(it / S) & 1u) ^ 1u,
+                                          abort, a.err, DEV_TIMEOUT_PRODUCER))
           break;
-        uint8_t* st = smem + (size_t)s * a.stage_bytes;
-        const uint32_t full = smem_u32(&tail->full[s]);
-        mbar_arrive_expect_tx(full, bytes);
+        const uint32_t fb = smem_u32(&full[s]);
+        const uint32_t dst = smem_u32(ring + (size_t)s * slot);
         const int kx = (kb0 + it) * 64;
-        if (a_ok[0]) tma_load_2d(smem_u32(st), &mapA, full, kx, a_row[0], pol_a);
-        if (a_ok[1]) tma_load_2d(smem_u32(st + a.a_tile_bytes), &mapA, full, kx, a_row[1], pol_a);
-        tma_load_2d(smem_u32(st + 2 * a.a_tile_bytes), &mapB, full, kx, b_row, pol_b);
+        mbar_arrive_expect_tx(fb, bytes);
+        if (is_a) {
+          if (a_ok[0]) tma_load_2d(dst, &mapA, fb, kx, a_row[0], pol);
+          if (a_ok[1]) tma_load_2d(dst + a.a_tile_bytes, &mapA, fb, kx, a_row[1], pol);
+        } else {
+          tma_load_2d(dst, &mapB, fb, kx, b_row, pol);
+        }
       }
     }
   } else if (warp == 1) {
@@ -128,31 +150,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_bf16(128, a.nbox);
       bool ok = true;
       for (int it = 0; it < nk; ++it) {
-        const int s = it % S;
-        const uint32_t ph = (uint32_t)(it / S) & 1u;
-        if (!mbar_wait_bounded(smem_u32(&tail->full[s]), ph, abort, a.err, DEV_TIMEOUT_MMA)) {
+        const int sw = it % SW, sx = it % SX;
+        if (!mbar_wait_bounded(smem_u32(&tail->wfull[sw]), (uint32_t)(it / SW) & 1u, abort, a.err,
+                               DEV_TIMEOUT_MMA) ||
+            !mbar_wait_bounded(smem_u32(&tail->xfull[sx]), (uint32_t)(it / SX) & 1u, abort, a.err,
+                               DEV_TIMEOUT_MMA)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t st = smem_u32(smem + (size_t)s * a.stage_bytes);
-        const uint64_t bdesc = sw128_desc(st + 2 * a.a_tile_bytes);
+        const uint32_t ws = smem_u32(wring + (size_t)sw * a.w_slot_bytes);
+        const uint32_t xs = smem_u32(xring + (size_t)sx * a.x_slot_bytes);
+        const uint32_t abase = kWeightIsA ? ws : xs;
+        const uint64_t bdesc = sw128_desc(kWeightIsA ? xs : ws);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             if (!a_ok[i]) continue;
-            const uint64_t adesc = sw128_desc(st + i * a.a_tile_bytes);
+            const uint64_t adesc = sw128_desc(abase + i * a.a_tile_bytes);
             mma_bf16(tmem + (uint32_t)(i * 256), adesc + 2 * kk, bdesc + 2 * kk, idesc,
                      (it | kk) != 0);
           }
         }
-        mma_commit(smem_u32(&tail->empty[s]));
+        mma_commit(smem_u32(&tail->wempty[sw]));
+        mma_commit(smem_u32(&tail->xempty[sx]));
       }
       if (ok) mma_commit(smem_u32(&tail->accf));
     }
   } else {
-    // Epilogue warps 2..5: warp w may only touch TMEM lanes 32*(w%4) .. +31.
+    // Epilogue warps 2..5: warp w may only touch TMEM lanes 32*(w%4) .. +31.  The
+    // outputs may still be read by the previous kernel until it completes.
+    pdl_wait();
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
@@ -165,10 +194,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < a.nbox; c += 16) {
             float v[16];
             tmem_ld16(lane_base + (uint32_t)(i * 256 + c), v);
+            if (a.atomic) {
+              for (int j = 0; j < 16; ++j) {
+                const int t = b_row + c + j;
+                if (t < a.T) atomicAdd(a.out_f32 + (size_t)t * a.ldo + n, v[j]);
+              }
+            } else {
+              // Plain stores of this split's partial sums; a warp writes 128 contiguous
+              // bytes per token.  The consumer kernel adds the splits in a fixed order.
+              float* base = a.out_f32 + (size_t)blockIdx.y * a.split_stride + n;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int t = b_row + c + j;
-              if (t < a.T) atomicAdd(a.out_f32 + (size_t)t * a.ldo + n, v[j]);
+              for (int j = 0; j < 16; ++j) {
+                const int t = b_row + c + j;
+                if (t < a.T) base[(size_t)t * a.ldo] = v[j];
+              }
             }
           }
         }
@@ -251,6 +290,8 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+uint32_t round1k(uint32_t v) { return (v + 1023) & ~1023u; }
+
 }  // namespace
 
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
@@ -314,6 +355,8 @@ const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_all
     if (!make_tmap_bf16(&L->mapA, act, act_rows_alloc, K, 128, err, sizeof(err))) return err;
     if (!make_tmap_bf16(&L->mapB, w, n_rows_w, K, 256, err, sizeof(err))) return err;
     L->grid = dim3((n_rows_w + 255) / 256, 1, (T + na * 128 - 1) / (na * 128));
+    a.w_slot_bytes = round1k(a.nbox * 128);
+    a.x_slot_bytes = round1k(a.na * a.a_tile_bytes);
   } else {
     if (tok_box < 16 || tok_box > 256 || tok_box % 16 != 0) return "token box must be 16..256, multiple of 16";
     if (n_rows_w % 128 != 0) return "GEMM N must be a multiple of 128";
@@ -328,31 +371,34 @@ const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_all
     if (!make_tmap_bf16(&L->mapB, act, act_rows_alloc, K, tok_box, err, sizeof(err))) return err;
     const int gx = (mode == GEMM_SWIGLU) ? (n_rows_w / 2) / 128 : (n_rows_w + a.na * 128 - 1) / (a.na * 128);
     L->grid = dim3(gx, a.splits, (T + tok_box - 1) / tok_box);
+    a.w_slot_bytes = round1k(a.na * a.a_tile_bytes);
+    a.x_slot_bytes = round1k(a.nbox * 128);
   }
   (void)num_sms;
-  a.stage_bytes = (uint32_t)(2 * a.a_tile_bytes + a.nbox * 128);
-  a.stage_bytes = (a.stage_bytes + 1023) & ~1023u;
-  const int avail = kMaxSmem - 1024 - (int)sizeof(SmemTail) - 64;
-  a.stages = avail / (int)a.stage_bytes;
-  if (a.stages > 8) a.stages = 8;
-  if (a.stages < 2) return "GEMM tile does not fit in shared memory";
-  L->smem = 1024 + (size_t)a.stages * a.stage_bytes + sizeof(SmemTail) + 64;
+  // Activations come from L2 (short latency): 3 slots, more when they are small.  The
+  // weight ring takes the rest of shared memory.
+  const int budget = kMaxSmem - 1024 - (int)sizeof(SmemTail) - 64;
+  a.x_stages = a.x_slot_bytes <= 8192 ? 6 : 3;
+  a.w_stages = (budget - a.x_stages * (int)a.x_slot_bytes) / (int)a.w_slot_bytes;
+  if (a.w_stages > kMaxStages) a.w_stages = kMaxStages;
+  if (a.w_stages < 2) return "GEMM tile does not fit in shared memory";
+  L->smem = 1024 + (size_t)a.w_stages * a.w_slot_bytes + (size_t)a.x_stages * a.x_slot_bytes +
+            sizeof(SmemTail) + 64;
   return "";
 }
 
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   switch (L.args.mode) {
     case GEMM_RED_ADD:
-      gemm_kernel<GEMM_RED_ADD><<<L.grid, kThreads, L.smem, s>>>(L.mapA, L.mapB, L.args);
-      break;
+      return launch_pdl(gemm_kernel<GEMM_RED_ADD>, L.grid, dim3(kThreads), L.smem, s, L.mapA,
+                        L.mapB, L.args);
     case GEMM_SWIGLU:
-      gemm_kernel<GEMM_SWIGLU><<<L.grid, kThreads, L.smem, s>>>(L.mapA, L.mapB, L.args);
-      break;
+      return launch_pdl(gemm_kernel<GEMM_SWIGLU>, L.grid, dim3(kThreads), L.smem, s, L.mapA,
+                        L.mapB, L.args);
     default:
-      gemm_kernel<GEMM_LMSTATS><<<L.grid, kThreads, L.smem, s>>>(L.mapA, L.mapB, L.args);
-      break;
+      return launch_pdl(gemm_kernel<GEMM_LMSTATS>, L.grid, dim3(kThreads), L.smem, s, L.mapA,
+                        L.mapB, L.args);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace lopa

@@ -12,6 +12,26 @@ namespace lopa {
 
 typedef __nv_bfloat16 bf16;
 
+// Launches `kern` with programmatic stream serialization (the kernels call pdl_wait
+// before reading their predecessor's outputs).
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ GEMM (tcgen05)
 enum GemmMode : int {
   GEMM_RED_ADD = 0,  // out_f32[t][n] += sum_k act[t][k] * w[n][k]   (weights on M, tokens on N)
@@ -26,13 +46,15 @@ struct GemmArgs {
   int a_rows;        // rows of the A tensor (tiles at or beyond are skipped)
   int k_blocks;      // K / 64
   int splits;        // split-K factor (grid.y)
-  int stages;        // smem pipeline depth
-  uint32_t a_tile_bytes, stage_bytes;
+  int w_stages, x_stages;  // depth of the weight and activation smem rings
+  uint32_t a_tile_bytes, w_slot_bytes, x_slot_bytes;
   int T;             // valid token rows
   int F;             // SWIGLU: row offset of the up half in [2F][K]
   int V, mask_id;    // LMSTATS
   float scale;       // LMSTATS logit scale
   float* out_f32;    int ldo;
+  int atomic;        // RED_ADD: 1 = atomicAdd into out_f32, 0 = store partial of split y
+  size_t split_stride;  // RED_ADD partials: elements between splits
   bf16* out_bf16;    int ldh;
   float* part_m; float* part_s; int* part_i; int part_ld;
   int* err;
@@ -71,16 +93,18 @@ struct AttnArgs {
   int Bq, Bk, Bk_stride, nbq, H, Hk;
 };
 cudaError_t launch_attention(const AttnArgs& a, int dh, cudaStream_t s);
+cudaError_t attention_set_smem_limits();
 
 // ------------------------------------------------------------------ pointwise
 cudaError_t launch_embed_norm(const int* tok, int T, const bf16* E, const bf16* g, float* x,
                               bf16* n, int d, float eps, cudaStream_t s);
-cudaError_t launch_rmsnorm(const float* x, const bf16* g, bf16* n, int T, int d, float eps,
-                           cudaStream_t s);
-cudaError_t launch_rope_prewrite(float* qkv, int T, int H, int Hk, int dh, bf16* q,
-                                 bf16* kdst, bf16* vdst, int kv_to_cache, int Bq,
-                                 const float* cos_t, const float* sin_t, const int* dP,
-                                 cudaStream_t s);
+cudaError_t launch_rope_prewrite(const float* qkv, int nsplit, size_t split_stride, int T, int H,
+                                 int Hk, int dh, bf16* q, bf16* kdst, bf16* vdst,
+                                 int kv_to_cache, int Bq, const float* cos_t, const float* sin_t,
+                                 const int* dP, cudaStream_t s);
+// x[t] += sum over splits of part[s][t]; n[t] = bf16(rmsnorm(x[t]) * g).
+cudaError_t launch_residual_norm(float* x, const float* part, int nsplit, size_t split_stride,
+                                 const bf16* g, bf16* n, int T, int d, float eps, cudaStream_t s);
 cudaError_t launch_lm_merge(const float* pm, const float* ps, const int* pi, int nvt,
                             int part_ld, int T, int* am, float* mp, cudaStream_t s);
 cudaError_t launch_rope_table(float* cos_t, float* sin_t, int S, int dh, double base,

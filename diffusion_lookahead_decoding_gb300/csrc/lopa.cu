@@ -28,6 +28,18 @@ namespace {
 
 thread_local std::string g_init_error;
 
+}  // namespace
+
+namespace lopa {
+// Programmatic dependent launch is on unless LOPA_NO_PDL is set (a debugging switch).
+bool pdl_enabled() {
+  static const bool on = getenv("LOPA_NO_PDL") == nullptr;
+  return on;
+}
+}  // namespace lopa
+
+namespace {
+
 struct Plan {
   int nb = 0, Bq = 0, T = 0, tok_box = 0, kv_to_cache = 0;
   bool lm = false;
@@ -54,7 +66,8 @@ struct lopa_ctx {
   bf16 *kc = nullptr, *vc = nullptr, *ks = nullptr, *vs = nullptr;
   float* x = nullptr;
   bf16* n = nullptr;
-  float* qkv = nullptr;
+  float* part = nullptr;  // split-K partial sums [split][T][N] of the projections
+  size_t part_floats = 0;
   bf16 *q = nullptr, *attn = nullptr, *hm = nullptr;
   float *pm = nullptr, *ps = nullptr;
   int* pi = nullptr;
@@ -124,6 +137,31 @@ int pick_splits(int tiles, int k_blocks, int num_sms) {
   return std::max(s, 1);
 }
 
+// Weight tiles per CTA and split count of a projection over T token rows.
+void proj_tiling(int nrows, int K, int T, int num_sms, int* na, int* splits) {
+  const int tok_box = std::min(256, round16(T));
+  const int zt = (T + tok_box - 1) / tok_box;
+  *na = nrows >= 256 ? 2 : 1;
+  const int tiles = ((nrows + *na * 128 - 1) / (*na * 128)) * zt;
+  *splits = pick_splits(tiles, K / 64, num_sms);
+}
+
+// Floats of split-K partials a forward over T rows needs.
+size_t partial_floats(const lopa_ctx* ctx, int T);
+
+size_t partial_floats(const lopa_ctx* ctx, int T) {
+  const lopa_model_config& m = ctx->mc;
+  const int rows[3] = {ctx->qkv_rows, m.d_model, m.d_model};
+  const int Ks[3] = {m.d_model, m.n_heads * m.head_dim, m.ffn};
+  size_t need = 0;
+  for (int i = 0; i < 3; ++i) {
+    int na, splits;
+    proj_tiling(rows[i], Ks[i], T, ctx->num_sms, &na, &splits);
+    need = std::max(need, (size_t)splits * T * rows[i]);
+  }
+  return need;
+}
+
 int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm, const int* tok,
                int* am_out, float* mp_out) {
   const lopa_model_config& m = ctx->mc;
@@ -142,31 +180,36 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
   p.gu.resize(L);
   p.dn.resize(L);
   const int zt = (p.T + p.tok_box - 1) / p.tok_box;
+  (void)zt;
   auto plan = [&](GemmLaunch& G, int mode, const void* act, int K, const void* w, int nrows,
                   const char* what) -> int {
-    int na = (mode == GEMM_RED_ADD && nrows >= 256) ? 2 : 1;
-    const int tiles = ((nrows + na * 128 - 1) / (na * 128)) * zt;
-    const int splits = mode == GEMM_RED_ADD ? pick_splits(tiles, K / 64, ctx->num_sms) : 1;
+    int na = 1, splits = 1;
+    if (mode == GEMM_RED_ADD) {
+      proj_tiling(nrows, K, p.T, ctx->num_sms, &na, &splits);
+      while (splits > 1 && (size_t)splits * p.T * nrows > ctx->part_floats) --splits;
+    }
     const char* e = plan_gemm(&G, mode, act, ctx->Tmax, p.T, w, nrows, K, na, splits, p.tok_box,
                               ctx->num_sms);
     if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s GEMM: %s", what, e);
+    if (mode == GEMM_RED_ADD) {
+      if ((size_t)G.args.splits * p.T * nrows > ctx->part_floats)
+        return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s GEMM: partial buffer too small", what);
+      G.args.out_f32 = ctx->part;
+      G.args.ldo = nrows;
+      G.args.atomic = 0;
+      G.args.split_stride = (size_t)p.T * nrows;
+    }
     G.args.err = &ctx->st->err;
     return 0;
   };
   for (int l = 0; l < L; ++l) {
     int r;
     if ((r = plan(p.qkv[l], GEMM_RED_ADD, ctx->n, d, ctx->wqkv[l], ctx->qkv_rows, "qkv"))) return r;
-    p.qkv[l].args.out_f32 = ctx->qkv;
-    p.qkv[l].args.ldo = ctx->qkv_rows;
     if ((r = plan(p.o[l], GEMM_RED_ADD, ctx->attn, H * dh, ctx->wo[l], d, "o"))) return r;
-    p.o[l].args.out_f32 = ctx->x;
-    p.o[l].args.ldo = d;
     if ((r = plan(p.gu[l], GEMM_SWIGLU, ctx->n, d, ctx->wgu[l], 2 * F, "gate/up"))) return r;
     p.gu[l].args.out_bf16 = ctx->hm;
     p.gu[l].args.ldh = F;
     if ((r = plan(p.dn[l], GEMM_RED_ADD, ctx->hm, F, ctx->wd[l], d, "down"))) return r;
-    p.dn[l].args.out_f32 = ctx->x;
-    p.dn[l].args.ldo = d;
   }
   if (lm) {
     const int na = p.T > 128 ? 2 : 1;
@@ -198,7 +241,8 @@ int enqueue_forward(lopa_ctx* ctx, const Plan& p) {
     bf16* ksl = ctx->ks + (size_t)l * ctx->scr_layer;
     bf16* vsl = ctx->vs + (size_t)l * ctx->scr_layer;
     CK(launch_gemm(p.qkv[l], s));
-    CK(launch_rope_prewrite(ctx->qkv, p.T, H, Hk, dh, ctx->q, p.kv_to_cache ? kcl : ksl,
+    CK(launch_rope_prewrite(ctx->part, p.qkv[l].args.splits, p.qkv[l].args.split_stride, p.T, H,
+                            Hk, dh, ctx->q, p.kv_to_cache ? kcl : ksl,
                             p.kv_to_cache ? vcl : vsl, p.kv_to_cache, p.Bq, ctx->cos_t, ctx->sin_t,
                             &ctx->st->P, s));
     AttnArgs aa;
@@ -218,11 +262,13 @@ int enqueue_forward(lopa_ctx* ctx, const Plan& p) {
     aa.Hk = Hk;
     CK(launch_attention(aa, dh, s));
     CK(launch_gemm(p.o[l], s));
-    CK(launch_rmsnorm(ctx->x, ctx->mlp_norm[l], ctx->n, p.T, d, m.rms_eps, s));
+    CK(launch_residual_norm(ctx->x, ctx->part, p.o[l].args.splits, p.o[l].args.split_stride,
+                            ctx->mlp_norm[l], ctx->n, p.T, d, m.rms_eps, s));
     CK(launch_gemm(p.gu[l], s));
     CK(launch_gemm(p.dn[l], s));
-    CK(launch_rmsnorm(ctx->x, l + 1 < L ? ctx->attn_norm[l + 1] : ctx->final_norm, ctx->n, p.T, d,
-                      m.rms_eps, s));
+    CK(launch_residual_norm(ctx->x, ctx->part, p.dn[l].args.splits, p.dn[l].args.split_stride,
+                            l + 1 < L ? ctx->attn_norm[l + 1] : ctx->final_norm, ctx->n, p.T, d,
+                            m.rms_eps, s));
   }
   if (p.lm) {
     CK(launch_gemm(p.lmh, s));
@@ -308,6 +354,7 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
   CK(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
   if (major != 10) return fail(ctx, LOPA_ERR_UNSUPPORTED, "needs an sm_10x GPU (found sm_%d%d)", major, minor);
   CK(gemm_set_smem_limits());
+  CK(attention_set_smem_limits());
   if (!ctx->stream) {
     CK(cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking));
     ctx->own_stream = true;
@@ -338,12 +385,14 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
   ctx->scr_layer = (size_t)ctx->nbmax * B * Hk * dh;
   ctx->nvt = (V + 255) / 256;
   ctx->part_ld = ctx->nbmax * B;
+  ctx->part_floats = std::max(partial_floats(ctx, ctx->nbmax * B),
+                              std::max(partial_floats(ctx, B), partial_floats(ctx, ctx->dc.max_prompt)));
   const size_t T = ctx->Tmax;
   int r;
   if ((r = dalloc(ctx, &ctx->kc, ctx->cache_layer * L)) || (r = dalloc(ctx, &ctx->vc, ctx->cache_layer * L)) ||
       (r = dalloc(ctx, &ctx->ks, ctx->scr_layer * L)) || (r = dalloc(ctx, &ctx->vs, ctx->scr_layer * L)) ||
       (r = dalloc(ctx, &ctx->x, T * d)) || (r = dalloc(ctx, &ctx->n, T * d)) ||
-      (r = dalloc(ctx, &ctx->qkv, T * ctx->qkv_rows)) || (r = dalloc(ctx, &ctx->q, T * H * dh)) ||
+      (r = dalloc(ctx, &ctx->part, ctx->part_floats)) || (r = dalloc(ctx, &ctx->q, T * H * dh)) ||
       (r = dalloc(ctx, &ctx->attn, T * H * dh)) || (r = dalloc(ctx, &ctx->hm, T * F)) ||
       (r = dalloc(ctx, &ctx->pm, (size_t)ctx->nvt * ctx->part_ld)) ||
       (r = dalloc(ctx, &ctx->ps, (size_t)ctx->nvt * ctx->part_ld)) ||
@@ -358,7 +407,6 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
       (r = dalloc(ctx, &ctx->st, 1)))
     return r;
   cudaStream_t s = ctx->stream;
-  CK(cudaMemsetAsync(ctx->qkv, 0, T * ctx->qkv_rows * sizeof(float), s));
   CK(cudaMemsetAsync(ctx->kc, 0, ctx->cache_layer * L * sizeof(bf16), s));
   CK(cudaMemsetAsync(ctx->vc, 0, ctx->cache_layer * L * sizeof(bf16), s));
   CK(cudaMemsetAsync(ctx->st, 0, sizeof(DevState), s));
@@ -551,8 +599,6 @@ int lopa_time_gemm(lopa_ctx* ctx, int kind, int iters, float* avg_ms) {
   float ms = 0.f;
   CK(cudaEventElapsedTime(&ms, ctx->ev0, ctx->ev1));
   *avg_ms = ms / iters;
-  // The q/k/v accumulator must start at zero for the next forward.
-  CK(cudaMemsetAsync(ctx->qkv, 0, (size_t)ctx->Tmax * ctx->qkv_rows * sizeof(float), s));
   return check_device_error(ctx);
 }
 
@@ -626,6 +672,20 @@ int lopa_read_kv(lopa_ctx* ctx, int layer, int pos0, int n, uint16_t* k, uint16_
   return 0;
 }
 
+int lopa_read_branch_kv(lopa_ctx* ctx, int layer, int branch, uint16_t* k, uint16_t* v) {
+  if (!ctx) return fail(nullptr, LOPA_ERR_INVALID_ARG, "ctx is null");
+  if (layer < 0 || layer >= ctx->mc.n_layers || branch < 0 || branch >= ctx->nbmax)
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "layer/branch out of range");
+  const size_t row = (size_t)ctx->mc.n_kv_heads * ctx->mc.head_dim;
+  const size_t n = (size_t)ctx->dc.block * row;
+  const size_t off = (size_t)layer * ctx->scr_layer + (size_t)branch * n;
+  cudaStream_t s = ctx->stream;
+  if (k) CK(cudaMemcpyAsync(k, ctx->ks + off, n * 2, cudaMemcpyDeviceToHost, s));
+  if (v) CK(cudaMemcpyAsync(v, ctx->vs + off, n * 2, cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  return 0;
+}
+
 // ---------------------------------------------------------------- kernel-level calls
 
 int lopa_linear_accumulate(const void* x, const void* w, float* y, int T, int N, int K, void* stream) {
@@ -646,6 +706,7 @@ int lopa_linear_accumulate(const void* x, const void* w, float* y, int T, int N,
   if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s", e);
   G.args.out_f32 = y;
   G.args.ldo = N;
+  G.args.atomic = 1;
   CK(launch_gemm(G, static_cast<cudaStream_t>(stream)));
   return 0;
 }
@@ -716,6 +777,7 @@ int lopa_branch_attention(const void* q, const void* k_prefix, const void* v_pre
   a.nbq = n_branches;
   a.H = n_heads;
   a.Hk = n_kv_heads;
+  CK(attention_set_smem_limits());
   CK(launch_attention(a, head_dim, static_cast<cudaStream_t>(stream)));
   return 0;
 }

@@ -30,6 +30,8 @@ __device__ __forceinline__ void store8(bf16* p, const float (&f)[8]) {
 __global__ void embed_norm_kernel(const int* __restrict__ tok, int T, const bf16* __restrict__ E,
                                   const bf16* __restrict__ g, float* __restrict__ x,
                                   bf16* __restrict__ n, int d, float eps) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -56,78 +58,150 @@ __global__ void embed_norm_kernel(const int* __restrict__ tok, int T, const bf16
   }
 }
 
-// n[t] = bf16(rmsnorm(x[t]) * g).  One warp per row.
-__global__ void rmsnorm_kernel(const float* __restrict__ x, const bf16* __restrict__ g,
-                               bf16* __restrict__ n, int T, int d, float eps) {
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
-  const float* xr = x + (size_t)t * d;
-  float ss = 0.f;
-  for (int c = lane * 8; c < d; c += 256) {
-    const float4 a = *reinterpret_cast<const float4*>(xr + c);
-    const float4 b = *reinterpret_cast<const float4*>(xr + c + 4);
-    ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z +
-          b.w * b.w;
-  }
-  ss = warp_sum(ss);
-  const float rs = rsqrtf(ss / (float)d + eps);
-  for (int c = lane * 8; c < d; c += 256) {
-    const float4 a = *reinterpret_cast<const float4*>(xr + c);
-    const float4 b = *reinterpret_cast<const float4*>(xr + c + 4);
-    float gg[8];
-    load8(g + c, gg);
-    float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+// Sums 4 consecutive floats over the split-K partials (independent 16-byte loads).
+__device__ __forceinline__ float4 sum_splits4(const float* p, int nsplit, size_t stride) {
+  float4 a = *reinterpret_cast<const float4*>(p);
+  int s = 1;
+  for (; s + 4 <= nsplit; s += 4) {
+    float4 q[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) f[i] = f[i] * rs * gg[i];
-    store8(n + (size_t)t * d + c, f);
+    for (int u = 0; u < 4; ++u) q[u] = *reinterpret_cast<const float4*>(p + (size_t)(s + u) * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) { a.x += q[u].x; a.y += q[u].y; a.z += q[u].z; a.w += q[u].w; }
   }
+  for (; s < nsplit; ++s) {
+    const float4 q = *reinterpret_cast<const float4*>(p + (size_t)s * stride);
+    a.x += q.x; a.y += q.y; a.z += q.z; a.w += q.w;
+  }
+  return a;
 }
 
-// Applies RoPE (rotate-half) to q and k of one token row, rounds q/k/v to bf16, writes q
-// to [T][H][dh] and k/v to their Pre-Write destination, and re-zeroes the fp32 q/k/v
-// accumulator row for the next layer.  Row t is position i = t % Bq of branch b = t / Bq
-// at absolute position P + i.  K/V go to the branch scratch [b][i] or, when
-// kv_to_cache, straight to the static cache row P + i (prompt prefill).
-__global__ void rope_prewrite_kernel(float* __restrict__ qkv, int T, int H, int Hk, int dh,
-                                     bf16* __restrict__ q, bf16* __restrict__ kdst,
-                                     bf16* __restrict__ vdst, int kv_to_cache, int Bq,
-                                     const float* __restrict__ cos_t,
+__device__ __forceinline__ void store4_bf16(bf16* p, float a, float b, float c, float d) {
+  uint2 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+  h[0] = __floats2bfloat162_rn(a, b);
+  h[1] = __floats2bfloat162_rn(c, d);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+// Sums the q/k/v split-K partials of one token row, applies RoPE (rotate-half) to q and
+// k, rounds q/k/v to bf16, writes q to [T][H][dh] and k/v to their Pre-Write destination.
+// Row t is position i = t % Bq of branch b = t / Bq at absolute position P + i.  K/V go
+// to the branch scratch [b][i] or, when kv_to_cache, straight to the static cache row
+// P + i (prompt prefill).  One CTA per row; a work item is 4 consecutive elements of a
+// head (j..j+3 with their rotation partners j+dh/2..+3).
+__global__ void rope_prewrite_kernel(const float* __restrict__ qkv, int nsplit, size_t split_stride,
+                                     int T, int H, int Hk, int dh, bf16* __restrict__ q,
+                                     bf16* __restrict__ kdst, bf16* __restrict__ vdst,
+                                     int kv_to_cache, int Bq, const float* __restrict__ cos_t,
                                      const float* __restrict__ sin_t, const int* __restrict__ dP) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   if (t >= T) return;
   const int P = dP ? *dP : 0;
   const int b = t / Bq, i = t - b * Bq;
   const int pos = P + i;
-  const int half = dh / 2;
-  const int nqk = (H + Hk) * half;   // rotation pairs in q and k
-  const int nv = Hk * dh;
+  const int half = dh / 2, hq = half / 4;
+  const int nqk = (H + Hk) * hq;  // 4-wide rotation items in q and k
+  const int nv = Hk * dh / 4;
   const int row_w = (H + 2 * Hk) * dh;
-  float* row = qkv + (size_t)t * row_w;
+  const float* row = qkv + (size_t)t * row_w;
   const size_t kv_row = kv_to_cache ? (size_t)(P + i) : (size_t)t;
-  for (int e = threadIdx.x; e < nqk; e += blockDim.x) {
-    const int head = e / half, j = e - head * half;
-    float* src = row + head * dh;
-    const float x1 = src[j], x2 = src[j + half];
-    const float c = cos_t[(size_t)pos * half + j], s = sin_t[(size_t)pos * half + j];
-    const float y1 = x1 * c - x2 * s, y2 = x2 * c + x1 * s;
-    if (head < H) {
-      bf16* qd = q + ((size_t)t * H + head) * dh;
-      qd[j] = __float2bfloat16_rn(y1);
-      qd[j + half] = __float2bfloat16_rn(y2);
+  const float* ct = cos_t + (size_t)pos * half;
+  const float* st = sin_t + (size_t)pos * half;
+  for (int e = threadIdx.x; e < nqk + nv; e += blockDim.x) {
+    if (e < nqk) {
+      const int head = e / hq, j = (e - head * hq) * 4;
+      const float* src = row + head * dh;
+      const float4 x1 = sum_splits4(src + j, nsplit, split_stride);
+      const float4 x2 = sum_splits4(src + j + half, nsplit, split_stride);
+      const float4 c = *reinterpret_cast<const float4*>(ct + j);
+      const float4 sn = *reinterpret_cast<const float4*>(st + j);
+      bf16* dst = head < H ? q + ((size_t)t * H + head) * dh
+                           : kdst + (kv_row * Hk + (head - H)) * dh;
+      store4_bf16(dst + j, x1.x * c.x - x2.x * sn.x, x1.y * c.y - x2.y * sn.y,
+                  x1.z * c.z - x2.z * sn.z, x1.w * c.w - x2.w * sn.w);
+      store4_bf16(dst + j + half, x2.x * c.x + x1.x * sn.x, x2.y * c.y + x1.y * sn.y,
+                  x2.z * c.z + x1.z * sn.z, x2.w * c.w + x1.w * sn.w);
     } else {
-      bf16* kd = kdst + (kv_row * Hk + (head - H)) * dh;
-      kd[j] = __float2bfloat16_rn(y1);
-      kd[j + half] = __float2bfloat16_rn(y2);
+      const int e4 = (e - nqk) * 4;
+      const float4 v = sum_splits4(row + (H + Hk) * dh + e4, nsplit, split_stride);
+      store4_bf16(vdst + kv_row * Hk * dh + e4, v.x, v.y, v.z, v.w);
     }
-    src[j] = 0.f;
-    src[j + half] = 0.f;
   }
-  for (int e = threadIdx.x; e < nv; e += blockDim.x) {
-    float* src = row + (H + Hk) * dh + e;
-    vdst[kv_row * Hk * dh + e] = __float2bfloat16_rn(*src);
-    *src = 0.f;
+  __syncthreads();
+  if (row_w % 32 == 0) discard_partial_row(row, split_stride, nsplit, row_w);
+}
+
+// Block-wide sum; every thread gets the total.  blockDim.x is a multiple of 32, <= 1024.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = lane < nw ? red[lane] : 0.f;
+  t = warp_sum(t);
+  return t;
+}
+
+// x[t] += sum_s part[s][t] (splits added in order), then n[t] = bf16(rmsnorm(x[t]) * g).
+// One CTA per row, one 8-element chunk per thread; the split loads are independent
+// 16-byte loads so that many are in flight per thread.
+__global__ void residual_norm_kernel(float* __restrict__ x, const float* __restrict__ part,
+                                     int nsplit, size_t split_stride, const bf16* __restrict__ g,
+                                     bf16* __restrict__ n, int T, int d, float eps) {
+  __shared__ float red[32];
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x;
+  const int c = threadIdx.x * 8;
+  const bool active = c < d;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float* xr = x + (size_t)t * d + c;
+  if (active) {
+    const float4 a = *reinterpret_cast<const float4*>(xr);
+    const float4 b = *reinterpret_cast<const float4*>(xr + 4);
+    acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+    acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+    const float* pr = part + (size_t)t * d + c;
+    int s = 0;
+    for (; s + 4 <= nsplit; s += 4) {
+      float4 p[8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        p[2 * u] = *reinterpret_cast<const float4*>(pr + (size_t)(s + u) * split_stride);
+        p[2 * u + 1] = *reinterpret_cast<const float4*>(pr + (size_t)(s + u) * split_stride + 4);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc[0] += p[2 * u].x; acc[1] += p[2 * u].y; acc[2] += p[2 * u].z; acc[3] += p[2 * u].w;
+        acc[4] += p[2 * u + 1].x; acc[5] += p[2 * u + 1].y; acc[6] += p[2 * u + 1].z;
+        acc[7] += p[2 * u + 1].w;
+      }
+    }
+    for (; s < nsplit; ++s) {
+      const float4 p0 = *reinterpret_cast<const float4*>(pr + (size_t)s * split_stride);
+      const float4 p1 = *reinterpret_cast<const float4*>(pr + (size_t)s * split_stride + 4);
+      acc[0] += p0.x; acc[1] += p0.y; acc[2] += p0.z; acc[3] += p0.w;
+      acc[4] += p1.x; acc[5] += p1.y; acc[6] += p1.z; acc[7] += p1.w;
+    }
+    *reinterpret_cast<float4*>(xr) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(xr + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) ss += acc[e] * acc[e];
+  ss = block_sum(ss, red);  // also a barrier: every thread has read its partials
+  const float rs = rsqrtf(ss / (float)d + eps);
+  if (active) {
+    float gg[8], f[8];
+    load8(g + c, gg);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = acc[e] * rs * gg[e];
+    store8(n + (size_t)t * d + c, f);
+  }
+  if (d % 32 == 0) discard_partial_row(part + (size_t)t * d, split_stride, nsplit, d);
 }
 
 struct Stat {
@@ -151,6 +225,8 @@ __device__ __forceinline__ Stat merge(Stat a, Stat b) {
 __global__ void lm_merge_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
                                 const int* __restrict__ pi, int nvt, int part_ld, int T,
                                 int* __restrict__ am, float* __restrict__ mp) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -190,29 +266,30 @@ __global__ void rope_table_kernel(float* cos_t, float* sin_t, int S, int dh, dou
 
 cudaError_t launch_embed_norm(const int* tok, int T, const bf16* E, const bf16* g, float* x,
                               bf16* n, int d, float eps, cudaStream_t s) {
-  embed_norm_kernel<<<(T + 7) / 8, 256, 0, s>>>(tok, T, E, g, x, n, d, eps);
-  return cudaGetLastError();
+  return launch_pdl(embed_norm_kernel, dim3((T + 7) / 8), dim3(256), 0, s, tok, T, E, g, x, n, d,
+                    eps);
 }
 
-cudaError_t launch_rmsnorm(const float* x, const bf16* g, bf16* n, int T, int d, float eps,
-                           cudaStream_t s) {
-  rmsnorm_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, g, n, T, d, eps);
-  return cudaGetLastError();
+cudaError_t launch_rope_prewrite(const float* qkv, int nsplit, size_t split_stride, int T, int H,
+                                 int Hk, int dh, bf16* q, bf16* kdst, bf16* vdst,
+                                 int kv_to_cache, int Bq, const float* cos_t, const float* sin_t,
+                                 const int* dP, cudaStream_t s) {
+  return launch_pdl(rope_prewrite_kernel, dim3(T), dim3(256), 0, s, qkv, nsplit, split_stride, T,
+                    H, Hk, dh, q, kdst, vdst, kv_to_cache, Bq, cos_t, sin_t, dP);
 }
 
-cudaError_t launch_rope_prewrite(float* qkv, int T, int H, int Hk, int dh, bf16* q,
-                                 bf16* kdst, bf16* vdst, int kv_to_cache, int Bq,
-                                 const float* cos_t, const float* sin_t, const int* dP,
-                                 cudaStream_t s) {
-  rope_prewrite_kernel<<<T, 256, 0, s>>>(qkv, T, H, Hk, dh, q, kdst, vdst, kv_to_cache, Bq, cos_t,
-                                         sin_t, dP);
-  return cudaGetLastError();
+cudaError_t launch_residual_norm(float* x, const float* part, int nsplit, size_t split_stride,
+                                 const bf16* g, bf16* n, int T, int d, float eps, cudaStream_t s) {
+  const int threads = ((d / 8 + 31) / 32) * 32;
+  if (threads > 1024) return cudaErrorInvalidValue;
+  return launch_pdl(residual_norm_kernel, dim3(T), dim3(threads), 0, s, x, part, nsplit,
+                    split_stride, g, n, T, d, eps);
 }
 
 cudaError_t launch_lm_merge(const float* pm, const float* ps, const int* pi, int nvt,
                             int part_ld, int T, int* am, float* mp, cudaStream_t s) {
-  lm_merge_kernel<<<(T + 7) / 8, 256, 0, s>>>(pm, ps, pi, nvt, part_ld, T, am, mp);
-  return cudaGetLastError();
+  return launch_pdl(lm_merge_kernel, dim3((T + 7) / 8), dim3(256), 0, s, pm, ps, pi, nvt, part_ld,
+                    T, am, mp);
 }
 
 cudaError_t launch_rope_table(float* cos_t, float* sin_t, int S, int dh, double base,

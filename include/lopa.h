@@ -165,6 +165,10 @@ int lopa_verify_forward(lopa_ctx* ctx, const int32_t* branch_tok, int nb, int32_
  * [n][Hk][dh] each (either may be NULL). */
 int lopa_read_kv(lopa_ctx* ctx, int layer, int pos0, int n, uint16_t* k, uint16_t* v);
 
+/* Copies the Pre-Write scratch K and V of one branch (the block K/V its last
+ * verification forward produced) for layer to host as bf16 words [B][Hk][dh] each. */
+int lopa_read_branch_kv(lopa_ctx* ctx, int layer, int branch, uint16_t* k, uint16_t* v);
+
 /* ---- kernel-level entry points (device pointers, caller's stream) -------------- */
 
 /* y[T][N] += x[T][K] . w[N][K]^T with bf16 inputs and fp32 accumulation on the

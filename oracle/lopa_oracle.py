@@ -107,8 +107,12 @@ def silu(x):
     return x / (1.0 + np.exp(-x))
 
 
-def linear(x, W):
-    """x @ W^T for a weight stored [out_features, in_features]."""
+def linear(x, W, accum="fp64"):
+    """x @ W^T for a weight stored [out_features, in_features].  accum='fp32' forms the
+    same sum with float32 arithmetic; it exists only to measure how strongly the result
+    depends on the accumulation precision (the problem's conditioning)."""
+    if accum == "fp32":
+        return (np.asarray(x, dtype=np.float32) @ np.asarray(W, dtype=np.float32).T).astype(np.float64)
     return np.asarray(x, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T
 
 
@@ -164,10 +168,11 @@ class OracleModel:
     hidden) to bf16, as the workload's "bf16 weights/activations" states; arithmetic
     stays float64.  ``act='fp64'`` keeps everything float64."""
 
-    def __init__(self, shape, weights, act="bf16", cache_weights=None):
+    def __init__(self, shape, weights, act="bf16", cache_weights=None, accum="fp64"):
         self.shape = shape
         self._w = weights  # name -> torch bf16 CPU tensor or numpy array
         self.act = act
+        self.accum = accum
         self.rnd = bf16_round if act == "bf16" else _identity
         if cache_weights is None:
             cache_weights = shape.streamed_params() < 400_000_000
@@ -229,9 +234,10 @@ def forward(model, cache, P, branches, want_logits=False):
     block_k, block_v = [], []
     for l in range(sh.n_layers):
         n = rnd(rmsnorm(x, model.W(f"attn_norm.{l}"), sh.rms_eps))
-        q = linear(n, model.W(f"wq.{l}")).reshape(nb, B, H, dh)
-        k = linear(n, model.W(f"wk.{l}")).reshape(nb, B, Hk, dh)
-        v = linear(n, model.W(f"wv.{l}")).reshape(nb, B, Hk, dh)
+        lin = lambda a, name: linear(a, model.W(name), model.accum)
+        q = lin(n, f"wq.{l}").reshape(nb, B, H, dh)
+        k = lin(n, f"wk.{l}").reshape(nb, B, Hk, dh)
+        v = lin(n, f"wv.{l}").reshape(nb, B, Hk, dh)
         q = rnd(np.stack([rope(q[b], pos, sh.rope_base) for b in range(nb)]))
         k = rnd(np.stack([rope(k[b], pos, sh.rope_base) for b in range(nb)]))
         v = rnd(v)
@@ -239,12 +245,12 @@ def forward(model, cache, P, branches, want_logits=False):
         block_v.append(v)
         attn = isolated_attention(q, cache.k[l][:P], cache.v[l][:P], k, v)
         o = rnd(attn.reshape(nb, B, H * dh))
-        x = x + linear(o, model.W(f"wo.{l}"))
+        x = x + lin(o, f"wo.{l}")
         n2 = rnd(rmsnorm(x, model.W(f"mlp_norm.{l}"), sh.rms_eps))
-        hm = rnd(silu(linear(n2, model.W(f"wg.{l}"))) * linear(n2, model.W(f"wu.{l}")))
-        x = x + linear(hm, model.W(f"wd.{l}"))
+        hm = rnd(silu(lin(n2, f"wg.{l}")) * lin(n2, f"wu.{l}"))
+        x = x + lin(hm, f"wd.{l}")
     hf = rnd(rmsnorm(x, model.W("final_norm"), sh.rms_eps))
-    z = sh.logit_scale * linear(hf, model.W("lm_head"))
+    z = sh.logit_scale * linear(hf, model.W("lm_head"), model.accum)
     am, mp, p2 = logit_summary(z, sh.mask_id)
     out = ForwardOut(am, mp, p2, x, block_k, block_v)
     if want_logits:
