@@ -250,18 +250,27 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnArgs a) {
     l += __shfl_xor_sync(0xffffffffu, l, 2);
     lrow[h2] = 1.0f / l;
   }
+  // Stage the CTA's 64 x DH output tile in shared memory (behind the exchange area), then
+  // write whole rows with 16-byte stores.
+  bf16* ostage = reinterpret_cast<bf16*>(smem_raw + (size_t)4 * 32 * PER * sizeof(float));
 #pragma unroll
   for (int h2 = 0; h2 < 2; ++h2) {
-    const int r = row0 + grp + h2 * 8;
-    if (r >= rows) continue;
-    const int i = r / G, hg = r - i * G;
-    bf16* orow = a.out + ((size_t)(b * a.Bq + i) * a.H + g * G + hg) * DH;
+    const int rr = rw * 16 + grp + h2 * 8;
 #pragma unroll
     for (int j = 0; j < DH / 8; ++j) {
       const float v0 = (o[j][2 * h2] * sc0[h2] + mine[j * 4 + 2 * h2] * sc1[h2]) * lrow[h2];
       const float v1 = (o[j][2 * h2 + 1] * sc0[h2] + mine[j * 4 + 2 * h2 + 1] * sc1[h2]) * lrow[h2];
-      *reinterpret_cast<uint32_t*>(orow + j * 8 + 2 * tig) = pack_bf16(v0, v1);
+      *reinterpret_cast<uint32_t*>(ostage + rr * DH + j * 8 + 2 * tig) = pack_bf16(v0, v1);
     }
+  }
+  group_sync(0);
+  for (int c = gtid; c < kRowsPerCta * CH; c += 128) {
+    const int rr = c / CH, col = (c - rr * CH) * 8;
+    const int r = blockIdx.x * kRowsPerCta + rr;
+    if (r >= rows) continue;
+    const int i = r / G, hg = r - i * G;
+    bf16* orow = a.out + ((size_t)(b * a.Bq + i) * a.H + g * G + hg) * DH;
+    *reinterpret_cast<uint4*>(orow + col) = *reinterpret_cast<const uint4*>(ostage + rr * DH + col);
   }
 }
 
@@ -282,6 +291,18 @@ cudaError_t attention_set_smem_limits() {
     return e;
   return cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)attn_smem<128>());
+}
+
+cudaError_t attention_set_carveout() {
+  cudaError_t e;
+  const int c = cudaSharedmemCarveoutMaxShared;
+  if ((e = cudaFuncSetAttribute(attn_kernel<32>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                c)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                c)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributePreferredSharedMemoryCarveout, c);
 }
 
 cudaError_t launch_attention(const AttnArgs& a, int dh, cudaStream_t s) {

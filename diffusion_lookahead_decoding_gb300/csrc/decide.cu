@@ -193,6 +193,17 @@ __global__ void state_reset_kernel(DevState* st, int P, int B, int mask_id) {
 
 }  // namespace
 
+cudaError_t decide_set_carveout() {
+  const int c = cudaSharedmemCarveoutMaxShared;
+  const void* ks[] = {(const void*)decide_kernel, (const void*)select_kernel,
+                      (const void*)commit_kv_kernel, (const void*)finalize_kernel};
+  for (const void* k : ks) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, c);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_decide(void* st, int B, int k, float tau, int mask_id, int* branch_tok,
                           int* valid, cudaStream_t s) {
   return launch_pdl(decide_kernel, dim3(1), dim3(LOPA_MAX_BLOCK), 0, s, static_cast<DevState*>(st),

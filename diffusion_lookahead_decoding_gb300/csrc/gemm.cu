@@ -17,10 +17,11 @@
 //
 // Weights and activations travel in two separate shared-memory rings: the weight ring
 // is deeper (weights come from HBM, activations from L2), so more weight bytes are in
-// flight per SM.  Roles in a CTA of 224 threads: warp 0 streams weights (before waiting
-// on the previous kernel, since weights never depend on it), warp 6 streams activations,
-// warp 1 allocates TMEM and issues the MMAs, warps 2..5 run the epilogue (each reads its
-// 32 TMEM lanes).  All waits are bounded (see common.cuh).
+// flight per SM.  Roles in a CTA of 352 threads: warp 0 streams weights (before waiting
+// on the previous kernel, since weights never depend on it), warp 10 streams
+// activations, warp 1 allocates TMEM and issues the MMAs, warps 2..9 run the epilogue
+// (two warps per TMEM lane quarter, splitting the columns), staging output tiles in the
+// freed rings so global writes are whole-row 16-byte stores.  All waits are bounded.
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -32,9 +33,13 @@ namespace lopa {
 
 namespace {
 
-constexpr int kThreads = 224;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (3 + kEpiWarps) * 32;  // W producer, MMA, 8 epilogue warps, X producer
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kMaxStages = 8;
+
+// Barrier among the eight epilogue warps only (named barrier 3, 256 threads).
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
 
 struct SmemTail {
   uint64_t wfull[kMaxStages], wempty[kMaxStages];
@@ -115,8 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = &tail->abort;
   pdl_trigger();
 
-  if (warp == 0 || warp == 6) {
-    // Producers: warp 0 streams the weight operand, warp 6 the activation operand.
+  if (warp == 0 || warp == 2 + kEpiWarps) {
+    // Producers: warp 0 streams the weight operand, the last warp the activation operand.
     const bool weights = warp == 0;
     if (lane == 0) {
       if (!weights) pdl_wait();  // activations are written by the previous kernel
@@ -135,13 +140,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         const uint32_t fb = smem_u32(&full[s]);
         const uint32_t dst = smem_u32(ring + (size_t)s * slot);
-        const int kx = (kb0 + it) * 64;
+        const int kb = kb0 + it;
+        const bool packed = weights && a.w_packed;
+        // Row-major: (x = k offset, y = row).  Tile-major: tile (row / tile_rows, kb) is
+        // one contiguous box at y = (tile * k_blocks + kb) * tile_rows, x = 0.
+        const int kx = packed ? 0 : kb * 64;
         mbar_arrive_expect_tx(fb, bytes);
         if (is_a) {
-          if (a_ok[0]) tma_load_2d(dst, &mapA, fb, kx, a_row[0], pol);
-          if (a_ok[1]) tma_load_2d(dst + a.a_tile_bytes, &mapA, fb, kx, a_row[1], pol);
+          const int y0 = packed ? ((a_row[0] >> 7) * a.k_blocks + kb) * 128 : a_row[0];
+          const int y1 = packed ? ((a_row[1] >> 7) * a.k_blocks + kb) * 128 : a_row[1];
+          if (a_ok[0]) tma_load_2d(dst, &mapA, fb, kx, y0, pol);
+          if (a_ok[1]) tma_load_2d(dst + a.a_tile_bytes, &mapA, fb, kx, y1, pol);
         } else {
-          tma_load_2d(dst, &mapB, fb, kx, b_row, pol);
+          const int y = packed ? ((b_row / a.nbox) * a.k_blocks + kb) * a.nbox : b_row;
+          tma_load_2d(dst, &mapB, fb, kx, y, pol);
         }
       }
     }
@@ -178,87 +190,141 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) mma_commit(smem_u32(&tail->accf));
     }
-  } else {
-    // Epilogue warps 2..5: warp w may only touch TMEM lanes 32*(w%4) .. +31.  The
-    // outputs may still be read by the previous kernel until it completes.
+  } else if (warp >= 2 && warp < 2 + kEpiWarps) {
+    // Epilogue warps 2..9: warp w may only touch TMEM lanes 32*(w%4) .. +31, so each
+    // lane quarter has two warps; they take alternate 16-column chunks.  The outputs may
+    // still be read by the previous kernel until it completes.
     pdl_wait();
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
+    const int te = threadIdx.x - 64;  // 0..255 over the epilogue warps
+    const int nchunk = a.nbox / 16;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     if (nk > 0 && mbar_wait_bounded(smem_u32(&tail->accf), 0, abort, a.err, DEV_TIMEOUT_EPILOGUE)) {
       tc_fence_after();
+      // Every MMA has completed, so the smem rings are free: output tiles are staged
+      // there in fp32 as [token][128 columns] and written out with 16-byte stores that
+      // cover whole row segments.
+      float* stage = reinterpret_cast<float*>(smem);
       if (MODE == GEMM_RED_ADD) {
         for (int i = 0; i < 2; ++i) {
           if (!a_ok[i]) continue;
           const int n = a_row[i] + r;
-          for (int c = 0; c < a.nbox; c += 16) {
-            float v[16];
-            tmem_ld16(lane_base + (uint32_t)(i * 256 + c), v);
-            if (a.atomic) {
+          if (a.atomic) {
+            for (int ci = half; ci < nchunk; ci += 2) {
+              float v[16];
+              tmem_ld16(lane_base + (uint32_t)(i * 256 + ci * 16), v);
               for (int j = 0; j < 16; ++j) {
-                const int t = b_row + c + j;
+                const int t = b_row + ci * 16 + j;
                 if (t < a.T) atomicAdd(a.out_f32 + (size_t)t * a.ldo + n, v[j]);
               }
-            } else {
-              // Plain stores of this split's partial sums; a warp writes 128 contiguous
-              // bytes per token.  The consumer kernel adds the splits in a fixed order.
-              float* base = a.out_f32 + (size_t)blockIdx.y * a.split_stride + n;
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int t = b_row + c + j;
-                if (t < a.T) base[(size_t)t * a.ldo] = v[j];
-              }
             }
+            continue;
           }
+          for (int ci = half; ci < nchunk; ci += 2) {
+            float v[16];
+            tmem_ld16(lane_base + (uint32_t)(i * 256 + ci * 16), v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) stage[(ci * 16 + j) * 128 + r] = v[j];
+          }
+          epilogue_sync();
+          // This split's partial sums; the consumer adds the splits in a fixed order.
+          float* base = a.out_f32 + (size_t)blockIdx.y * a.split_stride + a_row[i];
+          for (int e = te; e < a.nbox * 32; e += kEpiWarps * 32) {
+            const int tt = e >> 5, c4 = (e & 31) * 4;
+            if (b_row + tt < a.T)
+              *reinterpret_cast<float4*>(base + (size_t)(b_row + tt) * a.ldo + c4) =
+                  *reinterpret_cast<const float4*>(stage + tt * 128 + c4);
+          }
+          epilogue_sync();
         }
       } else if (MODE == GEMM_SWIGLU) {
-        const int f = a_row[0] + r;
-        for (int c = 0; c < a.nbox; c += 16) {
+        for (int ci = half; ci < nchunk; ci += 2) {
           float g[16], u[16];
-          tmem_ld16(lane_base + (uint32_t)c, g);
-          tmem_ld16(lane_base + (uint32_t)(256 + c), u);
+          tmem_ld16x2(lane_base + (uint32_t)(ci * 16), lane_base + (uint32_t)(256 + ci * 16), g, u);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = b_row + c + j;
-            const float h = g[j] / (1.0f + __expf(-g[j])) * u[j];
-            if (t < a.T) a.out_bf16[(size_t)t * a.ldh + f] = __float2bfloat16_rn(h);
+          for (int j = 0; j < 16; ++j)
+            stage[(ci * 16 + j) * 128 + r] = __fdividef(g[j], 1.0f + __expf(-g[j])) * u[j];
+        }
+        epilogue_sync();
+        bf16* base = a.out_bf16 + a_row[0];
+        for (int e = te; e < a.nbox * 16; e += kEpiWarps * 32) {
+          const int tt = e >> 4, c8 = (e & 15) * 8;
+          if (b_row + tt < a.T) {
+            const float4 x0 = *reinterpret_cast<const float4*>(stage + tt * 128 + c8);
+            const float4 x1 = *reinterpret_cast<const float4*>(stage + tt * 128 + c8 + 4);
+            uint4 o;
+            __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&o);
+            h2[0] = __floats2bfloat162_rn(x0.x, x0.y);
+            h2[1] = __floats2bfloat162_rn(x0.z, x0.w);
+            h2[2] = __floats2bfloat162_rn(x1.x, x1.y);
+            h2[3] = __floats2bfloat162_rn(x1.z, x1.w);
+            *reinterpret_cast<uint4*>(base + (size_t)(b_row + tt) * a.ldh + c8) = o;
           }
         }
       } else {
+        // Each warp pair (same lane quarter) scans alternate 16-column chunks of the
+        // 256-row vocabulary tile; the two running (max, sum exp, argmax) states of a
+        // token are merged through shared memory.
         const int vt = blockIdx.x;
+        float* xm = stage;
+        float* xs = stage + 128;
+        int* xi = reinterpret_cast<int*>(stage + 256);
         for (int i = 0; i < 2; ++i) {
           if (!a_ok[i]) continue;
           const int t = a_row[i] + r;
           float m = -INFINITY, ssum = 0.f;
-          int idx = 0;
-          for (int c = 0; c < a.nbox; c += 16) {
+          int idx = 0x7fffffff;
+          for (int ci = half; ci < nchunk; ci += 2) {
             float v[16];
             __syncwarp();
-            tmem_ld16(lane_base + (uint32_t)(i * 256 + c), v);
+            tmem_ld16(lane_base + (uint32_t)(i * 256 + ci * 16), v);
             float cm = -INFINITY;
-            int ci = 0;
+            int cidx = 0;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const int id = b_row + c + j;
+              const int id = b_row + ci * 16 + j;
               v[j] = (id < a.V && id != a.mask_id) ? v[j] * a.scale : -INFINITY;
-              if (v[j] > cm) { cm = v[j]; ci = id; }  // strict: lowest id wins ties
+              if (v[j] > cm) { cm = v[j]; cidx = id; }  // strict: lowest id wins ties
             }
             if (cm != -INFINITY) {
               const float nm = fmaxf(m, cm);
               float acc = (m == -INFINITY) ? 0.f : ssum * __expf(m - nm);
 #pragma unroll
               for (int j = 0; j < 16; ++j) acc += __expf(v[j] - nm);
-              if (cm > m) idx = ci;
+              if (cm > m) idx = cidx;
               m = nm;
               ssum = acc;
             }
           }
-          if (t < a.T) {
-            const size_t o = (size_t)vt * a.part_ld + t;
-            a.part_m[o] = m;
-            a.part_s[o] = ssum;
-            a.part_i[o] = idx;
+          if (half == 1) {
+            xm[r] = m;
+            xs[r] = ssum;
+            xi[r] = idx;
           }
+          epilogue_sync();
+          if (half == 0) {
+            const float m1 = xm[r], s1 = xs[r];
+            const int i1 = xi[r];
+            if (m1 != -INFINITY) {
+              if (m == -INFINITY) {
+                m = m1; ssum = s1; idx = i1;
+              } else {
+                const float nm = fmaxf(m, m1);
+                ssum = ssum * __expf(m - nm) + s1 * __expf(m1 - nm);
+                idx = m > m1 ? idx : (m1 > m ? i1 : min(idx, i1));
+                m = nm;
+              }
+            }
+            if (t < a.T) {
+              const size_t o = (size_t)vt * a.part_ld + t;
+              a.part_m[o] = m;
+              a.part_s[o] = ssum;
+              a.part_i[o] = m == -INFINITY ? 0 : idx;
+            }
+          }
+          epilogue_sync();
         }
       }
     }
@@ -291,6 +357,11 @@ EncodeTiledFn get_encode_fn() {
 }
 
 uint32_t round1k(uint32_t v) { return (v + 1023) & ~1023u; }
+
+// Smallest ring size that can hold a staged output tile of nbox tokens x 128 columns.
+uint32_t stage_bytes(int mode, int nbox) {
+  return mode == GEMM_LMSTATS ? 384 * 4 : (uint32_t)nbox * 128 * 4;
+}
 
 }  // namespace
 
@@ -330,20 +401,42 @@ cudaError_t gemm_set_smem_limits() {
   if ((e = cudaFuncSetAttribute(gemm_kernel<GEMM_SWIGLU>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem)) != cudaSuccess)
     return e;
-  return cudaFuncSetAttribute(gemm_kernel<GEMM_LMSTATS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kMaxSmem);
+  if ((e = cudaFuncSetAttribute(gemm_kernel<GEMM_LMSTATS>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem)) != cudaSuccess)
+    return e;
+  return set_uniform_carveout();
+}
+
+cudaError_t gemm_set_carveout() {
+  cudaError_t e;
+  const int c = cudaSharedmemCarveoutMaxShared;
+  if ((e = cudaFuncSetAttribute(gemm_kernel<GEMM_RED_ADD>,
+                                cudaFuncAttributePreferredSharedMemoryCarveout, c)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(gemm_kernel<GEMM_SWIGLU>,
+                                cudaFuncAttributePreferredSharedMemoryCarveout, c)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(gemm_kernel<GEMM_LMSTATS>,
+                              cudaFuncAttributePreferredSharedMemoryCarveout, c);
 }
 
 // act: [act_rows_alloc][K] bf16 activations (T valid rows); w: [n_rows_w][K] bf16.
 const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_alloc, int T,
                       const void* w, int n_rows_w, int K, int na, int splits, int tok_box,
-                      int num_sms) {
+                      int num_sms, bool w_packed) {
   static thread_local char err[256];
+  // Packed weights are viewed as [tiles * K/64 * tile_rows][64]: one box = one tile.
+  auto weight_map = [&](CUtensorMap* map, int tile_rows) {
+    if (!w_packed) return make_tmap_bf16(map, w, n_rows_w, K, tile_rows, err, sizeof(err));
+    const uint64_t tiles = (uint64_t)(n_rows_w + tile_rows - 1) / tile_rows;
+    return make_tmap_bf16(map, w, tiles * (K / 64) * tile_rows, 64, tile_rows, err, sizeof(err));
+  };
   memset(L, 0, sizeof(*L));
   GemmArgs& a = L->args;
   if (K % 64 != 0 || K <= 0) return "GEMM K must be a positive multiple of 64";
   if (T <= 0) return "GEMM needs at least one token row";
   a.mode = mode;
+  a.w_packed = w_packed ? 1 : 0;
   a.k_blocks = K / 64;
   a.T = T;
   a.a_tile_bytes = 128 * 128;  // 128 rows x 64 bf16
@@ -353,7 +446,7 @@ const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_all
     a.a_rows = T;
     a.splits = 1;
     if (!make_tmap_bf16(&L->mapA, act, act_rows_alloc, K, 128, err, sizeof(err))) return err;
-    if (!make_tmap_bf16(&L->mapB, w, n_rows_w, K, 256, err, sizeof(err))) return err;
+    if (!weight_map(&L->mapB, 256)) return err;
     L->grid = dim3((n_rows_w + 255) / 256, 1, (T + na * 128 - 1) / (na * 128));
     a.w_slot_bytes = round1k(a.nbox * 128);
     a.x_slot_bytes = round1k(a.na * a.a_tile_bytes);
@@ -367,7 +460,7 @@ const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_all
     a.splits = (mode == GEMM_SWIGLU) ? 1 : splits;
     if (a.splits < 1) a.splits = 1;
     if (a.splits > a.k_blocks) a.splits = a.k_blocks;
-    if (!make_tmap_bf16(&L->mapA, w, n_rows_w, K, 128, err, sizeof(err))) return err;
+    if (!weight_map(&L->mapA, 128)) return err;
     if (!make_tmap_bf16(&L->mapB, act, act_rows_alloc, K, tok_box, err, sizeof(err))) return err;
     const int gx = (mode == GEMM_SWIGLU) ? (n_rows_w / 2) / 128 : (n_rows_w + a.na * 128 - 1) / (a.na * 128);
     L->grid = dim3(gx, a.splits, (T + tok_box - 1) / tok_box);
@@ -382,6 +475,9 @@ const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_all
   a.w_stages = (budget - a.x_stages * (int)a.x_slot_bytes) / (int)a.w_slot_bytes;
   if (a.w_stages > kMaxStages) a.w_stages = kMaxStages;
   if (a.w_stages < 2) return "GEMM tile does not fit in shared memory";
+  if ((size_t)a.w_stages * a.w_slot_bytes + (size_t)a.x_stages * a.x_slot_bytes <
+      stage_bytes(mode, a.nbox))
+    return "GEMM output tile does not fit in the staging area";
   L->smem = 1024 + (size_t)a.w_stages * a.w_slot_bytes + (size_t)a.x_stages * a.x_slot_bytes +
             sizeof(SmemTail) + 64;
   return "";

@@ -58,6 +58,7 @@ struct GemmArgs {
   bf16* out_bf16;    int ldh;
   float* part_m; float* part_s; int* part_i; int part_ld;
   int* err;
+  int w_packed;      // weight operand in tile-major layout (see launch_pack_tiles)
 };
 
 struct GemmLaunch {
@@ -72,10 +73,24 @@ struct GemmLaunch {
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows, char* errbuf, size_t errlen);
 
-// Fills `L` for one GEMM.  Returns an empty string on success, else a reason.
+// Fills `L` for one GEMM.  Returns an empty string on success, else a reason.  With
+// w_packed the weight is in the tile-major layout written by launch_pack_tiles (tiles of
+// 128 rows, 256 for the LM head); otherwise it is row-major [n_rows_w][K].
 const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_alloc, int T,
                       const void* w, int n_rows_w, int K, int na, int splits, int tok_box,
-                      int num_sms);
+                      int num_sms, bool w_packed = false);
+
+// Tile-major weight packing: [rows][K] row-major -> [ceil(rows/tile_rows)][K/64][tile_rows][64].
+size_t packed_elems(int rows, int K, int tile_rows);
+cudaError_t launch_pack_tiles(const bf16* src, bf16* dst, int rows, int K, int tile_rows,
+                              cudaStream_t s);
+// Gives every kernel of the library the same (maximal) shared-memory carveout, so that
+// consecutive kernels never make an SM change its L1/shared split.
+cudaError_t set_uniform_carveout();
+cudaError_t gemm_set_carveout();
+cudaError_t attention_set_carveout();
+cudaError_t pointwise_set_carveout();
+cudaError_t decide_set_carveout();
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s);
 cudaError_t gemm_set_smem_limits();
 int gemm_max_smem();

@@ -36,6 +36,14 @@ bool pdl_enabled() {
   static const bool on = getenv("LOPA_NO_PDL") == nullptr;
   return on;
 }
+
+cudaError_t set_uniform_carveout() {
+  cudaError_t e;
+  if ((e = gemm_set_carveout()) != cudaSuccess) return e;
+  if ((e = attention_set_carveout()) != cudaSuccess) return e;
+  if ((e = pointwise_set_carveout()) != cudaSuccess) return e;
+  return decide_set_carveout();
+}
 }  // namespace lopa
 
 namespace {
@@ -189,7 +197,7 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
       while (splits > 1 && (size_t)splits * p.T * nrows > ctx->part_floats) --splits;
     }
     const char* e = plan_gemm(&G, mode, act, ctx->Tmax, p.T, w, nrows, K, na, splits, p.tok_box,
-                              ctx->num_sms);
+                              ctx->num_sms, /*w_packed=*/true);
     if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s GEMM: %s", what, e);
     if (mode == GEMM_RED_ADD) {
       if ((size_t)G.args.splits * p.T * nrows > ctx->part_floats)
@@ -214,7 +222,7 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
   if (lm) {
     const int na = p.T > 128 ? 2 : 1;
     const char* e = plan_gemm(&p.lmh, GEMM_LMSTATS, ctx->n, ctx->Tmax, p.T, ctx->lm_head, m.vocab,
-                              d, na, 1, 0, ctx->num_sms);
+                              d, na, 1, 0, ctx->num_sms, /*w_packed=*/true);
     if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "lm-head GEMM: %s", e);
     GemmArgs& a = p.lmh.args;
     a.V = m.vocab;
@@ -413,6 +421,22 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
   CK(cudaMemsetAsync(ctx->out_tokens, 0, (size_t)m.max_seq * sizeof(int), s));
   CK(launch_rope_table(ctx->cos_t, ctx->sin_t, m.max_seq, dh, (double)m.rope_base, s));
   CK(launch_state_reset(ctx->st, 0, B, m.mask_id, s));
+  // Owned tile-major copies of the projection weights and the LM head: every 16 KB
+  // (32 KB for the LM head) tile the GEMMs stream becomes one contiguous HBM run.
+  auto pack = [&](const bf16*& w, int rows, int K, int tile_rows) -> int {
+    bf16* p = nullptr;
+    int rr = dalloc(ctx, &p, packed_elems(rows, K, tile_rows));
+    if (rr) return rr;
+    CK(launch_pack_tiles(w, p, rows, K, tile_rows, s));
+    w = p;
+    return 0;
+  };
+  for (int l = 0; l < L; ++l) {
+    if ((r = pack(ctx->wqkv[l], ctx->qkv_rows, d, 128)) || (r = pack(ctx->wo[l], d, H * dh, 128)) ||
+        (r = pack(ctx->wgu[l], 2 * F, d, 128)) || (r = pack(ctx->wd[l], d, F, 128)))
+      return r;
+  }
+  if ((r = pack(ctx->lm_head, V, d, 256))) return r;
   CK(cudaEventCreate(&ctx->ev0));
   CK(cudaEventCreate(&ctx->ev1));
   CK(cudaMallocHost(&ctx->h_res, sizeof(lopa_step_result)));
@@ -587,17 +611,36 @@ int lopa_time_gemm(lopa_ctx* ctx, int kind, int iters, float* avg_ms) {
   const Plan& p = ctx->step_plan;
   const int L = ctx->mc.n_layers;
   cudaStream_t s = ctx->stream;
-  CK(cudaEventRecord(ctx->ev0, s));
-  for (int i = 0; i < iters; ++i) {
+  // The launches are captured into a graph (as in the decoding step), so host launch
+  // cost does not enter the timing; layers are cycled so no weight stays in L2.
+  cudaGraph_t g = nullptr;
+  cudaGraphExec_t ge = nullptr;
+  CK(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+  cudaError_t ce = cudaSuccess;
+  for (int i = 0; i < iters && ce == cudaSuccess; ++i) {
     const int l = i % L;
     const GemmLaunch& G = kind == 0 ? p.qkv[l] : kind == 1 ? p.o[l] : kind == 2 ? p.gu[l]
                         : kind == 3 ? p.dn[l] : p.lmh;
-    CK(launch_gemm(G, s));
+    ce = launch_gemm(G, s);
   }
-  CK(cudaEventRecord(ctx->ev1, s));
-  CK(cudaEventSynchronize(ctx->ev1));
+  cudaError_t ee = cudaStreamEndCapture(s, &g);
+  if (ce != cudaSuccess || ee != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    return fail(ctx, LOPA_ERR_CUDA, "capture of timed GEMMs failed: %s",
+                cudaGetErrorString(ce != cudaSuccess ? ce : ee));
+  }
+  ce = cudaGraphInstantiate(&ge, g, 0);
+  cudaGraphDestroy(g);
+  if (ce != cudaSuccess) return fail(ctx, LOPA_ERR_CUDA, "instantiate: %s", cudaGetErrorString(ce));
   float ms = 0.f;
-  CK(cudaEventElapsedTime(&ms, ctx->ev0, ctx->ev1));
+  ce = cudaGraphLaunch(ge, s);  // warm-up
+  if (ce == cudaSuccess) ce = cudaEventRecord(ctx->ev0, s);
+  if (ce == cudaSuccess) ce = cudaGraphLaunch(ge, s);
+  if (ce == cudaSuccess) ce = cudaEventRecord(ctx->ev1, s);
+  if (ce == cudaSuccess) ce = cudaEventSynchronize(ctx->ev1);
+  if (ce == cudaSuccess) ce = cudaEventElapsedTime(&ms, ctx->ev0, ctx->ev1);
+  cudaGraphExecDestroy(ge);
+  if (ce != cudaSuccess) return fail(ctx, LOPA_ERR_CUDA, "timed GEMMs: %s", cudaGetErrorString(ce));
   *avg_ms = ms / iters;
   return check_device_error(ctx);
 }

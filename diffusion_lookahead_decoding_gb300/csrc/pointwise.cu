@@ -264,6 +264,17 @@ __global__ void rope_table_kernel(float* cos_t, float* sin_t, int S, int dh, dou
 
 }  // namespace
 
+cudaError_t pointwise_set_carveout() {
+  const int c = cudaSharedmemCarveoutMaxShared;
+  const void* ks[] = {(const void*)embed_norm_kernel, (const void*)rope_prewrite_kernel,
+                      (const void*)residual_norm_kernel, (const void*)lm_merge_kernel};
+  for (const void* k : ks) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, c);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_embed_norm(const int* tok, int T, const bf16* E, const bf16* g, float* x,
                               bf16* n, int d, float eps, cudaStream_t s) {
   return launch_pdl(embed_norm_kernel, dim3((T + 7) / 8), dim3(256), 0, s, tok, T, E, g, x, n, d,
