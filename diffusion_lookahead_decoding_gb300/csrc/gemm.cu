@@ -222,11 +222,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             continue;
           }
-          for (int ci = half; ci < nchunk; ci += 2) {
-            float v[16];
-            tmem_ld16(lane_base + (uint32_t)(i * 256 + ci * 16), v);
+          // Two of this warp's chunks per TMEM wait.
+          for (int ci = half; ci < nchunk; ci += 4) {
+            float v[16], w[16];
+            if (ci + 2 < nchunk) {
+              tmem_ld16x2(lane_base + (uint32_t)(i * 256 + ci * 16),
+                          lane_base + (uint32_t)(i * 256 + ci * 16 + 32), v, w);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) stage[(ci * 16 + j) * 128 + r] = v[j];
+              for (int j = 0; j < 16; ++j) {
+                stage[(ci * 16 + j) * 128 + r] = v[j];
+                stage[(ci * 16 + 32 + j) * 128 + r] = w[j];
+              }
+            } else {
+              tmem_ld16(lane_base + (uint32_t)(i * 256 + ci * 16), v);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) stage[(ci * 16 + j) * 128 + r] = v[j];
+            }
           }
           epilogue_sync();
           // This split's partial sums; the consumer adds the splits in a fixed order.

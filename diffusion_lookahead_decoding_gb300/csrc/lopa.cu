@@ -142,6 +142,7 @@ int round16(int v) { return (v + 15) / 16 * 16; }
 int pick_splits(int tiles, int k_blocks, int num_sms) {
   int s = num_sms / std::max(tiles, 1);
   s = std::min(s, std::max(k_blocks / 2, 1));
+  s = std::min(s, 16);  // the consumers read every split: keep that bounded
   return std::max(s, 1);
 }
 

@@ -58,20 +58,20 @@ __global__ void embed_norm_kernel(const int* __restrict__ tok, int T, const bf16
   }
 }
 
-// Sums 4 consecutive floats over the split-K partials (independent 16-byte loads).
+// Sums 4 consecutive floats over the split-K partials, in split order, with the loads
+// issued eight at a time.
 __device__ __forceinline__ float4 sum_splits4(const float* p, int nsplit, size_t stride) {
   float4 a = *reinterpret_cast<const float4*>(p);
-  int s = 1;
-  for (; s + 4 <= nsplit; s += 4) {
-    float4 q[4];
+  for (int s0 = 1; s0 < nsplit; s0 += 8) {
+    float4 q[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) q[u] = *reinterpret_cast<const float4*>(p + (size_t)(s + u) * stride);
+    for (int u = 0; u < 8; ++u)
+      if (s0 + u < nsplit) q[u] = *reinterpret_cast<const float4*>(p + (size_t)(s0 + u) * stride);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) { a.x += q[u].x; a.y += q[u].y; a.z += q[u].z; a.w += q[u].w; }
-  }
-  for (; s < nsplit; ++s) {
-    const float4 q = *reinterpret_cast<const float4*>(p + (size_t)s * stride);
-    a.x += q.x; a.y += q.y; a.z += q.z; a.w += q.w;
+    for (int u = 0; u < 8; ++u)
+      if (s0 + u < nsplit) {
+        a.x += q[u].x; a.y += q[u].y; a.z += q[u].z; a.w += q[u].w;
+      }
   }
   return a;
 }
@@ -145,61 +145,51 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
+// Sums nsplit float4 partials at p, p + stride, ... onto acc in split order.  Loads are
+// issued eight at a time so that they are in flight together.
+__device__ __forceinline__ void add_splits4(float4& acc, const float* p, int nsplit,
+                                            size_t stride) {
+  for (int s0 = 0; s0 < nsplit; s0 += 8) {
+    float4 q[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (s0 + u < nsplit) q[u] = *reinterpret_cast<const float4*>(p + (size_t)(s0 + u) * stride);
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (s0 + u < nsplit) {
+        acc.x += q[u].x; acc.y += q[u].y; acc.z += q[u].z; acc.w += q[u].w;
+      }
+  }
+}
+
 // x[t] += sum_s part[s][t] (splits added in order), then n[t] = bf16(rmsnorm(x[t]) * g).
-// One CTA per row, one 8-element chunk per thread; the split loads are independent
-// 16-byte loads so that many are in flight per thread.
-__global__ void residual_norm_kernel(float* __restrict__ x, const float* __restrict__ part,
-                                     int nsplit, size_t split_stride, const bf16* __restrict__ g,
-                                     bf16* __restrict__ n, int T, int d, float eps) {
+// One CTA per row, four columns per thread.
+__global__ void __launch_bounds__(1024)
+    residual_norm_kernel(float* __restrict__ x, const float* __restrict__ part, int nsplit,
+                         size_t split_stride, const bf16* __restrict__ g, bf16* __restrict__ n,
+                         int T, int d, float eps) {
   __shared__ float red[32];
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;
-  const int c = threadIdx.x * 8;
+  const int c = threadIdx.x * 4;
   const bool active = c < d;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float* xr = x + (size_t)t * d + c;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (active) {
-    const float4 a = *reinterpret_cast<const float4*>(xr);
-    const float4 b = *reinterpret_cast<const float4*>(xr + 4);
-    acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
-    acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
-    const float* pr = part + (size_t)t * d + c;
-    int s = 0;
-    for (; s + 4 <= nsplit; s += 4) {
-      float4 p[8];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        p[2 * u] = *reinterpret_cast<const float4*>(pr + (size_t)(s + u) * split_stride);
-        p[2 * u + 1] = *reinterpret_cast<const float4*>(pr + (size_t)(s + u) * split_stride + 4);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        acc[0] += p[2 * u].x; acc[1] += p[2 * u].y; acc[2] += p[2 * u].z; acc[3] += p[2 * u].w;
-        acc[4] += p[2 * u + 1].x; acc[5] += p[2 * u + 1].y; acc[6] += p[2 * u + 1].z;
-        acc[7] += p[2 * u + 1].w;
-      }
-    }
-    for (; s < nsplit; ++s) {
-      const float4 p0 = *reinterpret_cast<const float4*>(pr + (size_t)s * split_stride);
-      const float4 p1 = *reinterpret_cast<const float4*>(pr + (size_t)s * split_stride + 4);
-      acc[0] += p0.x; acc[1] += p0.y; acc[2] += p0.z; acc[3] += p0.w;
-      acc[4] += p1.x; acc[5] += p1.y; acc[6] += p1.z; acc[7] += p1.w;
-    }
-    *reinterpret_cast<float4*>(xr) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    *reinterpret_cast<float4*>(xr + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    float* xr = x + (size_t)t * d + c;
+    acc = *reinterpret_cast<const float4*>(xr);
+    add_splits4(acc, part + (size_t)t * d + c, nsplit, split_stride);
+    *reinterpret_cast<float4*>(xr) = acc;
   }
-  float ss = 0.f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) ss += acc[e] * acc[e];
+  float ss = acc.x * acc.x + acc.y * acc.y + acc.z * acc.z + acc.w * acc.w;
   ss = block_sum(ss, red);  // also a barrier: every thread has read its partials
   const float rs = rsqrtf(ss / (float)d + eps);
   if (active) {
-    float gg[8], f[8];
-    load8(g + c, gg);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] = acc[e] * rs * gg[e];
-    store8(n + (size_t)t * d + c, f);
+    const uint2 gu = *reinterpret_cast<const uint2*>(g + c);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gu);
+    const float2 g01 = __bfloat1622float2(g2[0]), g23 = __bfloat1622float2(g2[1]);
+    store4_bf16(n + (size_t)t * d + c, acc.x * rs * g01.x, acc.y * rs * g01.y, acc.z * rs * g23.x,
+                acc.w * rs * g23.y);
   }
   if (d % 32 == 0) discard_partial_row(part + (size_t)t * d, split_stride, nsplit, d);
 }
@@ -291,7 +281,7 @@ cudaError_t launch_rope_prewrite(const float* qkv, int nsplit, size_t split_stri
 
 cudaError_t launch_residual_norm(float* x, const float* part, int nsplit, size_t split_stride,
                                  const bf16* g, bf16* n, int T, int d, float eps, cudaStream_t s) {
-  const int threads = ((d / 8 + 31) / 32) * 32;
+  const int threads = ((d / 4 + 31) / 32) * 32;
   if (threads > 1024) return cudaErrorInvalidValue;
   return launch_pdl(residual_norm_kernel, dim3(T), dim3(threads), 0, s, x, part, nsplit,
                     split_stride, g, n, T, d, eps);

@@ -166,6 +166,24 @@ def test_kv_cache_prompt_matches_oracle_and_commits_are_fresh(name):
             np.testing.assert_array_equal(vf, committed[l][1][j * B:(j + 1) * B])
 
 
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_decode_is_deterministic(name):
+    """The split-K sums are added in a fixed order and no kernel uses atomics, so two
+    decodes of the same prompt (and two identical forwards) agree bit for bit."""
+    shape, dshape, w, dec, prompt = _setup(name)
+    br = seeded_branches(shape, dshape.k + 1, dshape.block, seed=8)
+    a1, m1, h1 = dec.verify_forward(br, want_hidden=True)
+    a2, m2, h2 = dec.verify_forward(br, want_hidden=True)
+    np.testing.assert_array_equal(a1, a2)
+    np.testing.assert_array_equal(m1, m2)
+    np.testing.assert_array_equal(h1, h2)
+    t1, s1 = dec.decode(dshape.gen_len)
+    dec.rewind(dshape.prompt_len)
+    t2, s2 = dec.decode(dshape.gen_len)
+    np.testing.assert_array_equal(t1, t2)
+    assert s1["forwards"] == s2["forwards"] and s1["steps"] == s2["steps"]
+
+
 def test_state_errors_leave_state_unchanged():
     from diffusion_lookahead_decoding_gb300 import _lib as L
     shape, dshape, w = workload_weights("tiny")
@@ -191,5 +209,5 @@ def test_state_errors_leave_state_unchanged():
         dec.step()  # cache full
     assert e.value.code == L.ERR_BAD_STATE
     dec.rewind(dshape.prompt_len)
-    toks2, _ = dec.decode(dshape.gen_len)  # rewound decode reproduces the tokens
-    assert (toks2 == toks).mean() > 0.9
+    toks2, _ = dec.decode(dshape.gen_len)  # a rewound decode reproduces the tokens
+    np.testing.assert_array_equal(toks2, toks)
