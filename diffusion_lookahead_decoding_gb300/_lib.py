@@ -80,6 +80,9 @@ SIGNATURES = {
     "lopa_lmhead_argmax": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                      C.c_float, C.c_int, C.c_void_p, C.c_size_t, C.c_void_p,
                                      C.c_void_p, C.c_void_p]),
+    "lopa_lmhead_argmax_static": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
+                                            C.c_float, C.c_int, C.c_void_p, C.c_void_p,
+                                            C.c_void_p]),
     "lopa_branch_attention": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int,
                                         C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                         C.c_int, C.c_int, C.c_void_p, C.c_void_p]),

@@ -12,6 +12,9 @@ namespace lopa {
 
 typedef __nv_bfloat16 bf16;
 
+// Sets the message lopa_last_error(NULL) returns (failures of context-free calls).
+void set_global_error(const char* msg);
+
 // Launches `kern` with programmatic stream serialization (the kernels call pdl_wait
 // before reading their predecessor's outputs).
 bool pdl_enabled();

@@ -31,6 +31,8 @@ thread_local std::string g_init_error;
 }  // namespace
 
 namespace lopa {
+void set_global_error(const char* msg) { g_init_error = msg ? msg : ""; }
+
 // Programmatic dependent launch is on unless LOPA_NO_PDL is set (a debugging switch).
 bool pdl_enabled() {
   static const bool on = getenv("LOPA_NO_PDL") == nullptr;

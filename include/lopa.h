@@ -193,6 +193,25 @@ int lopa_lmhead_argmax(const void* hidden, const void* lm_head, int rows, int d_
                        size_t workspace_bytes, int32_t* argmax_out, float* maxp_out,
                        void* stream);
 
+/* lopa_lmhead_argmax for callers that cannot allocate device memory.  (The paper has no
+ * counterpart; this is a deployment convenience.)  Code running under a caller-owned
+ * memory pool, in a loop that must never enter an allocator, or in a host that hands out
+ * only fixed buffers cannot provide the workspace lopa_lmhead_argmax needs.  This call
+ * computes the same result with its workspace in a fixed 4 MiB array inside the
+ * library's device memory, held on every GPU that loads the library until exit; it
+ * allocates nothing and calls no allocating routine.
+ *   - rows * ceil(vocab / 256) * 12 must be <= 4 MiB (e.g. 256 rows at vocab 152064);
+ *     larger requests return LOPA_ERR_INVALID_ARG with a message in lopa_last_error(NULL).
+ *   - The first call on a device (with that device current) looks up the array's device
+ *     address; make that first call before any stream capture that includes this call.
+ *   - All calls on a device share the array: calls that can overlap on the GPU (e.g. on
+ *     different streams without ordering) race and must be avoided.  Nothing in the array
+ *     needs clearing between calls.
+ * Other arguments, layouts and results are those of lopa_lmhead_argmax. */
+int lopa_lmhead_argmax_static(const void* hidden, const void* lm_head, int rows, int d_model,
+                              int vocab, float logit_scale, int mask_id, int32_t* argmax_out,
+                              float* maxp_out, void* stream);
+
 /* Branch-isolated attention (same passage, "attention isolated between branches"):
  * for branch b, query row (i, h) attends to the shared prefix keys [0, prefix_len)
  * and to its own block keys [0, block) only, bidirectionally, with softmax scale
