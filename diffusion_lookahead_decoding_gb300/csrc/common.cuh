@@ -18,6 +18,7 @@ enum DeviceError : int {
   DEV_TIMEOUT_MMA = 2,
   DEV_TIMEOUT_EPILOGUE = 3,
   DEV_BAD_INDEX = 4,
+  DEV_TIMEOUT_CLUSTER = 5,
 };
 
 // Upper bound of any spin-wait on the device (nanoseconds of %globaltimer).
@@ -224,26 +225,80 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Drops a 128-byte line from L2 without writing it back (its contents become undefined).
-// Used on split-K partial sums once they have been consumed, so that dead partials never
-// cost HBM write bandwidth.
-__device__ __forceinline__ void l2_discard128(const void* p) {
-  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+// ---------------------------------------------------------------- thread-block clusters
+// Distributed shared memory: a CTA reads its cluster peers' shared memory through
+// shared::cluster addresses (mapa) and signals them through their mbarriers.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
 }
-
-// Discards the `row_floats`-wide row at `base` of each of `nsplit` partial splits
-// (`stride` floats apart); the row must start on a 128-byte boundary and the calling CTA
-// must have finished reading it.
-__device__ __forceinline__ void discard_partial_row(const float* base, size_t stride, int nsplit,
-                                                    int row_floats) {
-  const int lines = row_floats / 32;
-  for (int e = threadIdx.x; e < lines * nsplit; e += blockDim.x) {
-    const int s = e / lines, l = e - s * lines;
-    l2_discard128(base + (size_t)s * stride + (size_t)l * 32);
+// The shared::cluster address of the variable at local shared address `addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Split cluster barrier: every thread arrives once after its CTA's mbarriers are
+// initialised; a thread that later touches a peer waits first.  Arrivals happen at
+// kernel start, before any wait, and a cluster's CTAs are co-scheduled, so the wait
+// always completes.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrives (release, cluster scope) on the mbarrier at shared::cluster address `addr`.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait (as mbar_wait_bounded) with cluster-scope acquire, for phases completed by
+// peers' releases.
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity,
+                                                          volatile int* abort, int* err, int code) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (err) atomicExch(err, code);
+      *abort = 1;
+      return false;
+    }
   }
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 
 // ---------------------------------------------------------------- misc
+// Rounds four floats to bf16 (nearest-even) and stores them as one 8-byte word.
+__device__ __forceinline__ void store4_bf16(bf16* p, float a, float b, float c, float d) {
+  uint2 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+  h[0] = __floats2bfloat162_rn(a, b);
+  h[1] = __floats2bfloat162_rn(c, d);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

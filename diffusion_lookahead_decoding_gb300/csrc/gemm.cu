@@ -9,6 +9,11 @@
 //   RED_ADD : D[w_row][tok] = W . X^T over a K-split; the epilogue stores the split's
 //             fp32 partial [split][T][N] (summed in a fixed order by the consumer) or,
 //             for the standalone call, adds it atomically into an fp32 [T][N] output.
+//   QKV     : the q/k/v projection.  The K-splits of one output tile form a thread-block
+//             cluster; each CTA stages its fp32 partial tile in shared memory and CTA r
+//             of the cluster sums token slice r over all splits (fixed split order)
+//             through distributed shared memory, applies RoPE to q/k and writes bf16 q,
+//             K and V (the Pre-Write).  These partial sums never leave the cluster.
 //   SWIGLU  : two accumulators (gate rows f, up rows F+f) and an epilogue that writes
 //             bf16 silu(gate)*up for the down projection.
 //   LMSTATS : tokens on M (two 128-row tiles), 256 vocab rows on N; the epilogue keeps
@@ -45,6 +50,7 @@ struct SmemTail {
   uint64_t wfull[kMaxStages], wempty[kMaxStages];
   uint64_t xfull[kMaxStages], xempty[kMaxStages];
   uint64_t accf;
+  uint64_t cfull, cdone;  // clustered modes: all splits staged / all slices read
   uint32_t tmem_addr;
   int abort;
 };
@@ -69,7 +75,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int a_row[2];
   bool a_ok[2];
   int b_row;
-  if (MODE == GEMM_RED_ADD) {
+  constexpr bool kCluster = MODE == GEMM_QKV;
+  if (MODE == GEMM_RED_ADD || kCluster) {
     a_row[0] = blockIdx.x * a.na * 128;
     a_row[1] = a_row[0] + 128;
     b_row = blockIdx.z * a.nbox;
@@ -104,6 +111,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&tail->xempty[s]), 1);
     }
     mbar_init(smem_u32(&tail->accf), 1);
+    if (kCluster) {
+      mbar_init(smem_u32(&tail->cfull), a.splits);
+      mbar_init(smem_u32(&tail->cdone), a.splits);
+    }
     tail->abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&mapA);
@@ -116,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (kCluster) cluster_arrive_relaxed();  // this CTA's mbarriers are initialised
   const uint32_t tmem = tail->tmem_addr;
   volatile int* abort = &tail->abort;
   pdl_trigger();
@@ -201,17 +213,136 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int te = threadIdx.x - 64;  // 0..255 over the epilogue warps
     const int nchunk = a.nbox / 16;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    if (nk > 0 && mbar_wait_bounded(smem_u32(&tail->accf), 0, abort, a.err, DEV_TIMEOUT_EPILOGUE)) {
+    // Copies accumulator i to `stage` as fp32 [token][128 columns], two of this warp's
+    // 16-column chunks per TMEM wait.
+    auto stage_acc = [&](int i, float* stage) {
+      for (int ci = half; ci < nchunk; ci += 4) {
+        float v[16], w[16];
+        if (ci + 2 < nchunk) {
+          tmem_ld16x2(lane_base + (uint32_t)(i * 256 + ci * 16),
+                      lane_base + (uint32_t)(i * 256 + ci * 16 + 32), v, w);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            stage[(ci * 16 + j) * 128 + r] = v[j];
+            stage[(ci * 16 + 32 + j) * 128 + r] = w[j];
+          }
+        } else {
+          tmem_ld16(lane_base + (uint32_t)(i * 256 + ci * 16), v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) stage[(ci * 16 + j) * 128 + r] = v[j];
+        }
+      }
+    };
+    if (kCluster) {
+      // Split-K sum inside the cluster.  Per 128-row accumulator ("round"): every CTA
+      // stages its partial tile in its (now idle) smem rings and signals all peers' cfull;
+      // CTA `rank` then sums tokens [tlo, tlo + ntok) of the tile over the splits in split
+      // order, reading the peers' stages through distributed shared memory, and signals
+      // cdone so that peers may overwrite (or release) their stage.
+      const bool ok = nk > 0 && mbar_wait_bounded(smem_u32(&tail->accf), 0, abort, a.err,
+                                                  DEV_TIMEOUT_EPILOGUE);
       tc_fence_after();
-      // Every MMA has completed, so the smem rings are free: output tiles are staged
-      // there in fp32 as [token][128 columns] and written out with 16-byte stores that
-      // cover whole row segments.
+      float* stage = reinterpret_cast<float*>(smem);
+      const int S = a.splits;
+      const int rank = (int)cluster_ctarank();
+      uint32_t peer[kMaxClusterSplits];
+#pragma unroll
+      for (int c = 0; c < kMaxClusterSplits; ++c)
+        peer[c] = c < S ? mapa_shared(smem_u32(stage), (uint32_t)c) : 0u;
+      const int tlo = rank * a.nbox / S, ntok = (rank + 1) * a.nbox / S - tlo;
+      const uint32_t cfull = smem_u32(&tail->cfull), cdone = smem_u32(&tail->cdone);
+      const int P = a.dP ? *a.dP : 0;
+      cluster_wait();  // every peer's mbarriers are initialised
+      int round = 0;
+      for (int i = 0; i < 2; ++i) {
+        if (!a_ok[i]) continue;  // the same for every CTA of the cluster
+        if (round > 0)
+          mbar_wait_cluster_bounded(cdone, (uint32_t)(round - 1) & 1u, abort, a.err,
+                                    DEV_TIMEOUT_CLUSTER);
+        if (ok) stage_acc(i, stage);
+        epilogue_sync();
+        if (te == 0)
+          for (int c = 0; c < S; ++c) mbar_arrive_cluster(mapa_shared(cfull, (uint32_t)c));
+        if (mbar_wait_cluster_bounded(cfull, (uint32_t)round & 1u, abort, a.err,
+                                      DEV_TIMEOUT_CLUSTER)) {
+          // Work item e: token tlo + e/16, columns j..j+3 of a head and their rotation
+          // partners j+dh/2..+3.  Two items per pass keep 4*S loads in flight per thread.
+          const int dh = a.dh, hdh = dh >> 1, per_head = dh >> 3;
+          const int nitem = ntok * 16;
+          constexpr int kStep = kEpiWarps * 32;
+          for (int e0 = te; e0 < nitem; e0 += 2 * kStep) {
+            float4 v[2][2][kMaxClusterSplits];
+            uint32_t off[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int e = e0 + h * kStep;
+              const int tt = tlo + (e >> 4), u = e & 15;
+              const int hd = u / per_head, j = (u - hd * per_head) * 4;
+              off[h] = (uint32_t)(tt * 128 + hd * dh + j) * 4u;
+              if (e < nitem) {
+#pragma unroll
+                for (int c = 0; c < kMaxClusterSplits; ++c)
+                  if (c < S) {
+                    v[h][0][c] = ld_dsmem_f4(peer[c] + off[h]);
+                    v[h][1][c] = ld_dsmem_f4(peer[c] + off[h] + (uint32_t)hdh * 4u);
+                  }
+              }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int e = e0 + h * kStep;
+              const int tt = tlo + (e >> 4), u = e & 15;
+              const int t = b_row + tt;
+              if (e >= nitem || t >= a.T) continue;
+              const int hd = u / per_head, j = (u - hd * per_head) * 4;
+              float4 x1 = v[h][0][0], x2 = v[h][1][0];
+#pragma unroll
+              for (int c = 1; c < kMaxClusterSplits; ++c)
+                if (c < S) {
+                  x1.x += v[h][0][c].x; x1.y += v[h][0][c].y; x1.z += v[h][0][c].z; x1.w += v[h][0][c].w;
+                  x2.x += v[h][1][c].x; x2.y += v[h][1][c].y; x2.z += v[h][1][c].z; x2.w += v[h][1][c].w;
+                }
+              const int head = a_row[i] / dh + hd;
+              const int bi = t % a.Bq;
+              const size_t kv_row = a.kv_to_cache ? (size_t)(P + bi) : (size_t)t;
+              bf16* dst;
+              if (head < a.H + a.Hk) {
+                // RoPE, rotate-half form, at absolute position P + bi.
+                const float4 cs = *reinterpret_cast<const float4*>(a.cos_t + (size_t)(P + bi) * hdh + j);
+                const float4 sn = *reinterpret_cast<const float4*>(a.sin_t + (size_t)(P + bi) * hdh + j);
+                const float4 y1 = make_float4(x1.x * cs.x - x2.x * sn.x, x1.y * cs.y - x2.y * sn.y,
+                                              x1.z * cs.z - x2.z * sn.z, x1.w * cs.w - x2.w * sn.w);
+                x2 = make_float4(x2.x * cs.x + x1.x * sn.x, x2.y * cs.y + x1.y * sn.y,
+                                 x2.z * cs.z + x1.z * sn.z, x2.w * cs.w + x1.w * sn.w);
+                x1 = y1;
+                dst = head < a.H ? a.q + ((size_t)t * a.H + head) * dh
+                                 : a.kdst + (kv_row * a.Hk + (head - a.H)) * dh;
+              } else {
+                dst = a.vdst + (kv_row * a.Hk + (head - a.H - a.Hk)) * dh;
+              }
+              store4_bf16(dst + j, x1.x, x1.y, x1.z, x1.w);
+              store4_bf16(dst + j + hdh, x2.x, x2.y, x2.z, x2.w);
+            }
+          }
+        }
+        epilogue_sync();
+        if (te == 0)
+          for (int c = 0; c < S; ++c) mbar_arrive_cluster(mapa_shared(cdone, (uint32_t)c));
+        ++round;
+      }
+      // Stay resident until every peer has finished reading this CTA's stage.
+      if (round > 0)
+        mbar_wait_cluster_bounded(cdone, (uint32_t)(round - 1) & 1u, abort, a.err,
+                                  DEV_TIMEOUT_CLUSTER);
+    } else if (nk > 0 &&
+               mbar_wait_bounded(smem_u32(&tail->accf), 0, abort, a.err, DEV_TIMEOUT_EPILOGUE)) {
+      tc_fence_after();
       float* stage = reinterpret_cast<float*>(smem);
       if (MODE == GEMM_RED_ADD) {
         for (int i = 0; i < 2; ++i) {
           if (!a_ok[i]) continue;
-          const int n = a_row[i] + r;
-          if (a.atomic) {
+          if (a.atomic) {  // standalone accumulate: fp32 atomics into out_f32
+            const int n = a_row[i] + r;
             for (int ci = half; ci < nchunk; ci += 2) {
               float v[16];
               tmem_ld16(lane_base + (uint32_t)(i * 256 + ci * 16), v);
@@ -222,23 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             continue;
           }
-          // Two of this warp's chunks per TMEM wait.
-          for (int ci = half; ci < nchunk; ci += 4) {
-            float v[16], w[16];
-            if (ci + 2 < nchunk) {
-              tmem_ld16x2(lane_base + (uint32_t)(i * 256 + ci * 16),
-                          lane_base + (uint32_t)(i * 256 + ci * 16 + 32), v, w);
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                stage[(ci * 16 + j) * 128 + r] = v[j];
-                stage[(ci * 16 + 32 + j) * 128 + r] = w[j];
-              }
-            } else {
-              tmem_ld16(lane_base + (uint32_t)(i * 256 + ci * 16), v);
-#pragma unroll
-              for (int j = 0; j < 16; ++j) stage[(ci * 16 + j) * 128 + r] = v[j];
-            }
-          }
+          stage_acc(i, stage);
           epilogue_sync();
           // This split's partial sums; the consumer adds the splits in a fixed order.
           float* base = a.out_f32 + (size_t)blockIdx.y * a.split_stride + a_row[i];
@@ -404,31 +519,50 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 
 int gemm_max_smem() { return kMaxSmem; }
 
+template <int MODE>
+const void* kernel_ptr() {
+  return reinterpret_cast<const void*>(gemm_kernel<MODE>);
+}
+
+const void* const kKernels[] = {kernel_ptr<GEMM_RED_ADD>(), kernel_ptr<GEMM_SWIGLU>(),
+                                kernel_ptr<GEMM_LMSTATS>(), kernel_ptr<GEMM_QKV>()};
+
 cudaError_t gemm_set_smem_limits() {
-  cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gemm_kernel<GEMM_RED_ADD>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(gemm_kernel<GEMM_SWIGLU>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(gemm_kernel<GEMM_LMSTATS>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem)) != cudaSuccess)
-    return e;
+  for (const void* k : kKernels) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (e != cudaSuccess) return e;
+  }
   return set_uniform_carveout();
 }
 
 cudaError_t gemm_set_carveout() {
-  cudaError_t e;
-  const int c = cudaSharedmemCarveoutMaxShared;
-  if ((e = cudaFuncSetAttribute(gemm_kernel<GEMM_RED_ADD>,
-                                cudaFuncAttributePreferredSharedMemoryCarveout, c)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(gemm_kernel<GEMM_SWIGLU>,
-                                cudaFuncAttributePreferredSharedMemoryCarveout, c)) != cudaSuccess)
-    return e;
-  return cudaFuncSetAttribute(gemm_kernel<GEMM_LMSTATS>,
-                              cudaFuncAttributePreferredSharedMemoryCarveout, c);
+  for (const void* k : kKernels) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+int gemm_cluster_capacity(int mode, int cs, size_t smem) {
+  if (mode < 0 || mode > GEMM_QKV || cs < 1 || cs > kMaxClusterSplits) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, (unsigned)cs, 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)cs;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kKernels[mode], &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 // act: [act_rows_alloc][K] bf16 activations (T valid rows); w: [n_rows_w][K] bf16.
@@ -465,12 +599,20 @@ const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_all
     if (tok_box < 16 || tok_box > 256 || tok_box % 16 != 0) return "token box must be 16..256, multiple of 16";
     if (n_rows_w % 128 != 0) return "GEMM N must be a multiple of 128";
     a.na = (mode == GEMM_SWIGLU) ? 2 : na;
+    if (a.na != 1 && a.na != 2) return "GEMM tiles per CTA must be 1 or 2";
     a.F = n_rows_w / 2;
     a.nbox = tok_box;
     a.a_rows = n_rows_w;
     a.splits = (mode == GEMM_SWIGLU) ? 1 : splits;
     if (a.splits < 1) a.splits = 1;
-    if (a.splits > a.k_blocks) a.splits = a.k_blocks;
+    if (gemm_mode_clustered(mode)) {
+      // The K-splits of a tile are one cluster: 1, 2 or 4 CTAs, each with >= 1 K block.
+      if ((a.splits & (a.splits - 1)) != 0 || a.splits > kMaxClusterSplits ||
+          a.splits > a.k_blocks)
+        return "cluster split count must be 1, 2 or 4 and at most K/64";
+    } else if (a.splits > a.k_blocks) {
+      a.splits = a.k_blocks;
+    }
     if (!weight_map(&L->mapA, 128)) return err;
     if (!make_tmap_bf16(&L->mapB, act, act_rows_alloc, K, tok_box, err, sizeof(err))) return err;
     const int gx = (mode == GEMM_SWIGLU) ? (n_rows_w / 2) / 128 : (n_rows_w + a.na * 128 - 1) / (a.na * 128);
@@ -495,16 +637,19 @@ const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_all
 }
 
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s) {
+  const dim3 blk(kThreads);
   switch (L.args.mode) {
     case GEMM_RED_ADD:
-      return launch_pdl(gemm_kernel<GEMM_RED_ADD>, L.grid, dim3(kThreads), L.smem, s, L.mapA,
-                        L.mapB, L.args);
+      return launch_pdl(gemm_kernel<GEMM_RED_ADD>, L.grid, blk, L.smem, s, L.mapA, L.mapB, L.args);
     case GEMM_SWIGLU:
-      return launch_pdl(gemm_kernel<GEMM_SWIGLU>, L.grid, dim3(kThreads), L.smem, s, L.mapA,
-                        L.mapB, L.args);
+      return launch_pdl(gemm_kernel<GEMM_SWIGLU>, L.grid, blk, L.smem, s, L.mapA, L.mapB, L.args);
+    case GEMM_LMSTATS:
+      return launch_pdl(gemm_kernel<GEMM_LMSTATS>, L.grid, blk, L.smem, s, L.mapA, L.mapB, L.args);
+    case GEMM_QKV:
+      return launch_pdl_cluster(gemm_kernel<GEMM_QKV>, L.grid, blk, L.smem, s, L.args.splits,
+                                L.mapA, L.mapB, L.args);
     default:
-      return launch_pdl(gemm_kernel<GEMM_LMSTATS>, L.grid, dim3(kThreads), L.smem, s, L.mapA,
-                        L.mapB, L.args);
+      return cudaErrorInvalidValue;
   }
 }
 

@@ -16,23 +16,36 @@ typedef __nv_bfloat16 bf16;
 void set_global_error(const char* msg);
 
 // Launches `kern` with programmatic stream serialization (the kernels call pdl_wait
-// before reading their predecessor's outputs).
+// before reading their predecessor's outputs) and, when cluster_y > 0, as thread-block
+// clusters of (1, cluster_y, 1) CTAs.
 bool pdl_enabled();
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t s, Args... args) {
+cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t s, int cluster_y, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cluster_y > 0) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = (unsigned)cluster_y;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  return launch_pdl_cluster(kern, grid, block, smem, s, 0, args...);
 }
 
 // ------------------------------------------------------------------ GEMM (tcgen05)
@@ -40,7 +53,13 @@ enum GemmMode : int {
   GEMM_RED_ADD = 0,  // out_f32[t][n] += sum_k act[t][k] * w[n][k]   (weights on M, tokens on N)
   GEMM_SWIGLU = 1,   // out_bf16[t][f] = silu(gate) * up             (weights on M, tokens on N)
   GEMM_LMSTATS = 2,  // per (vocab tile, token): max, sum exp, argmax  (tokens on M, vocab on N)
+  GEMM_QKV = 3,      // q/k/v projection + RoPE + bf16 Pre-Write; split-K summed in a cluster
 };
+
+// Modes whose K-splits form one thread-block cluster and are summed through distributed
+// shared memory; such a cluster has 1, 2 or 4 CTAs.
+inline bool gemm_mode_clustered(int mode) { return mode == GEMM_QKV; }
+constexpr int kMaxClusterSplits = 4;
 
 struct GemmArgs {
   int mode;
@@ -48,7 +67,7 @@ struct GemmArgs {
   int nbox;          // rows of the B tile = MMA N (16..256, multiple of 16)
   int a_rows;        // rows of the A tensor (tiles at or beyond are skipped)
   int k_blocks;      // K / 64
-  int splits;        // split-K factor (grid.y)
+  int splits;        // split-K factor (grid.y); the cluster size in the clustered modes
   int w_stages, x_stages;  // depth of the weight and activation smem rings
   uint32_t a_tile_bytes, w_slot_bytes, x_slot_bytes;
   int T;             // valid token rows
@@ -60,6 +79,13 @@ struct GemmArgs {
   size_t split_stride;  // RED_ADD partials: elements between splits
   bf16* out_bf16;    int ldh;
   float* part_m; float* part_s; int* part_i; int part_ld;
+  // QKV: A rows are [H q heads | Hk k heads | Hk v heads] x dh.  Token row t is position
+  // t % Bq of its branch, at absolute position *dP + t % Bq.  q -> [T][H][dh]; k/v ->
+  // kdst/vdst row t ([T][Hk][dh]) or, with kv_to_cache, cache row *dP + t % Bq.
+  bf16* q; bf16* kdst; bf16* vdst;
+  const float* cos_t; const float* sin_t;  // [positions][dh/2]
+  const int* dP;
+  int H, Hk, dh, Bq, kv_to_cache;
   int* err;
   int w_packed;      // weight operand in tile-major layout (see launch_pack_tiles)
 };
@@ -96,6 +122,9 @@ cudaError_t pointwise_set_carveout();
 cudaError_t decide_set_carveout();
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s);
 cudaError_t gemm_set_smem_limits();
+// Clusters of `cs` GEMM CTAs (with `smem` bytes of dynamic shared memory each) that can
+// be resident at once; 0 if such clusters cannot be launched.
+int gemm_cluster_capacity(int mode, int cs, size_t smem);
 int gemm_max_smem();
 
 // ------------------------------------------------------------------ attention
@@ -116,11 +145,7 @@ cudaError_t attention_set_smem_limits();
 // ------------------------------------------------------------------ pointwise
 cudaError_t launch_embed_norm(const int* tok, int T, const bf16* E, const bf16* g, float* x,
                               bf16* n, int d, float eps, cudaStream_t s);
-cudaError_t launch_rope_prewrite(const float* qkv, int nsplit, size_t split_stride, int T, int H,
-                                 int Hk, int dh, bf16* q, bf16* kdst, bf16* vdst,
-                                 int kv_to_cache, int Bq, const float* cos_t, const float* sin_t,
-                                 const int* dP, cudaStream_t s);
-// x[t] += sum over splits of part[s][t]; n[t] = bf16(rmsnorm(x[t]) * g).
+// x[t] += sum over splits of part[s][t] (split order); n[t] = bf16(rmsnorm(x[t]) * g).
 cudaError_t launch_residual_norm(float* x, const float* part, int nsplit, size_t split_stride,
                                  const bf16* g, bf16* n, int T, int d, float eps, cudaStream_t s);
 cudaError_t launch_lm_merge(const float* pm, const float* ps, const int* pi, int nvt,

@@ -68,6 +68,7 @@ struct lopa_ctx {
   cudaStream_t stream = nullptr;
   bool own_stream = false;
   int num_sms = 0;
+  int ccap[kMaxClusterSplits + 1] = {};  // resident clusters of 1, 2, 4 q/k/v-GEMM CTAs
   // borrowed weights
   const bf16 *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
   std::vector<const bf16*> attn_norm, wqkv, wo, mlp_norm, wgu, wd;
@@ -76,7 +77,7 @@ struct lopa_ctx {
   bf16 *kc = nullptr, *vc = nullptr, *ks = nullptr, *vs = nullptr;
   float* x = nullptr;
   bf16* n = nullptr;
-  float* part = nullptr;  // split-K partial sums [split][T][N] of the projections
+  float* part = nullptr;  // split-K partial sums [split][T][d] of the O and down projections
   size_t part_floats = 0;
   bf16 *q = nullptr, *attn = nullptr, *hm = nullptr;
   float *pm = nullptr, *ps = nullptr;
@@ -148,7 +149,7 @@ int pick_splits(int tiles, int k_blocks, int num_sms) {
   return std::max(s, 1);
 }
 
-// Weight tiles per CTA and split count of a projection over T token rows.
+// Weight tiles per CTA and split count of a split-K projection over T token rows.
 void proj_tiling(int nrows, int K, int T, int num_sms, int* na, int* splits) {
   const int tok_box = std::min(256, round16(T));
   const int zt = (T + tok_box - 1) / tok_box;
@@ -157,20 +158,42 @@ void proj_tiling(int nrows, int K, int T, int num_sms, int* na, int* splits) {
   *splits = pick_splits(tiles, K / 64, num_sms);
 }
 
-// Floats of split-K partials a forward over T rows needs.
-size_t partial_floats(const lopa_ctx* ctx, int T);
-
+// Floats of split-K partials a forward over T rows needs (output and down projections).
 size_t partial_floats(const lopa_ctx* ctx, int T) {
   const lopa_model_config& m = ctx->mc;
-  const int rows[3] = {ctx->qkv_rows, m.d_model, m.d_model};
-  const int Ks[3] = {m.d_model, m.n_heads * m.head_dim, m.ffn};
+  const int Ks[2] = {m.n_heads * m.head_dim, m.ffn};
   size_t need = 0;
-  for (int i = 0; i < 3; ++i) {
+  for (int i = 0; i < 2; ++i) {
     int na, splits;
-    proj_tiling(rows[i], Ks[i], T, ctx->num_sms, &na, &splits);
-    need = std::max(need, (size_t)splits * T * rows[i]);
+    proj_tiling(m.d_model, Ks[i], T, ctx->num_sms, &na, &splits);
+    need = std::max(need, (size_t)splits * T * m.d_model);
   }
   return need;
+}
+
+// Tiling of the clustered q/k/v GEMM over T token rows: na weight tiles (128 rows each)
+// per CTA and cs K-splits per output tile, the splits of a tile forming one cluster.
+// Picks the most CTAs that are resident at once (all tiles in one wave), then the larger
+// na (fewer activation re-reads), then the smaller cluster (less exchange).  When no
+// choice fits one wave, na = 2 and cs = 1.
+void qkv_tiling(const lopa_ctx* ctx, int nrows, int K, int T, int* na, int* cs) {
+  const int tok_box = std::min(256, round16(T));
+  const int zt = (T + tok_box - 1) / tok_box;
+  int best = 0;
+  *na = 2;
+  *cs = 1;
+  for (int n = 2; n >= 1; --n) {
+    const int tiles = ((nrows + n * 128 - 1) / (n * 128)) * zt;
+    for (int c = 1; c <= kMaxClusterSplits; c *= 2) {
+      if (c > 1 && c > K / 64 / 2) break;
+      if (tiles > ctx->ccap[c]) continue;
+      if (tiles * c > best) {
+        best = tiles * c;
+        *na = n;
+        *cs = c;
+      }
+    }
+  }
 }
 
 int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm, const int* tok,
@@ -190,12 +213,12 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
   p.o.resize(L);
   p.gu.resize(L);
   p.dn.resize(L);
-  const int zt = (p.T + p.tok_box - 1) / p.tok_box;
-  (void)zt;
   auto plan = [&](GemmLaunch& G, int mode, const void* act, int K, const void* w, int nrows,
                   const char* what) -> int {
-    int na = 1, splits = 1;
-    if (mode == GEMM_RED_ADD) {
+    int na = 2, splits = 1;
+    if (mode == GEMM_QKV) {
+      qkv_tiling(ctx, nrows, K, p.T, &na, &splits);
+    } else if (mode == GEMM_RED_ADD) {
       proj_tiling(nrows, K, p.T, ctx->num_sms, &na, &splits);
       while (splits > 1 && (size_t)splits * p.T * nrows > ctx->part_floats) --splits;
     }
@@ -215,7 +238,19 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
   };
   for (int l = 0; l < L; ++l) {
     int r;
-    if ((r = plan(p.qkv[l], GEMM_RED_ADD, ctx->n, d, ctx->wqkv[l], ctx->qkv_rows, "qkv"))) return r;
+    if ((r = plan(p.qkv[l], GEMM_QKV, ctx->n, d, ctx->wqkv[l], ctx->qkv_rows, "qkv"))) return r;
+    GemmArgs& qa = p.qkv[l].args;
+    qa.q = ctx->q;
+    qa.kdst = kv_to_cache ? ctx->kc + (size_t)l * ctx->cache_layer : ctx->ks + (size_t)l * ctx->scr_layer;
+    qa.vdst = kv_to_cache ? ctx->vc + (size_t)l * ctx->cache_layer : ctx->vs + (size_t)l * ctx->scr_layer;
+    qa.cos_t = ctx->cos_t;
+    qa.sin_t = ctx->sin_t;
+    qa.dP = &ctx->st->P;
+    qa.H = H;
+    qa.Hk = m.n_kv_heads;
+    qa.dh = dh;
+    qa.Bq = Bq;
+    qa.kv_to_cache = kv_to_cache;
     if ((r = plan(p.o[l], GEMM_RED_ADD, ctx->attn, H * dh, ctx->wo[l], d, "o"))) return r;
     if ((r = plan(p.gu[l], GEMM_SWIGLU, ctx->n, d, ctx->wgu[l], 2 * F, "gate/up"))) return r;
     p.gu[l].args.out_bf16 = ctx->hm;
@@ -247,22 +282,16 @@ int enqueue_forward(lopa_ctx* ctx, const Plan& p) {
   cudaStream_t s = ctx->stream;
   CK(launch_embed_norm(p.tok, p.T, ctx->embed, ctx->attn_norm[0], ctx->x, ctx->n, d, m.rms_eps, s));
   for (int l = 0; l < L; ++l) {
-    bf16* kcl = ctx->kc + (size_t)l * ctx->cache_layer;
-    bf16* vcl = ctx->vc + (size_t)l * ctx->cache_layer;
-    bf16* ksl = ctx->ks + (size_t)l * ctx->scr_layer;
-    bf16* vsl = ctx->vs + (size_t)l * ctx->scr_layer;
-    CK(launch_gemm(p.qkv[l], s));
-    CK(launch_rope_prewrite(ctx->part, p.qkv[l].args.splits, p.qkv[l].args.split_stride, p.T, H,
-                            Hk, dh, ctx->q, p.kv_to_cache ? kcl : ksl,
-                            p.kv_to_cache ? vcl : vsl, p.kv_to_cache, p.Bq, ctx->cos_t, ctx->sin_t,
-                            &ctx->st->P, s));
+    const bf16* kcl = ctx->kc + (size_t)l * ctx->cache_layer;
+    const bf16* vcl = ctx->vc + (size_t)l * ctx->cache_layer;
+    CK(launch_gemm(p.qkv[l], s));  // q, k, v + RoPE; K/V Pre-Write
     AttnArgs aa;
     aa.q = ctx->q;
     aa.out = ctx->attn;
     aa.kc = kcl;
     aa.vc = vcl;
-    aa.kb = ksl;
-    aa.vb = vsl;
+    aa.kb = ctx->ks + (size_t)l * ctx->scr_layer;
+    aa.vb = ctx->vs + (size_t)l * ctx->scr_layer;
     aa.dP = &ctx->st->P;
     aa.pk_add = p.kv_to_cache ? p.T : 0;
     aa.Bq = p.Bq;
@@ -272,11 +301,11 @@ int enqueue_forward(lopa_ctx* ctx, const Plan& p) {
     aa.H = H;
     aa.Hk = Hk;
     CK(launch_attention(aa, dh, s));
-    CK(launch_gemm(p.o[l], s));
+    CK(launch_gemm(p.o[l], s));  // split-K partials of attn . Wo^T
     CK(launch_residual_norm(ctx->x, ctx->part, p.o[l].args.splits, p.o[l].args.split_stride,
                             ctx->mlp_norm[l], ctx->n, p.T, d, m.rms_eps, s));
     CK(launch_gemm(p.gu[l], s));
-    CK(launch_gemm(p.dn[l], s));
+    CK(launch_gemm(p.dn[l], s));  // split-K partials of h . Wd^T
     CK(launch_residual_norm(ctx->x, ctx->part, p.dn[l].args.splits, p.dn[l].args.split_stride,
                             l + 1 < L ? ctx->attn_norm[l + 1] : ctx->final_norm, ctx->n, p.T, d,
                             m.rms_eps, s));
@@ -341,6 +370,7 @@ int validate(const lopa_model_config* c, const lopa_decode_config* d) {
   if (c->d_model % 128 || c->ffn % 128 || ((c->n_heads + 2 * c->n_kv_heads) * c->head_dim) % 128 ||
       (c->n_heads * c->head_dim) % 64)
     return fail(ctx, LOPA_ERR_UNSUPPORTED, "d_model, ffn and q/k/v rows must be multiples of 128");
+  if (c->d_model > 4096) return fail(ctx, LOPA_ERR_UNSUPPORTED, "d_model must be <= 4096");
   if (c->mask_id < 0 || c->mask_id >= c->vocab) return fail(ctx, LOPA_ERR_INVALID_ARG, "mask_id out of range");
   if (!(c->rms_eps >= 0.f) || !(c->rope_base > 0.f) || !std::isfinite(c->logit_scale))
     return fail(ctx, LOPA_ERR_INVALID_ARG, "bad rms_eps / rope_base / logit_scale");
@@ -366,6 +396,9 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
   if (major != 10) return fail(ctx, LOPA_ERR_UNSUPPORTED, "needs an sm_10x GPU (found sm_%d%d)", major, minor);
   CK(gemm_set_smem_limits());
   CK(attention_set_smem_limits());
+  for (int c = 1; c <= kMaxClusterSplits; c *= 2)
+    ctx->ccap[c] = gemm_cluster_capacity(GEMM_QKV, c, (size_t)gemm_max_smem());
+  if (ctx->ccap[1] < 1) return fail(ctx, LOPA_ERR_UNSUPPORTED, "projection GEMM cannot be resident");
   if (!ctx->stream) {
     CK(cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking));
     ctx->own_stream = true;

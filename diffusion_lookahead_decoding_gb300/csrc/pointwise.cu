@@ -1,5 +1,5 @@
-// Memory-bound kernels of the verification forward: embedding + RMSNorm, RMSNorm,
-// RoPE + K/V Pre-Write, the LM-head partial merge, and the RoPE table.
+// Memory-bound kernels of the verification forward: embedding + RMSNorm, split-K sum +
+// residual add + RMSNorm, the LM-head partial merge, and the RoPE table.
 #include "common.cuh"
 #include "internal.h"
 
@@ -58,82 +58,6 @@ __global__ void embed_norm_kernel(const int* __restrict__ tok, int T, const bf16
   }
 }
 
-// Sums 4 consecutive floats over the split-K partials, in split order, with the loads
-// issued eight at a time.
-__device__ __forceinline__ float4 sum_splits4(const float* p, int nsplit, size_t stride) {
-  float4 a = *reinterpret_cast<const float4*>(p);
-  for (int s0 = 1; s0 < nsplit; s0 += 8) {
-    float4 q[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (s0 + u < nsplit) q[u] = *reinterpret_cast<const float4*>(p + (size_t)(s0 + u) * stride);
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (s0 + u < nsplit) {
-        a.x += q[u].x; a.y += q[u].y; a.z += q[u].z; a.w += q[u].w;
-      }
-  }
-  return a;
-}
-
-__device__ __forceinline__ void store4_bf16(bf16* p, float a, float b, float c, float d) {
-  uint2 u;
-  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-  h[0] = __floats2bfloat162_rn(a, b);
-  h[1] = __floats2bfloat162_rn(c, d);
-  *reinterpret_cast<uint2*>(p) = u;
-}
-
-// Sums the q/k/v split-K partials of one token row, applies RoPE (rotate-half) to q and
-// k, rounds q/k/v to bf16, writes q to [T][H][dh] and k/v to their Pre-Write destination.
-// Row t is position i = t % Bq of branch b = t / Bq at absolute position P + i.  K/V go
-// to the branch scratch [b][i] or, when kv_to_cache, straight to the static cache row
-// P + i (prompt prefill).  One CTA per row; a work item is 4 consecutive elements of a
-// head (j..j+3 with their rotation partners j+dh/2..+3).
-__global__ void rope_prewrite_kernel(const float* __restrict__ qkv, int nsplit, size_t split_stride,
-                                     int T, int H, int Hk, int dh, bf16* __restrict__ q,
-                                     bf16* __restrict__ kdst, bf16* __restrict__ vdst,
-                                     int kv_to_cache, int Bq, const float* __restrict__ cos_t,
-                                     const float* __restrict__ sin_t, const int* __restrict__ dP) {
-  pdl_wait();
-  pdl_trigger();
-  const int t = blockIdx.x;
-  if (t >= T) return;
-  const int P = dP ? *dP : 0;
-  const int b = t / Bq, i = t - b * Bq;
-  const int pos = P + i;
-  const int half = dh / 2, hq = half / 4;
-  const int nqk = (H + Hk) * hq;  // 4-wide rotation items in q and k
-  const int nv = Hk * dh / 4;
-  const int row_w = (H + 2 * Hk) * dh;
-  const float* row = qkv + (size_t)t * row_w;
-  const size_t kv_row = kv_to_cache ? (size_t)(P + i) : (size_t)t;
-  const float* ct = cos_t + (size_t)pos * half;
-  const float* st = sin_t + (size_t)pos * half;
-  for (int e = threadIdx.x; e < nqk + nv; e += blockDim.x) {
-    if (e < nqk) {
-      const int head = e / hq, j = (e - head * hq) * 4;
-      const float* src = row + head * dh;
-      const float4 x1 = sum_splits4(src + j, nsplit, split_stride);
-      const float4 x2 = sum_splits4(src + j + half, nsplit, split_stride);
-      const float4 c = *reinterpret_cast<const float4*>(ct + j);
-      const float4 sn = *reinterpret_cast<const float4*>(st + j);
-      bf16* dst = head < H ? q + ((size_t)t * H + head) * dh
-                           : kdst + (kv_row * Hk + (head - H)) * dh;
-      store4_bf16(dst + j, x1.x * c.x - x2.x * sn.x, x1.y * c.y - x2.y * sn.y,
-                  x1.z * c.z - x2.z * sn.z, x1.w * c.w - x2.w * sn.w);
-      store4_bf16(dst + j + half, x2.x * c.x + x1.x * sn.x, x2.y * c.y + x1.y * sn.y,
-                  x2.z * c.z + x1.z * sn.z, x2.w * c.w + x1.w * sn.w);
-    } else {
-      const int e4 = (e - nqk) * 4;
-      const float4 v = sum_splits4(row + (H + Hk) * dh + e4, nsplit, split_stride);
-      store4_bf16(vdst + kv_row * Hk * dh + e4, v.x, v.y, v.z, v.w);
-    }
-  }
-  __syncthreads();
-  if (row_w % 32 == 0) discard_partial_row(row, split_stride, nsplit, row_w);
-}
-
 // Block-wide sum; every thread gets the total.  blockDim.x is a multiple of 32, <= 1024.
 __device__ __forceinline__ float block_sum(float v, float* red) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
@@ -145,53 +69,66 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
-// Sums nsplit float4 partials at p, p + stride, ... onto acc in split order.  Loads are
-// issued eight at a time so that they are in flight together.
-__device__ __forceinline__ void add_splits4(float4& acc, const float* p, int nsplit,
-                                            size_t stride) {
-  for (int s0 = 0; s0 < nsplit; s0 += 8) {
-    float4 q[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (s0 + u < nsplit) q[u] = *reinterpret_cast<const float4*>(p + (size_t)(s0 + u) * stride);
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (s0 + u < nsplit) {
-        acc.x += q[u].x; acc.y += q[u].y; acc.z += q[u].z; acc.w += q[u].w;
-      }
-  }
-}
-
-// x[t] += sum_s part[s][t] (splits added in order), then n[t] = bf16(rmsnorm(x[t]) * g).
-// One CTA per row, four columns per thread.
-__global__ void __launch_bounds__(1024)
+// x[t] += sum_s part[s][t] (splits added in order after x), then
+// n[t] = bf16(x[t] * rsqrt(mean(x[t]^2) + eps) * g).  One CTA per row, eight columns per
+// thread; the partial loads of four splits are in flight together, and two CTAs fit an
+// SM, so a 256-row batch is resident in one wave.  Consumed partials are dropped from L2.
+__global__ void __launch_bounds__(512, 2)
     residual_norm_kernel(float* __restrict__ x, const float* __restrict__ part, int nsplit,
                          size_t split_stride, const bf16* __restrict__ g, bf16* __restrict__ n,
-                         int T, int d, float eps) {
+                         int d, float eps) {
   __shared__ float red[32];
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;
-  const int c = threadIdx.x * 4;
+  const int c = threadIdx.x * 8;
   const bool active = c < d;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
   if (active) {
     float* xr = x + (size_t)t * d + c;
-    acc = *reinterpret_cast<const float4*>(xr);
-    add_splits4(acc, part + (size_t)t * d + c, nsplit, split_stride);
-    *reinterpret_cast<float4*>(xr) = acc;
+    a0 = *reinterpret_cast<const float4*>(xr);
+    a1 = *reinterpret_cast<const float4*>(xr + 4);
+    const float* p = part + (size_t)t * d + c;
+    for (int s0 = 0; s0 < nsplit; s0 += 4) {
+      float4 q0[4], q1[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (s0 + u < nsplit) {
+          const float* ps = p + (size_t)(s0 + u) * split_stride;
+          q0[u] = *reinterpret_cast<const float4*>(ps);
+          q1[u] = *reinterpret_cast<const float4*>(ps + 4);
+        }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (s0 + u < nsplit) {
+          a0.x += q0[u].x; a0.y += q0[u].y; a0.z += q0[u].z; a0.w += q0[u].w;
+          a1.x += q1[u].x; a1.y += q1[u].y; a1.z += q1[u].z; a1.w += q1[u].w;
+        }
+    }
+    *reinterpret_cast<float4*>(xr) = a0;
+    *reinterpret_cast<float4*>(xr + 4) = a1;
   }
-  float ss = acc.x * acc.x + acc.y * acc.y + acc.z * acc.z + acc.w * acc.w;
+  float ss = a0.x * a0.x + a0.y * a0.y + a0.z * a0.z + a0.w * a0.w;
+  ss += a1.x * a1.x + a1.y * a1.y + a1.z * a1.z + a1.w * a1.w;
   ss = block_sum(ss, red);  // also a barrier: every thread has read its partials
   const float rs = rsqrtf(ss / (float)d + eps);
   if (active) {
-    const uint2 gu = *reinterpret_cast<const uint2*>(g + c);
-    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gu);
-    const float2 g01 = __bfloat1622float2(g2[0]), g23 = __bfloat1622float2(g2[1]);
-    store4_bf16(n + (size_t)t * d + c, acc.x * rs * g01.x, acc.y * rs * g01.y, acc.z * rs * g23.x,
-                acc.w * rs * g23.y);
+    float gg[8], f[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    load8(g + c, gg);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = f[i] * rs * gg[i];
+    store8(n + (size_t)t * d + c, f);
   }
-  if (d % 32 == 0) discard_partial_row(part + (size_t)t * d, split_stride, nsplit, d);
+  // Drop the consumed partial rows from L2 without write-back (128-byte lines).
+  if (d % 32 == 0) {
+    const int lines = d / 32;
+    const float* rowp = part + (size_t)t * d;
+    for (int e = threadIdx.x; e < lines * nsplit; e += blockDim.x) {
+      const int sp = e / lines, l = e - sp * lines;
+      asm volatile("discard.global.L2 [%0], 128;" ::"l"(rowp + (size_t)sp * split_stride + (size_t)l * 32)
+                   : "memory");
+    }
+  }
 }
 
 struct Stat {
@@ -256,8 +193,8 @@ __global__ void rope_table_kernel(float* cos_t, float* sin_t, int S, int dh, dou
 
 cudaError_t pointwise_set_carveout() {
   const int c = cudaSharedmemCarveoutMaxShared;
-  const void* ks[] = {(const void*)embed_norm_kernel, (const void*)rope_prewrite_kernel,
-                      (const void*)residual_norm_kernel, (const void*)lm_merge_kernel};
+  const void* ks[] = {(const void*)embed_norm_kernel, (const void*)residual_norm_kernel,
+                      (const void*)lm_merge_kernel};
   for (const void* k : ks) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, c);
     if (e != cudaSuccess) return e;
@@ -271,20 +208,12 @@ cudaError_t launch_embed_norm(const int* tok, int T, const bf16* E, const bf16* 
                     eps);
 }
 
-cudaError_t launch_rope_prewrite(const float* qkv, int nsplit, size_t split_stride, int T, int H,
-                                 int Hk, int dh, bf16* q, bf16* kdst, bf16* vdst,
-                                 int kv_to_cache, int Bq, const float* cos_t, const float* sin_t,
-                                 const int* dP, cudaStream_t s) {
-  return launch_pdl(rope_prewrite_kernel, dim3(T), dim3(256), 0, s, qkv, nsplit, split_stride, T,
-                    H, Hk, dh, q, kdst, vdst, kv_to_cache, Bq, cos_t, sin_t, dP);
-}
-
 cudaError_t launch_residual_norm(float* x, const float* part, int nsplit, size_t split_stride,
                                  const bf16* g, bf16* n, int T, int d, float eps, cudaStream_t s) {
-  const int threads = ((d / 4 + 31) / 32) * 32;
-  if (threads > 1024) return cudaErrorInvalidValue;
+  const int threads = ((d / 8 + 31) / 32) * 32;
+  if (threads > 512 || d % 8 != 0) return cudaErrorInvalidValue;
   return launch_pdl(residual_norm_kernel, dim3(T), dim3(threads), 0, s, x, part, nsplit,
-                    split_stride, g, n, T, d, eps);
+                    split_stride, g, n, d, eps);
 }
 
 cudaError_t launch_lm_merge(const float* pm, const float* ps, const int* pi, int nvt,

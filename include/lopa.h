@@ -53,7 +53,7 @@ typedef struct lopa_ctx lopa_ctx; /* opaque; owned by the library */
  * rotate-half convention, grouped-query attention, SwiGLU MLP, untied LM head).
  * Kernel limits: head_dim in {32, 64, 128}; d_model, n_heads*head_dim and ffn
  * multiples of 64; (n_heads + 2*n_kv_heads)*head_dim, d_model and ffn multiples of
- * 128; n_heads a multiple of n_kv_heads. */
+ * 128; d_model <= 4096; n_heads a multiple of n_kv_heads. */
 typedef struct {
   int n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab;
   int mask_id;       /* token id of [MASK]; it is never predicted */
