@@ -83,7 +83,7 @@ SIGNATURES = {
     "lopa_lmhead_argmax_static": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                             C.c_float, C.c_int, C.c_void_p, C.c_void_p,
                                             C.c_void_p]),
-    "lopa_branch_attention": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int,
+    "lopa_branch_attention": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
                                         C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                         C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
 }

@@ -207,13 +207,25 @@ def lmhead_argmax(hidden: torch.Tensor, lm_head: torch.Tensor, logit_scale: floa
 
 
 def branch_attention(q, k_prefix, v_prefix, k_block, v_block):
-    """q [nb*B, H, dh], k/v_prefix [P, Hk, dh], k/v_block [nb, B, Hk, dh] (bf16, cuda)."""
+    """Branch-isolated attention on natural layouts: q [nb*B, H, dh], k/v_prefix [P, Hk, dh],
+    k/v_block [nb, B, Hk, dh] (bf16, cuda).  Returns out [nb*B, H*dh].
+
+    The library works on the verification forward's layouts (group-major q, values
+    transposed); this wrapper only rearranges the tensors (torch copies) before the call.
+    """
     nb, B, Hk, dh = k_block.shape
     H = q.shape[1]
+    G = H // Hk
     P = k_prefix.shape[0]
+    qg = q.reshape(nb * B, Hk, G, dh).permute(1, 0, 2, 3).contiguous()
+    ld = max(8, (P + 7) // 8 * 8)
+    vtp = torch.zeros(Hk * dh, ld, dtype=torch.bfloat16, device=q.device)
+    if P:
+        vtp[:, :P] = v_prefix.reshape(P, Hk * dh).t()
+    vtb = v_block.reshape(nb * B, Hk * dh).t().contiguous()
+    kp, kb = k_prefix.contiguous(), k_block.contiguous()
     out = torch.empty(nb * B, H * dh, dtype=torch.bfloat16, device=q.device)
     L.check(L.load().lopa_branch_attention(
-        q.data_ptr(), k_prefix.data_ptr() if P else None, v_prefix.data_ptr() if P else None, P,
-        k_block.data_ptr(), v_block.data_ptr(), nb, B, H, Hk, dh, out.data_ptr(),
-        _stream_ptr()))
+        qg.data_ptr(), kp.data_ptr() if P else None, vtp.data_ptr() if P else None, P, ld,
+        kb.data_ptr(), vtb.data_ptr(), nb, B, H, Hk, dh, out.data_ptr(), _stream_ptr()))
     return out

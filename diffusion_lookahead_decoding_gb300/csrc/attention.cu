@@ -7,13 +7,29 @@
 // ("Decoding-efficiency revolution" blog, section 3.3: a branch sees the prompt and its
 // own tokens, never another branch's).
 //
-// One CTA serves 64 query rows of one (branch, KV head): the rows are the (position,
-// head-in-group) pairs that share KV head g, so every K/V tile in shared memory serves all
-// query heads of the group (grouped-query attention).  Its 8 warps form two key groups of
-// 4 row-warps; key tiles of 64 alternate between the groups, each group double-buffers
-// its tiles with cp.async, and the two partial softmax states are merged at the end.
-// S = Q K^T and P V run on bf16 mma.sync with an fp32 online softmax; P enters P V as a
-// bf16 head plus a bf16 tail, which keeps its fp32 accuracy.
+// Layouts (written by the q/k/v projection epilogue):
+//   q      [Hk][T][G][dh]   group-major: the rows of KV head g are (token t, head-in-group
+//                           hg) pairs, t = b * Bq + i, so one K/V tile serves every query
+//                           head of the group (grouped-query attention);
+//   K      [pos][Hk][dh]    prefix cache; block keys [nb][Bk_stride][Hk][dh];
+//   V^T    [Hk*dh][ld]      values stored transposed (position innermost), so a V tile is
+//                           a K-major operand of P V;
+//   out    [T][H*dh].
+// Key tiles run over the prefix first, then over the block keys of the branches that a
+// CTA's rows belong to, with a per-row branch mask.
+//
+// head_dim 128 runs on the 5th-generation tensor cores (tcgen05): a CTA owns 128 query
+// rows (= TMEM lanes).  One warp streams Q once and K / V^T tiles of 64 keys with TMA;
+// one warp issues S = Q K^T into a double-buffered TMEM tile and O += P V into a TMEM
+// accumulator; the softmax warps (one thread per row and column half) run the online
+// softmax - reading S from
+// TMEM, writing P as a bf16 head and a bf16 tail (two MMAs keep P's fp32 accuracy) into
+// shared memory, and rescaling O in TMEM only when a row's running maximum grows by more
+// than 2^8 (the result is unchanged: O and the normaliser share the same reference).
+// Eight softmax warps: two per TMEM lane quarter, each on half of the 64 key columns.
+// head_dim 32 and 64 run on bf16 mma.sync with the same layouts.
+#include <cstring>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -21,8 +37,373 @@ namespace lopa {
 
 namespace {
 
-constexpr int kRowsPerCta = 64;
 constexpr int kKeyTile = 64;
+
+// Key-tile schedule shared by both kernels: prefix tiles [0, n_pre), then block-key
+// tiles covering the scratch columns [kb_lo, kb_end) of the branches in [b_lo, b_hi].
+struct KeySched {
+  int Pk, n_pre, kb_lo, n_br;
+};
+
+__device__ __forceinline__ KeySched key_sched(const AttnArgs& a, int b_lo, int b_hi) {
+  KeySched k;
+  k.Pk = a.pk_add + (a.dP ? *a.dP : 0);
+  k.n_pre = (k.Pk + kKeyTile - 1) / kKeyTile;
+  k.kb_lo = b_lo * a.Bk_stride;
+  const int kb_end = b_hi * a.Bk_stride + a.Bk;
+  k.n_br = a.Bk > 0 ? (kb_end - k.kb_lo + kKeyTile - 1) / kKeyTile : 0;
+  return k;
+}
+
+// Key columns [lo, hi) of tile j (tile-local) that a row of branch br may see: the
+// committed prefix, or the br-th branch's own block keys.
+__device__ __forceinline__ void visible_range(const AttnArgs& a, const KeySched& k, int j, int br,
+                                              int& lo, int& hi) {
+  if (j < k.n_pre) {
+    lo = 0;
+    hi = k.Pk - j * kKeyTile;
+    return;
+  }
+  lo = br * a.Bk_stride - (k.kb_lo + (j - k.n_pre) * kKeyTile);
+  hi = lo + a.Bk;
+}
+
+// 2^x on the special-function unit (ex2.approx: relative error about 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ================================================================ tcgen05 path (dh = 128)
+constexpr int kTcRows = 128;
+constexpr int kTcStages = 3;
+constexpr int kTcSoftWarps = 8;  // two per TMEM lane quarter, each on half the columns
+constexpr int kTcThreads = (2 + kTcSoftWarps) * 32;  // warp 0 TMA, warp 1 MMA, softmax
+constexpr uint32_t kTcQBytes = 128 * 128 * 2;   // two 64-column SW128 atoms of 16 KB
+constexpr uint32_t kTcKBytes = 64 * 128 * 2;    // two atoms of 8 KB
+constexpr uint32_t kTcVBytes = 128 * 64 * 2;    // V^T tile: 128 rows (dh) x 64 keys
+constexpr uint32_t kTcPBytes = 128 * 64 * 2;    // one P half (head or tail)
+constexpr uint32_t kTcStageBytes = kTcKBytes + kTcVBytes;
+constexpr uint32_t kTcOffKV = kTcQBytes;
+constexpr uint32_t kTcOffP = kTcOffKV + kTcStages * kTcStageBytes;
+constexpr uint32_t kTcOffTail = kTcOffP + 2 * 2 * kTcPBytes;
+constexpr float kLazyRescale = 8.0f;  // log2 units
+
+struct TcTail {
+  uint64_t qfull;
+  uint64_t kvfull[kTcStages], kvempty[kTcStages];
+  uint64_t sfull[2], sempty[2], pfull[2], pempty[2];
+  uint64_t odone;
+  float xmax[2][2][kTcRows];  // [tile parity][column half][row]: half-row maxima
+  float xsum[2][kTcRows];     // [column half][row]: half-row sums of P
+  uint32_t tmem;
+  int abort;
+};
+constexpr size_t kTcSmem = 1024 + kTcOffTail + sizeof(TcTail);
+
+struct TcMaps {
+  CUtensorMap q, kc, vtc, kb, vtb;
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    attn_tc_kernel(const __grid_constant__ TcMaps m, const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  TcTail* tail = reinterpret_cast<TcTail*>(smem + kTcOffTail);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.H / a.Hk;
+  const int T = a.nbq * a.Bq;
+  const int rows = T * G;  // query rows of this KV head
+  const int g = blockIdx.y;
+  const int R0 = blockIdx.x * kTcRows;
+  const int b_lo = (R0 / G) / a.Bq;
+  const int b_hi = (min(R0 + kTcRows, rows) - 1) / G / a.Bq;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&tail->qfull), 1);
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(smem_u32(&tail->kvfull[s]), 1);
+      mbar_init(smem_u32(&tail->kvempty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&tail->sfull[s]), 1);
+      mbar_init(smem_u32(&tail->sempty[s]), kTcSoftWarps * 32);
+      mbar_init(smem_u32(&tail->pfull[s]), kTcSoftWarps * 32);
+      mbar_init(smem_u32(&tail->pempty[s]), 1);
+    }
+    mbar_init(smem_u32(&tail->odone), 1);
+    tail->abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&m.q);
+    tma_prefetch_desc(&m.kc);
+    tma_prefetch_desc(&m.vtc);
+    tma_prefetch_desc(&m.kb);
+    tma_prefetch_desc(&m.vtb);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tail->tmem), 256);  // S0 [0,64), S1 [64,128), O [128,256)
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tail->tmem;
+  volatile int* abort = &tail->abort;
+  pdl_trigger();
+  pdl_wait();  // q and the block keys come from the previous kernel; out may be read by it
+  const KeySched ks = key_sched(a, b_lo, b_hi);
+  const int n = ks.n_pre + ks.n_br;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last(), once = policy_evict_first();
+      const uint32_t qf = smem_u32(&tail->qfull);
+      mbar_arrive_expect_tx(qf, kTcQBytes);
+      const int qy = g * rows + R0;
+      tma_load_2d(smem_u32(smem), &m.q, qf, 0, qy, once);
+      tma_load_2d(smem_u32(smem + kTcQBytes / 2), &m.q, qf, 64, qy, once);
+      for (int j = 0; j < n; ++j) {
+        const int s = j % kTcStages;
+        if (j >= kTcStages &&
+            !mbar_wait_bounded(smem_u32(&tail->kvempty[s]), (uint32_t)(j / kTcStages - 1) & 1u,
+                               abort, a.err, DEV_TIMEOUT_PRODUCER))
+          break;
+        const uint32_t fb = smem_u32(&tail->kvfull[s]);
+        const uint32_t kdst = smem_u32(smem + kTcOffKV + s * kTcStageBytes);
+        const uint32_t vdst = kdst + kTcKBytes;
+        mbar_arrive_expect_tx(fb, kTcStageBytes);
+        if (j < ks.n_pre) {
+          const int k0 = j * kKeyTile;
+          tma_load_2d(kdst, &m.kc, fb, g * 128, k0, keep);
+          tma_load_2d(kdst + kTcKBytes / 2, &m.kc, fb, g * 128 + 64, k0, keep);
+          tma_load_2d(vdst, &m.vtc, fb, k0, g * 128, keep);
+        } else {
+          const int c0 = ks.kb_lo + (j - ks.n_pre) * kKeyTile;
+          tma_load_2d(kdst, &m.kb, fb, g * 128, c0, keep);
+          tma_load_2d(kdst + kTcKBytes / 2, &m.kb, fb, g * 128 + 64, c0, keep);
+          tma_load_2d(vdst, &m.vtb, fb, c0, g * 128, keep);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16(128, kKeyTile);
+      const uint32_t idesc_o = idesc_bf16(128, 128);
+      bool ok = mbar_wait_bounded(smem_u32(&tail->qfull), 0, abort, a.err, DEV_TIMEOUT_MMA);
+      const uint32_t qs = smem_u32(smem);
+      for (int j = 0; ok && j <= n; ++j) {
+        if (j < n) {  // S_j = Q K_j^T
+          const int s = j % kTcStages, sb = j & 1;
+          if (!mbar_wait_bounded(smem_u32(&tail->kvfull[s]), (uint32_t)(j / kTcStages) & 1u, abort,
+                                 a.err, DEV_TIMEOUT_MMA) ||
+              (j >= 2 && !mbar_wait_bounded(smem_u32(&tail->sempty[sb]),
+                                            (uint32_t)((j >> 1) - 1) & 1u, abort, a.err,
+                                            DEV_TIMEOUT_MMA))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kbase = smem_u32(smem + kTcOffKV + s * kTcStageBytes);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = sw128_desc(qs + (kk >> 2) * (kTcQBytes / 2)) + 2 * (kk & 3);
+            const uint64_t bd = sw128_desc(kbase + (kk >> 2) * (kTcKBytes / 2)) + 2 * (kk & 3);
+            mma_bf16(tmem + (uint32_t)(sb * kKeyTile), ad, bd, idesc_s, kk > 0);
+          }
+          mma_commit(smem_u32(&tail->sfull[sb]));
+        }
+        if (j >= 1) {  // O += P_i V_i for i = j - 1, P as head + tail
+          const int i = j - 1, pb = i & 1, si = i % kTcStages;
+          if (!mbar_wait_bounded(smem_u32(&tail->pfull[pb]), (uint32_t)(i >> 1) & 1u, abort, a.err,
+                                 DEV_TIMEOUT_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vbase = smem_u32(smem + kTcOffKV + si * kTcStageBytes + kTcKBytes);
+          const uint32_t pbase = smem_u32(smem + kTcOffP + pb * 2 * kTcPBytes);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sw128_desc(pbase + h * kTcPBytes) + 2 * kk;
+              const uint64_t bd = sw128_desc(vbase) + 2 * kk;
+              mma_bf16(tmem + 128u, ad, bd, idesc_o, (i | h | kk) != 0);
+            }
+          }
+          mma_commit(smem_u32(&tail->kvempty[si]));
+          mma_commit(smem_u32(&tail->pempty[pb]));
+        }
+      }
+      if (ok) mma_commit(smem_u32(&tail->odone));
+    }
+  } else {
+    // Softmax + epilogue.  Warp w serves TMEM lane quarter q = w % 4 (query rows
+    // 32q..32q+31, one per lane) and column half h: S columns [32h, 32h+32) and O columns
+    // [64h, 64h+64); the two warps of a quarter exchange their half-row maxima through
+    // shared memory (named barrier 1 + q).  tcgen05.ld/st are warp-wide, so every decision
+    // guarding one is made uniform across the warp.
+    constexpr unsigned kAll = 0xffffffffu;
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int r = q * 32 + lane;
+    const int R = R0 + r;
+    const bool row_ok = R < rows;
+    const int t = row_ok ? R / G : 0;
+    const int hg = row_ok ? R - t * G : 0;
+    const int br = t / a.Bq;
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t o_base = lane_base + 128u + (uint32_t)(h * 64);
+    const float sl2 = 1.4426950408889634f / sqrtf(128.0f);  // log2(e) / sqrt(dh)
+    // Both warps of a quarter pass the same number of pair barriers: after a failed
+    // (bounded) wait a warp keeps iterating with its waits and TMEM accesses skipped
+    // (`ok` stays warp-uniform), so its partner is never left at a barrier.
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory"); };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      ok = ok && __all_sync(kAll, mbar_wait_bounded(smem_u32(bar), parity, abort, a.err,
+                                                    DEV_TIMEOUT_EPILOGUE));
+    };
+    for (int j = 0; j < n; ++j) {
+      const int sb = j & 1;
+      wait_all(&tail->sfull[sb], (uint32_t)(j >> 1) & 1u);
+      float sv[32];
+      if (ok) {
+        tc_fence_after();
+        float x0[16], x1[16];
+        tmem_ld16x2(lane_base + (uint32_t)(sb * 64 + h * 32), lane_base + (uint32_t)(sb * 64 + h * 32 + 16),
+                    x0, x1);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          sv[c] = x0[c];
+          sv[16 + c] = x1[c];
+        }
+        tc_fence_before();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sv[c] = -INFINITY;
+      }
+      mbar_arrive(smem_u32(&tail->sempty[sb]));  // S buffer may be overwritten
+      // Mask only where the tile is not wholly visible (the last prefix tile, block keys).
+      if (j >= ks.n_pre - 1) {
+        int vlo, vhi;
+        visible_range(a, ks, j, br, vlo, vhi);
+        vlo -= h * 32;
+        vhi -= h * 32;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (c < vlo || c >= vhi) sv[c] = -INFINITY;
+      }
+      float hm = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) hm = fmaxf(hm, sv[c]);
+      tail->xmax[sb][h][r] = hm;
+      pair_sync();
+      const float mx = fmaxf(hm, tail->xmax[sb][h ^ 1][r]) * sl2;  // row max, log2 units
+      // Lazy rescale: a row moves its reference maximum only when the tile maximum
+      // exceeds it by more than 2^8 (also at its first visible key).  O then holds
+      // P_0..P_{j-1} V relative to the old reference and is rescaled once P_{j-1} V has
+      // landed; the warp rescales together, rows that keep their reference with alpha = 1.
+      const bool need = mx > m_ref + kLazyRescale;
+      const bool need_o = need && m_ref != -INFINITY;  // only for j >= 1
+      const float alpha = need_o ? exp2f(m_ref - mx) : 1.f;
+      if (ok && __any_sync(kAll, need_o)) wait_all(&tail->pempty[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u);
+      if (ok && __any_sync(kAll, need_o)) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          float u[16], w[16];
+          tmem_ld16x2(o_base + c, o_base + c + 16, u, w);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            u[e] *= alpha;
+            w[e] *= alpha;
+          }
+          tmem_st16(o_base + c, u);
+          tmem_st16(o_base + c + 16, w);
+        }
+        tmem_st_wait();
+      }
+      if (need_o) l *= alpha;
+      if (need) m_ref = mx;
+      // P = 2^(s * sl2 - m_ref) (masked s = -inf gives 0) as bf16 head + bf16 tail, in the
+      // 128-byte-swizzled K-major layout of an MMA A operand (16-byte chunk c of row r at
+      // chunk c ^ (r % 8)).
+      if (j >= 2) wait_all(&tail->pempty[sb], (uint32_t)((j - 2) >> 1) & 1u);
+      uint8_t* ph = smem + kTcOffP + sb * 2 * kTcPBytes + r * 128;
+      uint8_t* pt = ph + kTcPBytes;
+      const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        uint4 hv, tv;
+        uint32_t* hw = reinterpret_cast<uint32_t*>(&hv);
+        uint32_t* tw = reinterpret_cast<uint32_t*>(&tv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = ex2_approx(fmaf(sv[c8 * 8 + 2 * e], sl2, nm));
+          const float p1 = ex2_approx(fmaf(sv[c8 * 8 + 2 * e + 1], sl2, nm));
+          l += p0 + p1;
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          const float2 hf = __bfloat1622float2(h2);
+          const __nv_bfloat162 t2 = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+          hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          tw[e] = *reinterpret_cast<const uint32_t*>(&t2);
+        }
+        const int off = ((h * 4 + c8) ^ (r & 7)) << 4;
+        *reinterpret_cast<uint4*>(ph + off) = hv;
+        *reinterpret_cast<uint4*>(pt + off) = tv;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();  // orders any O rescale (tcgen05.st) before the P V MMAs
+      mbar_arrive(smem_u32(&tail->pfull[sb]));
+    }
+    // Epilogue: out row = O / l in bf16 (a row that saw no key is written as zeros); l is
+    // the sum of the two half-row sums, which share the row's reference maximum.
+    const bool got = ok && n > 0 &&
+                     mbar_wait_bounded(smem_u32(&tail->odone), 0, abort, a.err, DEV_TIMEOUT_EPILOGUE);
+    const bool have_o = __all_sync(kAll, got);
+    tc_fence_after();
+    tail->xsum[h][r] = l;
+    pair_sync();
+    const float lt = l + tail->xsum[h ^ 1][r];
+    const float inv = lt > 0.f ? 1.0f / lt : 0.f;
+    bf16* orow = a.out + ((size_t)t * a.H + g * G + hg) * 128 + h * 64;
+#pragma unroll
+    for (int c = 0; c < 64; c += 32) {
+      float u[16], w[16];
+      if (have_o) {
+        tmem_ld16x2(o_base + c, o_base + c + 16, u, w);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) u[e] = w[e] = 0.f;
+      }
+      uint4 o4[4];
+      uint32_t* ow = reinterpret_cast<uint32_t*>(o4);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const __nv_bfloat162 v0 = __floats2bfloat162_rn(u[2 * e] * inv, u[2 * e + 1] * inv);
+        const __nv_bfloat162 v1 = __floats2bfloat162_rn(w[2 * e] * inv, w[2 * e + 1] * inv);
+        ow[e] = *reinterpret_cast<const uint32_t*>(&v0);
+        ow[8 + e] = *reinterpret_cast<const uint32_t*>(&v1);
+      }
+      if (row_ok) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) reinterpret_cast<uint4*>(orow + c)[e] = o4[e];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ================================================================ mma.sync path (dh 32, 64)
+constexpr int kRowsPerCta = 64;
 constexpr int kThreads = 256;
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4],
@@ -39,6 +420,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 16-byte async copy; bytes < 16 zero-fills the rest (bytes = 0: a zero chunk).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
                : "memory");
@@ -54,12 +436,22 @@ __device__ __forceinline__ void cp_async_wait() {
 __device__ __forceinline__ void group_sync(int kg) {
   asm volatile("bar.sync %0, 128;" ::"r"(1 + kg) : "memory");
 }
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
 
+// One CTA serves 64 query rows of one (branch, KV head).  Its 8 warps form two key groups
+// of 4 row-warps; key tiles alternate between the groups, each group double-buffers its
+// K and V^T tiles with cp.async, and the two partial softmax states are merged at the end.
 template <int DH>
-__global__ void __launch_bounds__(kThreads) attn_kernel(const AttnArgs a) {
-  constexpr int PITCH = DH + 8;  // bf16/f16 elements per smem row (breaks bank conflicts)
-  constexpr int TILE = kKeyTile * PITCH;
-  constexpr int CH = DH / 8;     // 16-byte chunks per key row
+__global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnArgs a) {
+  constexpr int KP = DH + 8;        // K tile row pitch (elements)
+  constexpr int VP = kKeyTile + 8;  // V^T tile row pitch
+  constexpr int KT = kKeyTile * KP, VT = DH * VP;
+  constexpr int CH = DH / 8;        // 16-byte chunks per key row
   extern __shared__ __align__(16) uint8_t smem_raw[];
   bf16* sm = reinterpret_cast<bf16*>(smem_raw);
 
@@ -70,35 +462,35 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnArgs a) {
   const int grp = lane >> 2, tig = lane & 3;
   const int b = blockIdx.z, g = blockIdx.y;
   const int G = a.H / a.Hk;
-  const int rows = a.Bq * G;
-  const int Pk = a.pk_add + (a.dP ? *a.dP : 0);
-  const int nkeys = Pk + a.Bk;
-  const int ntiles = (nkeys + kKeyTile - 1) / kKeyTile;
+  const int T = a.nbq * a.Bq;
+  const int rows = a.Bq * G;  // rows of this (branch, KV head)
+  const KeySched ks = key_sched(a, b, b);
+  const int ntiles = ks.n_pre + ks.n_br;
   const int my_tiles = ntiles > kg ? (ntiles - kg + 1) / 2 : 0;
   const float sl2 = 1.4426950408889634f / sqrtf((float)DH);  // log2(e) / sqrt(dh)
-  // This key group's buffers: K of buffer j at (4kg + 2j) tiles, V right after it.
-  auto Kb = [&](int j) { return sm + (kg * 4 + 2 * j) * TILE; };
-  auto Vb = [&](int j) { return sm + (kg * 4 + 2 * j + 1) * TILE; };
+  // This key group's buffers: K of buffer j, then V^T of buffer j.
+  auto Kb = [&](int j) { return sm + (kg * 2 + j) * (KT + VT); };
+  auto Vb = [&](int j) { return sm + (kg * 2 + j) * (KT + VT) + KT; };
 
   auto load_tile = [&](int tile, int buf) {
+    const bool pre = tile < ks.n_pre;
+    const int base = pre ? tile * kKeyTile : ks.kb_lo + (tile - ks.n_pre) * kKeyTile;
+    const int lim = pre ? ks.Pk : b * a.Bk_stride + a.Bk;  // first invisible column
     for (int c = gtid; c < kKeyTile * CH; c += 128) {
       const int key = c / CH, col = (c - key * CH) * 8;
-      const int kk = tile * kKeyTile + key;
-      const bf16 *ks = a.kb, *vs = a.vb;
-      int bytes = 0;
-      if (kk < Pk) {
-        const size_t off = ((size_t)kk * a.Hk + g) * DH + col;
-        ks = a.kc + off;
-        vs = a.vc + off;
-        bytes = 16;
-      } else if (kk < nkeys) {
-        const size_t off = (((size_t)b * a.Bk_stride + (kk - Pk)) * a.Hk + g) * DH + col;
-        ks = a.kb + off;
-        vs = a.vb + off;
-        bytes = 16;
-      }
-      cp_async16(smem_u32(Kb(buf) + key * PITCH + col), ks, bytes);  // bytes 0 -> zeros
-      cp_async16(smem_u32(Vb(buf) + key * PITCH + col), vs, bytes);
+      const int kk = base + key;
+      const bf16* src = pre ? a.kc + ((size_t)kk * a.Hk + g) * DH + col
+                            : a.kb + ((size_t)kk * a.Hk + g) * DH + col;
+      const bool in = kk < lim;
+      cp_async16(smem_u32(Kb(buf) + key * KP + col), in ? src : a.kb, in ? 16 : 0);
+    }
+    for (int c = gtid; c < DH * (kKeyTile / 8); c += 128) {
+      const int d = c >> 3, k8 = (c & 7) * 8;
+      const int kk = base + k8;
+      const int nv = min(max(lim - kk, 0), 8);
+      const bf16* src = pre ? a.vtc + (size_t)(g * DH + d) * a.ldvc + kk
+                            : a.vtb + (size_t)(g * DH + d) * a.ldvb + kk;
+      cp_async16(smem_u32(Vb(buf) + d * VP + k8), nv > 0 ? src : a.kb, nv * 2);
     }
     cp_async_commit();
   };
@@ -112,8 +504,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnArgs a) {
     for (int h2 = 0; h2 < 2; ++h2) {
       int r = row0 + grp + h2 * 8;
       r = r < rows ? r : rows - 1;
-      const int i = r / G, hg = r - i * G;
-      qrow[h2] = a.q + ((size_t)(b * a.Bq + i) * a.H + g * G + hg) * DH;
+      qrow[h2] = a.q + ((size_t)g * T * G + (size_t)b * a.Bq * G + r) * DH;
     }
 #pragma unroll
     for (int kc = 0; kc < DH / 16; ++kc) {
@@ -142,27 +533,32 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnArgs a) {
     group_sync(kg);
     const bf16* Ks = Kb(buf);
     const bf16* Vs = Vb(buf);
-    const int kt = tile * kKeyTile;
 
+    // S = Q K^T; one ldmatrix.x4 fetches the B fragments of two 8-key groups.
     float s[8][4];
 #pragma unroll
     for (int ng = 0; ng < 8; ++ng) s[ng][0] = s[ng][1] = s[ng][2] = s[ng][3] = 0.f;
 #pragma unroll
     for (int kc = 0; kc < DH / 16; ++kc) {
 #pragma unroll
-      for (int ng = 0; ng < 8; ++ng) {
-        const bf16* kp = Ks + (ng * 8 + grp) * PITCH + kc * 16 + 2 * tig;
-        mma_bf16_16816(s[ng], qa[kc], *reinterpret_cast<const uint32_t*>(kp),
-                       *reinterpret_cast<const uint32_t*>(kp + 8));
+      for (int np = 0; np < 4; ++np) {
+        const int mi = lane >> 3;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(smem_u32(Ks + (np * 16 + (mi >> 1) * 8 + (lane & 7)) * KP + kc * 16 + (mi & 1) * 8),
+                b0, b1, b2, b3);
+        mma_bf16_16816(s[2 * np], qa[kc], b0, b1);
+        mma_bf16_16816(s[2 * np + 1], qa[kc], b2, b3);
       }
     }
+    int vlo, vhi;
+    visible_range(a, ks, tile, b, vlo, vhi);
     float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int ng = 0; ng < 8; ++ng) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int key = kt + ng * 8 + 2 * tig + (e & 1);
-        const float v = key < nkeys ? s[ng][e] * sl2 : -INFINITY;
+        const int c = ng * 8 + 2 * tig + (e & 1);
+        const float v = (c >= vlo && c < vhi) ? s[ng][e] * sl2 : -INFINITY;
         s[ng][e] = v;
         tmax[e >> 1] = fmaxf(tmax[e >> 1], v);
       }
@@ -173,7 +569,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnArgs a) {
       tmax[h2] = fmaxf(tmax[h2], __shfl_xor_sync(0xffffffffu, tmax[h2], 1));
       tmax[h2] = fmaxf(tmax[h2], __shfl_xor_sync(0xffffffffu, tmax[h2], 2));
       const float mnew = fmaxf(mrow[h2], tmax[h2]);
-      alpha[h2] = exp2f(mrow[h2] - mnew);  // 0 on the first tile (mrow = -inf)
+      alpha[h2] = mnew == -INFINITY ? 1.f : exp2f(mrow[h2] - mnew);
       mrow[h2] = mnew;
       lrow[h2] *= alpha[h2];
     }
@@ -182,40 +578,45 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnArgs a) {
       o[j][0] *= alpha[0]; o[j][1] *= alpha[0];
       o[j][2] *= alpha[1]; o[j][3] *= alpha[1];
     }
-    // P = hi + lo with both parts bf16 (16 significant bits): P V keeps fp32-level
-    // accuracy, so the bf16 rounding of the attention output matches an exact softmax.
+    // P = head + tail, both bf16 (16 significant bits): P V keeps fp32-level accuracy.
     uint32_t pa[4][4], pl[4][4];
 #pragma unroll
     for (int ng = 0; ng < 8; ++ng) {
-      const float p0 = exp2f(s[ng][0] - mrow[0]), p1 = exp2f(s[ng][1] - mrow[0]);
-      const float p2 = exp2f(s[ng][2] - mrow[1]), p3 = exp2f(s[ng][3] - mrow[1]);
-      lrow[0] += p0 + p1;
-      lrow[1] += p2 + p3;
+      float p[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        p[e] = s[ng][e] == -INFINITY ? 0.f : exp2f(s[ng][e] - mrow[e >> 1]);
+      lrow[0] += p[0] + p[1];
+      lrow[1] += p[2] + p[3];
       const int kc2 = ng >> 1, hi = ng & 1;
-      const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
-      const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
+      const __nv_bfloat162 h01 = __floats2bfloat162_rn(p[0], p[1]);
+      const __nv_bfloat162 h23 = __floats2bfloat162_rn(p[2], p[3]);
       const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
       pa[kc2][hi * 2 + 0] = *reinterpret_cast<const uint32_t*>(&h01);
       pa[kc2][hi * 2 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
-      pl[kc2][hi * 2 + 0] = pack_bf16(p0 - f01.x, p1 - f01.y);
-      pl[kc2][hi * 2 + 1] = pack_bf16(p2 - f23.x, p3 - f23.y);
+      pl[kc2][hi * 2 + 0] = pack_bf16(p[0] - f01.x, p[1] - f01.y);
+      pl[kc2][hi * 2 + 1] = pack_bf16(p[2] - f23.x, p[3] - f23.y);
     }
+    // O += P V, 16 keys at a time; V^T rows are (dh) with keys contiguous, so the B
+    // fragments come from non-transposing ldmatrix.
 #pragma unroll
     for (int kc2 = 0; kc2 < 4; ++kc2) {
+      uint32_t vf[DH / 16][4];
 #pragma unroll
       for (int dg = 0; dg < DH / 16; ++dg) {
         const int mi = lane >> 3;
-        const int key = kc2 * 16 + (mi & 1) * 8 + (lane & 7);
-        const int col = dg * 16 + (mi >> 1) * 8;
-        const uint32_t addr = smem_u32(Vs + key * PITCH + col);
-        uint32_t r0, r1, r2, r3;
-        asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                     : "r"(addr));
-        mma_bf16_16816(o[2 * dg], pa[kc2], r0, r1);
-        mma_bf16_16816(o[2 * dg + 1], pa[kc2], r2, r3);
-        mma_bf16_16816(o[2 * dg], pl[kc2], r0, r1);
-        mma_bf16_16816(o[2 * dg + 1], pl[kc2], r2, r3);
+        ldsm_x4(smem_u32(Vs + (dg * 16 + (mi >> 1) * 8 + (lane & 7)) * VP + kc2 * 16 + (mi & 1) * 8),
+                vf[dg][0], vf[dg][1], vf[dg][2], vf[dg][3]);
+      }
+#pragma unroll
+      for (int dg = 0; dg < DH / 16; ++dg) {
+        mma_bf16_16816(o[2 * dg], pa[kc2], vf[dg][0], vf[dg][1]);
+        mma_bf16_16816(o[2 * dg + 1], pa[kc2], vf[dg][2], vf[dg][3]);
+      }
+#pragma unroll
+      for (int dg = 0; dg < DH / 16; ++dg) {
+        mma_bf16_16816(o[2 * dg], pl[kc2], vf[dg][0], vf[dg][1]);
+        mma_bf16_16816(o[2 * dg + 1], pl[kc2], vf[dg][2], vf[dg][3]);
       }
     }
     group_sync(kg);  // this buffer is refilled two tiles later
@@ -248,7 +649,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnArgs a) {
     float l = lrow[h2] * sc0[h2] + mine[DH / 2 + 2 + h2] * sc1[h2];
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
-    lrow[h2] = 1.0f / l;
+    lrow[h2] = l > 0.f ? 1.0f / l : 0.f;
   }
   // Stage the CTA's 64 x DH output tile in shared memory (behind the exchange area), then
   // write whole rows with 16-byte stores.
@@ -275,44 +676,87 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnArgs a) {
 }
 
 template <int DH>
-constexpr size_t attn_smem() {
-  return (size_t)8 * kKeyTile * (DH + 8) * sizeof(bf16);
+constexpr size_t attn_mma_smem() {
+  return (size_t)4 * (kKeyTile * (DH + 8) + DH * (kKeyTile + 8)) * sizeof(bf16);
 }
 
 }  // namespace
 
 cudaError_t attention_set_smem_limits() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(attn_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)attn_smem<32>())) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(attn_mma_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)attn_mma_smem<32>())) != cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)attn_smem<64>())) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)attn_mma_smem<64>())) != cudaSuccess)
     return e;
-  return cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)attn_smem<128>());
+  return cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kTcSmem);
 }
 
 cudaError_t attention_set_carveout() {
-  cudaError_t e;
-  const int c = cudaSharedmemCarveoutMaxShared;
-  if ((e = cudaFuncSetAttribute(attn_kernel<32>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                c)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                c)) != cudaSuccess)
-    return e;
-  return cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributePreferredSharedMemoryCarveout, c);
+  const void* ks[] = {(const void*)attn_mma_kernel<32>, (const void*)attn_mma_kernel<64>,
+                      (const void*)attn_tc_kernel};
+  for (const void* k : ks) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
-cudaError_t launch_attention(const AttnArgs& a, int dh, cudaStream_t s) {
-  const int rows = a.Bq * (a.H / a.Hk);
-  dim3 grid((rows + kRowsPerCta - 1) / kRowsPerCta, a.Hk, a.nbq);
-  switch (dh) {
-    case 32: return launch_pdl(attn_kernel<32>, grid, dim3(kThreads), attn_smem<32>(), s, a);
-    case 64: return launch_pdl(attn_kernel<64>, grid, dim3(kThreads), attn_smem<64>(), s, a);
-    case 128: return launch_pdl(attn_kernel<128>, grid, dim3(kThreads), attn_smem<128>(), s, a);
-    default: return cudaErrorInvalidValue;
+const char* plan_attention(AttnLaunch* L, const AttnArgs& a, int dh, int kc_rows, int vtc_cols) {
+  static thread_local char err[256];
+  memset(L, 0, sizeof(*L));
+  L->args = a;
+  L->dh = dh;
+  const int G = a.H / a.Hk;
+  const int T = a.nbq * a.Bq;
+  if (a.H % a.Hk || T < 1) return "attention: bad head grouping or empty batch";
+  if (a.Bk > a.Bk_stride || (a.Bk > 0 && a.Bk_stride % 8)) return "attention: block stride must be a multiple of 8";
+  if (a.ldvc % 8 || a.ldvb % 8 || (a.Bk > 0 && a.ldvb < a.nbq * a.Bk_stride))
+    return "attention: V^T row lengths must be multiples of 8 covering every branch";
+  if (dh == 32 || dh == 64) {
+    L->grid = dim3((a.Bq * G + kRowsPerCta - 1) / kRowsPerCta, a.Hk, a.nbq);
+    return "";
+  }
+  if (dh != 128) return "attention: head_dim must be 32, 64 or 128";
+  static_assert(sizeof(TcMaps) == 5 * sizeof(CUtensorMap), "tensor map pack");
+  CUtensorMap* maps = &L->maps[0];
+  const int kbr = a.nbq * a.Bk_stride;
+  // With no prefix or no block keys the corresponding maps are never used: point them
+  // at the query array so that every map is valid.
+  if (!make_tmap_bf16(&maps[0], a.q, (uint64_t)a.Hk * T * G, 128, 128, err, sizeof(err)) ||
+      !make_tmap_bf16(&maps[1], kc_rows > 0 ? (const void*)a.kc : (const void*)a.q,
+                      kc_rows > 0 ? kc_rows : T, kc_rows > 0 ? (uint64_t)a.Hk * 128 : 128, 64,
+                      err, sizeof(err)) ||
+      !make_tmap_bf16(&maps[2], vtc_cols > 0 ? (const void*)a.vtc : (const void*)a.q,
+                      vtc_cols > 0 ? (uint64_t)a.Hk * 128 : T, vtc_cols > 0 ? vtc_cols : 128, 128,
+                      err, sizeof(err), vtc_cols > 0 ? (uint64_t)a.ldvc : 0) ||
+      !make_tmap_bf16(&maps[3], a.Bk > 0 ? (const void*)a.kb : (const void*)a.q,
+                      a.Bk > 0 ? kbr : T, a.Bk > 0 ? (uint64_t)a.Hk * 128 : 128, 64, err,
+                      sizeof(err)) ||
+      !make_tmap_bf16(&maps[4], a.Bk > 0 ? (const void*)a.vtb : (const void*)a.q,
+                      a.Bk > 0 ? (uint64_t)a.Hk * 128 : T, a.Bk > 0 ? kbr : 128, 128, err,
+                      sizeof(err), a.Bk > 0 ? (uint64_t)a.ldvb : 0))
+    return err;
+  L->grid = dim3((T * G + kTcRows - 1) / kTcRows, a.Hk, 1);
+  return "";
+}
+
+cudaError_t launch_attention(const AttnLaunch& L, cudaStream_t s) {
+  switch (L.dh) {
+    case 32:
+      return launch_pdl(attn_mma_kernel<32>, L.grid, dim3(kThreads), attn_mma_smem<32>(), s, L.args);
+    case 64:
+      return launch_pdl(attn_mma_kernel<64>, L.grid, dim3(kThreads), attn_mma_smem<64>(), s, L.args);
+    case 128: {
+      TcMaps m;
+      memcpy(&m, L.maps, sizeof(m));
+      return launch_pdl(attn_tc_kernel, L.grid, dim3(kTcThreads), kTcSmem, s, m, L.args);
+    }
+    default:
+      return cudaErrorInvalidValue;
   }
 }
 

@@ -141,21 +141,32 @@ __global__ void select_kernel(DevState* st, int B, int nb, int mask_id,
 }
 
 // grid: (L, 2 [K, V], chunks); copies B rows of row_elems bf16 of the winner's branch.
+// Commit-Winner: copies the winner branch's block K ([B][row_elems] rows) and V^T
+// (columns [w*B, w*B+B) of each of the row_elems rows) from the Pre-Write scratch into the
+// static cache at the block position P.  blockIdx.y: 0 = K, 1 = V^T.
 __global__ void commit_kv_kernel(const DevState* st, const bf16* __restrict__ ks,
-                                 const bf16* __restrict__ vs, bf16* __restrict__ kc,
-                                 bf16* __restrict__ vc, int B, int row_elems,
-                                 size_t layer_stride_cache, size_t layer_stride_scr) {
+                                 const bf16* __restrict__ vts, bf16* __restrict__ kc,
+                                 bf16* __restrict__ vtc, int B, int row_elems, KvStrides kv) {
   pdl_wait();
   pdl_trigger();
   const int l = blockIdx.x;
   const int w = st->winner;
   const int P = st->P;
-  const bf16* src = (blockIdx.y == 0 ? ks : vs) + (size_t)l * layer_stride_scr +
-                    (size_t)w * B * row_elems;
-  bf16* dst = (blockIdx.y == 0 ? kc : vc) + (size_t)l * layer_stride_cache + (size_t)P * row_elems;
-  const int n16 = B * row_elems / 8;
-  for (int e = blockIdx.z * blockDim.x + threadIdx.x; e < n16; e += gridDim.z * blockDim.x)
-    reinterpret_cast<uint4*>(dst)[e] = reinterpret_cast<const uint4*>(src)[e];
+  if (blockIdx.y == 0) {
+    const bf16* src = ks + (size_t)l * kv.k_scr + (size_t)w * B * row_elems;
+    bf16* dst = kc + (size_t)l * kv.k_cache + (size_t)P * row_elems;
+    const int n16 = B * row_elems / 8;
+    for (int e = blockIdx.z * blockDim.x + threadIdx.x; e < n16; e += gridDim.z * blockDim.x)
+      reinterpret_cast<uint4*>(dst)[e] = reinterpret_cast<const uint4*>(src)[e];
+  } else {
+    const bf16* src = vts + (size_t)l * kv.v_scr + (size_t)w * B;
+    bf16* dst = vtc + (size_t)l * kv.v_cache + P;
+    const int n = B * row_elems;
+    for (int e = blockIdx.z * blockDim.x + threadIdx.x; e < n; e += gridDim.z * blockDim.x) {
+      const int r = e / B, c = e - r * B;
+      dst[(size_t)r * kv.ld_cache + c] = src[(size_t)r * kv.ld_scr + c];
+    }
+  }
 }
 
 __global__ void finalize_kernel(DevState* st, int B, int mask_id, int* __restrict__ out_tokens) {
@@ -217,16 +228,13 @@ cudaError_t launch_select(void* st, int B, int nb, int mask_id, const int* branc
                     B, nb, mask_id, branch_tok, valid, am_b, mp_b);
 }
 
-cudaError_t launch_commit_kv(const void* st, const bf16* ks, const bf16* vs, bf16* kc,
-                             bf16* vc, int L, int nb, int B, int row_elems,
-                             size_t layer_stride_cache, size_t layer_stride_scr,
+cudaError_t launch_commit_kv(const void* st, const bf16* ks, const bf16* vts, bf16* kc,
+                             bf16* vtc, int L, int B, int row_elems, const KvStrides& kv,
                              cudaStream_t s) {
-  (void)nb;
-  const int n16 = B * row_elems / 8;
-  const int chunks = (n16 + 255) / 256 < 8 ? (n16 + 255) / 256 : 8;
+  const int n = B * row_elems;
+  const int chunks = (n + 255) / 256 < 16 ? (n + 255) / 256 : 16;
   return launch_pdl(commit_kv_kernel, dim3(L, 2, chunks), dim3(256), 0, s,
-                    static_cast<const DevState*>(st), ks, vs, kc, vc, B, row_elems,
-                    layer_stride_cache, layer_stride_scr);
+                    static_cast<const DevState*>(st), ks, vts, kc, vtc, B, row_elems, kv);
 }
 
 cudaError_t launch_finalize(void* st, int B, int mask_id, int* out_tokens, cudaStream_t s) {

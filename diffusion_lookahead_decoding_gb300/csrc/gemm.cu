@@ -233,14 +233,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
+    // Every epilogue thread waits for the accumulator (bounded); the warp-wide TMEM reads
+    // then follow one decision for all eight warps, taken after a barrier from the shared
+    // abort flag (set by any wait of the CTA that gave up).
+    auto accum_ready = [&]() {
+      mbar_wait_bounded(smem_u32(&tail->accf), 0, abort, a.err, DEV_TIMEOUT_EPILOGUE);
+      epilogue_sync();
+      return *abort == 0;
+    };
     if (kCluster) {
       // Split-K sum inside the cluster.  Per 128-row accumulator ("round"): every CTA
       // stages its partial tile in its (now idle) smem rings and signals all peers' cfull;
       // CTA `rank` then sums tokens [tlo, tlo + ntok) of the tile over the splits in split
       // order, reading the peers' stages through distributed shared memory, and signals
       // cdone so that peers may overwrite (or release) their stage.
-      const bool ok = nk > 0 && mbar_wait_bounded(smem_u32(&tail->accf), 0, abort, a.err,
-                                                  DEV_TIMEOUT_EPILOGUE);
+      const bool ok = nk > 0 && accum_ready();
       tc_fence_after();
       float* stage = reinterpret_cast<float*>(smem);
       const int S = a.splits;
@@ -265,26 +272,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < S; ++c) mbar_arrive_cluster(mapa_shared(cfull, (uint32_t)c));
         if (mbar_wait_cluster_bounded(cfull, (uint32_t)round & 1u, abort, a.err,
                                       DEV_TIMEOUT_CLUSTER)) {
-          // Work item e: token tlo + e/16, columns j..j+3 of a head and their rotation
-          // partners j+dh/2..+3.  Two items per pass keep 4*S loads in flight per thread.
           const int dh = a.dh, hdh = dh >> 1, per_head = dh >> 3;
-          const int nitem = ntok * 16;
+          const int G = a.H / a.Hk;
+          const int head0 = a_row[i] / dh;  // first head of this 128-row tile
+          const int vfirst = a.H + a.Hk;    // first value head
           constexpr int kStep = kEpiWarps * 32;
+          // (1) q and k.  Work item e: token tlo + e/16, columns j..j+3 of a head and their
+          // rotation partners j+dh/2..+3.  Two items per pass keep 4*S loads in flight.
+          const int nitem = head0 < vfirst ? ntok * 16 : 0;
           for (int e0 = te; e0 < nitem; e0 += 2 * kStep) {
             float4 v[2][2][kMaxClusterSplits];
-            uint32_t off[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int e = e0 + h * kStep;
               const int tt = tlo + (e >> 4), u = e & 15;
               const int hd = u / per_head, j = (u - hd * per_head) * 4;
-              off[h] = (uint32_t)(tt * 128 + hd * dh + j) * 4u;
-              if (e < nitem) {
+              const uint32_t off = (uint32_t)(tt * 128 + hd * dh + j) * 4u;
+              if (e < nitem && head0 + hd < vfirst) {
 #pragma unroll
                 for (int c = 0; c < kMaxClusterSplits; ++c)
                   if (c < S) {
-                    v[h][0][c] = ld_dsmem_f4(peer[c] + off[h]);
-                    v[h][1][c] = ld_dsmem_f4(peer[c] + off[h] + (uint32_t)hdh * 4u);
+                    v[h][0][c] = ld_dsmem_f4(peer[c] + off);
+                    v[h][1][c] = ld_dsmem_f4(peer[c] + off + (uint32_t)hdh * 4u);
                   }
               }
             }
@@ -293,8 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int e = e0 + h * kStep;
               const int tt = tlo + (e >> 4), u = e & 15;
               const int t = b_row + tt;
-              if (e >= nitem || t >= a.T) continue;
               const int hd = u / per_head, j = (u - hd * per_head) * 4;
+              const int head = head0 + hd;
+              if (e >= nitem || t >= a.T || head >= vfirst) continue;
               float4 x1 = v[h][0][0], x2 = v[h][1][0];
 #pragma unroll
               for (int c = 1; c < kMaxClusterSplits; ++c)
@@ -302,26 +312,75 @@ __global__ void __launch_bounds__(kThreads, 1)
                   x1.x += v[h][0][c].x; x1.y += v[h][0][c].y; x1.z += v[h][0][c].z; x1.w += v[h][0][c].w;
                   x2.x += v[h][1][c].x; x2.y += v[h][1][c].y; x2.z += v[h][1][c].z; x2.w += v[h][1][c].w;
                 }
-              const int head = a_row[i] / dh + hd;
+              // RoPE, rotate-half form, at absolute position P + bi.
               const int bi = t % a.Bq;
+              const float4 cs = *reinterpret_cast<const float4*>(a.cos_t + (size_t)(P + bi) * hdh + j);
+              const float4 sn = *reinterpret_cast<const float4*>(a.sin_t + (size_t)(P + bi) * hdh + j);
+              const float4 y1 = make_float4(x1.x * cs.x - x2.x * sn.x, x1.y * cs.y - x2.y * sn.y,
+                                            x1.z * cs.z - x2.z * sn.z, x1.w * cs.w - x2.w * sn.w);
+              const float4 y2 = make_float4(x2.x * cs.x + x1.x * sn.x, x2.y * cs.y + x1.y * sn.y,
+                                            x2.z * cs.z + x1.z * sn.z, x2.w * cs.w + x1.w * sn.w);
+              // q: group-major [Hk][T][G][dh]; k: [row][Hk][dh], row = cache position or t.
               const size_t kv_row = a.kv_to_cache ? (size_t)(P + bi) : (size_t)t;
-              bf16* dst;
-              if (head < a.H + a.Hk) {
-                // RoPE, rotate-half form, at absolute position P + bi.
-                const float4 cs = *reinterpret_cast<const float4*>(a.cos_t + (size_t)(P + bi) * hdh + j);
-                const float4 sn = *reinterpret_cast<const float4*>(a.sin_t + (size_t)(P + bi) * hdh + j);
-                const float4 y1 = make_float4(x1.x * cs.x - x2.x * sn.x, x1.y * cs.y - x2.y * sn.y,
-                                              x1.z * cs.z - x2.z * sn.z, x1.w * cs.w - x2.w * sn.w);
-                x2 = make_float4(x2.x * cs.x + x1.x * sn.x, x2.y * cs.y + x1.y * sn.y,
-                                 x2.z * cs.z + x1.z * sn.z, x2.w * cs.w + x1.w * sn.w);
-                x1 = y1;
-                dst = head < a.H ? a.q + ((size_t)t * a.H + head) * dh
-                                 : a.kdst + (kv_row * a.Hk + (head - a.H)) * dh;
-              } else {
-                dst = a.vdst + (kv_row * a.Hk + (head - a.H - a.Hk)) * dh;
+              bf16* dst = head < a.H
+                              ? a.q + (((size_t)(head / G) * a.T + t) * G + head % G) * dh
+                              : a.kdst + (kv_row * a.Hk + (head - a.H)) * dh;
+              store4_bf16(dst + j, y1.x, y1.y, y1.z, y1.w);
+              store4_bf16(dst + j + hdh, y2.x, y2.y, y2.z, y2.w);
+            }
+          }
+          // (2) v, stored transposed: V^T[(head - vfirst) * dh + d][column], column = cache
+          // position or t.  Work item: 4 columns of the tile x 8 consecutive tokens, so the
+          // stores are 16-byte runs along the position axis.
+          const int vcol0 = max(vfirst * dh - a_row[i], 0);
+          if (vcol0 < 128) {
+            const int nf4 = (128 - vcol0) / 4, ntg = (ntok + 7) / 8;
+            for (int e = te; e < nf4 * ntg; e += kStep) {
+              const int f = vcol0 + (e % nf4) * 4, tt0 = tlo + (e / nf4) * 8;
+              float4 acc[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (tt0 + k >= tlo + ntok) continue;
+                const uint32_t off = (uint32_t)((tt0 + k) * 128 + f) * 4u;
+                float4 w[kMaxClusterSplits];
+#pragma unroll
+                for (int c = 0; c < kMaxClusterSplits; ++c)
+                  if (c < S) w[c] = ld_dsmem_f4(peer[c] + off);
+                acc[k] = w[0];
+#pragma unroll
+                for (int c = 1; c < kMaxClusterSplits; ++c)
+                  if (c < S) {
+                    acc[k].x += w[c].x; acc[k].y += w[c].y; acc[k].z += w[c].z; acc[k].w += w[c].w;
+                  }
               }
-              store4_bf16(dst + j, x1.x, x1.y, x1.z, x1.w);
-              store4_bf16(dst + j + hdh, x2.x, x2.y, x2.z, x2.w);
+              const int vrow = a_row[i] + f - vfirst * dh;  // (value head) * dh + d
+              const int t0 = b_row + tt0;
+              const int col0 = a.kv_to_cache ? P + t0 % a.Bq : t0;
+              const bool whole = tt0 + 8 <= tlo + ntok && t0 + 8 <= a.T && (col0 & 7) == 0 &&
+                                 (!a.kv_to_cache || t0 % a.Bq + 8 <= a.Bq);
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                bf16* vr = a.vdst + (size_t)(vrow + q4) * a.ldv;
+                float x[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                  x[k] = q4 == 0 ? acc[k].x : q4 == 1 ? acc[k].y : q4 == 2 ? acc[k].z : acc[k].w;
+                if (whole) {
+                  uint4 o;
+                  __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) h2[k] = __floats2bfloat162_rn(x[2 * k], x[2 * k + 1]);
+                  *reinterpret_cast<uint4*>(vr + col0) = o;
+                } else {
+#pragma unroll
+                  for (int k = 0; k < 8; ++k) {
+                    const int t = t0 + k;
+                    if (tt0 + k >= tlo + ntok || t >= a.T) continue;
+                    vr[a.kv_to_cache ? P + t % a.Bq : t] = __float2bfloat16_rn(x[k]);
+                  }
+                }
+              }
             }
           }
         }
@@ -334,8 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (round > 0)
         mbar_wait_cluster_bounded(cdone, (uint32_t)(round - 1) & 1u, abort, a.err,
                                   DEV_TIMEOUT_CLUSTER);
-    } else if (nk > 0 &&
-               mbar_wait_bounded(smem_u32(&tail->accf), 0, abort, a.err, DEV_TIMEOUT_EPILOGUE)) {
+    } else if (nk > 0 && accum_ready()) {
       tc_fence_after();
       float* stage = reinterpret_cast<float*>(smem);
       if (MODE == GEMM_RED_ADD) {
@@ -492,18 +550,19 @@ uint32_t stage_bytes(int mode, int nbox) {
 }  // namespace
 
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                    uint32_t box_rows, char* errbuf, size_t errlen) {
+                    uint32_t box_rows, char* errbuf, size_t errlen, uint64_t ld) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) {
     snprintf(errbuf, errlen, "cuTensorMapEncodeTiled unavailable");
     return false;
   }
-  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (cols * 2) % 16 != 0) {
+  if (ld == 0) ld = cols;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (ld * 2) % 16 != 0 || ld < cols) {
     snprintf(errbuf, errlen, "tensor map base/stride not 16-byte aligned");
     return false;
   }
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
+  cuuint64_t strides[1] = {ld * 2};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,

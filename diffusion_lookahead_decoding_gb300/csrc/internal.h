@@ -80,9 +80,10 @@ struct GemmArgs {
   bf16* out_bf16;    int ldh;
   float* part_m; float* part_s; int* part_i; int part_ld;
   // QKV: A rows are [H q heads | Hk k heads | Hk v heads] x dh.  Token row t is position
-  // t % Bq of its branch, at absolute position *dP + t % Bq.  q -> [T][H][dh]; k/v ->
-  // kdst/vdst row t ([T][Hk][dh]) or, with kv_to_cache, cache row *dP + t % Bq.
-  bf16* q; bf16* kdst; bf16* vdst;
+  // t % Bq of its branch, at absolute position *dP + t % Bq.  q -> group-major
+  // [Hk][T][H/Hk][dh]; k -> kdst [row][Hk][dh]; v -> transposed vdst [Hk*dh][ldv] at
+  // column row; row = t, or with kv_to_cache the cache position *dP + t % Bq.
+  bf16* q; bf16* kdst; bf16* vdst; int ldv;
   const float* cos_t; const float* sin_t;  // [positions][dh/2]
   const int* dP;
   int H, Hk, dh, Bq, kv_to_cache;
@@ -97,10 +98,11 @@ struct GemmLaunch {
   size_t smem;
 };
 
-// Encodes a 2-D bf16 tensor map over a row-major [rows][cols] matrix with a box of
-// box_rows x 64 columns and 128-byte swizzle.  Returns false on failure.
+// Encodes a 2-D bf16 tensor map over a row-major [rows][cols] matrix (row pitch ld
+// elements, 0 = cols) with a box of box_rows x 64 columns and 128-byte swizzle; reads
+// outside [rows][cols] return zeros.  Returns false on failure.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                    uint32_t box_rows, char* errbuf, size_t errlen);
+                    uint32_t box_rows, char* errbuf, size_t errlen, uint64_t ld = 0);
 
 // Fills `L` for one GEMM.  Returns an empty string on success, else a reason.  With
 // w_packed the weight is in the tile-major layout written by launch_pack_tiles (tiles of
@@ -128,18 +130,31 @@ int gemm_cluster_capacity(int mode, int cs, size_t smem);
 int gemm_max_smem();
 
 // ------------------------------------------------------------------ attention
+// Layouts: q [Hk][nbq*Bq][G][dh] (group-major rows), out [nbq*Bq][H*dh], keys row-major
+// [pos][Hk][dh], values transposed [Hk*dh][positions].
 struct AttnArgs {
-  const bf16* q;       // [nbq*Bq][H][dh]
-  bf16* out;           // [nbq*Bq][H*dh]
+  const bf16* q;
+  bf16* out;
   const bf16* kc;      // prefix keys   [*][Hk][dh]
-  const bf16* vc;
+  const bf16* vtc;     // prefix values [Hk*dh][ldvc]
   const bf16* kb;      // block keys    [nbq][Bk_stride][Hk][dh]
-  const bf16* vb;
+  const bf16* vtb;     // block values  [Hk*dh][nbq*Bk_stride]
   const int* dP;       // device prefix length (may be null -> 0)
   int pk_add;          // prefix keys = *dP + pk_add
+  int ldvc, ldvb;      // row lengths of vtc and vtb (multiples of 8)
   int Bq, Bk, Bk_stride, nbq, H, Hk;
+  int* err;            // device error word (bounded waits), may be null
 };
-cudaError_t launch_attention(const AttnArgs& a, int dh, cudaStream_t s);
+struct AttnLaunch {
+  CUtensorMap maps[5];  // head_dim 128: q, prefix K, prefix V^T, block K, block V^T
+  AttnArgs args;
+  int dh;
+  dim3 grid;
+};
+// Fills `L` (tensor maps over kc with kc_rows positions and vtc with vtc_cols positions;
+// reads beyond are zeros).  Returns an empty string on success, else a reason.
+const char* plan_attention(AttnLaunch* L, const AttnArgs& a, int dh, int kc_rows, int vtc_cols);
+cudaError_t launch_attention(const AttnLaunch& L, cudaStream_t s);
 cudaError_t attention_set_smem_limits();
 
 // ------------------------------------------------------------------ pointwise
@@ -176,9 +191,14 @@ cudaError_t launch_decide(void* st, int B, int k, float tau, int mask_id, int* b
 cudaError_t launch_select(void* st, int B, int nb, int mask_id, const int* branch_tok,
                           const int* valid, const int* am_b, const float* mp_b,
                           cudaStream_t s);
-cudaError_t launch_commit_kv(const void* st, const bf16* ks, const bf16* vs, bf16* kc,
-                             bf16* vc, int L, int nb, int B, int row_elems,
-                             size_t layer_stride_cache, size_t layer_stride_scr,
+// Per-layer strides (elements) of the K cache / scratch ([pos][Hk*dh] rows) and of the
+// transposed V cache / scratch ([Hk*dh][ld] rows), and the V^T row lengths.
+struct KvStrides {
+  size_t k_cache, k_scr, v_cache, v_scr;
+  int ld_cache, ld_scr;
+};
+cudaError_t launch_commit_kv(const void* st, const bf16* ks, const bf16* vts, bf16* kc,
+                             bf16* vtc, int L, int B, int row_elems, const KvStrides& kv,
                              cudaStream_t s);
 cudaError_t launch_finalize(void* st, int B, int mask_id, int* out_tokens, cudaStream_t s);
 cudaError_t launch_state_reset(void* st, int P, int B, int mask_id, cudaStream_t s);

@@ -57,6 +57,7 @@ struct Plan {
   int* am_out = nullptr;
   float* mp_out = nullptr;
   std::vector<GemmLaunch> qkv, o, gu, dn;
+  std::vector<AttnLaunch> attn;
   GemmLaunch lmh;
 };
 
@@ -89,7 +90,10 @@ struct lopa_ctx {
   int* out_tokens = nullptr;
   DevState* st = nullptr;
   int Tmax = 0, nbmax = 0, qkv_rows = 0;
-  size_t cache_layer = 0, scr_layer = 0;
+  // K cache [L][max_seq][Hk*dh], K scratch [L][nbmax*B][Hk*dh]; values transposed:
+  // V^T cache [L][Hk*dh][vt_ld], V^T scratch [L][Hk*dh][nbmax*B].
+  size_t cache_layer = 0, scr_layer = 0, vt_cache_layer = 0;
+  int vt_ld = 0;
   // graphs
   Plan step_plan, start_plan;
   cudaGraphExec_t step_exec = nullptr, start_exec = nullptr;
@@ -210,6 +214,7 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
   p.am_out = am_out;
   p.mp_out = mp_out;
   p.qkv.resize(L);
+  p.attn.resize(L);
   p.o.resize(L);
   p.gu.resize(L);
   p.dn.resize(L);
@@ -241,8 +246,13 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
     if ((r = plan(p.qkv[l], GEMM_QKV, ctx->n, d, ctx->wqkv[l], ctx->qkv_rows, "qkv"))) return r;
     GemmArgs& qa = p.qkv[l].args;
     qa.q = ctx->q;
-    qa.kdst = kv_to_cache ? ctx->kc + (size_t)l * ctx->cache_layer : ctx->ks + (size_t)l * ctx->scr_layer;
-    qa.vdst = kv_to_cache ? ctx->vc + (size_t)l * ctx->cache_layer : ctx->vs + (size_t)l * ctx->scr_layer;
+    bf16* kcl = ctx->kc + (size_t)l * ctx->cache_layer;
+    bf16* vcl = ctx->vc + (size_t)l * ctx->vt_cache_layer;
+    bf16* ksl = ctx->ks + (size_t)l * ctx->scr_layer;
+    bf16* vsl = ctx->vs + (size_t)l * ctx->scr_layer;
+    qa.kdst = kv_to_cache ? kcl : ksl;
+    qa.vdst = kv_to_cache ? vcl : vsl;
+    qa.ldv = kv_to_cache ? ctx->vt_ld : ctx->nbmax * ctx->dc.block;
     qa.cos_t = ctx->cos_t;
     qa.sin_t = ctx->sin_t;
     qa.dP = &ctx->st->P;
@@ -251,6 +261,26 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
     qa.dh = dh;
     qa.Bq = Bq;
     qa.kv_to_cache = kv_to_cache;
+    AttnArgs aa;
+    aa.q = ctx->q;
+    aa.out = ctx->attn;
+    aa.kc = kcl;
+    aa.vtc = vcl;
+    aa.kb = ksl;
+    aa.vtb = vsl;
+    aa.dP = &ctx->st->P;
+    aa.pk_add = kv_to_cache ? p.T : 0;
+    aa.ldvc = ctx->vt_ld;
+    aa.ldvb = ctx->nbmax * ctx->dc.block;
+    aa.Bq = Bq;
+    aa.Bk = kv_to_cache ? 0 : Bq;
+    aa.Bk_stride = Bq;
+    aa.nbq = nb;
+    aa.H = H;
+    aa.Hk = m.n_kv_heads;
+    aa.err = &ctx->st->err;
+    const char* ea = plan_attention(&p.attn[l], aa, dh, m.max_seq, ctx->vt_ld);
+    if (ea[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s", ea);
     if ((r = plan(p.o[l], GEMM_RED_ADD, ctx->attn, H * dh, ctx->wo[l], d, "o"))) return r;
     if ((r = plan(p.gu[l], GEMM_SWIGLU, ctx->n, d, ctx->wgu[l], 2 * F, "gate/up"))) return r;
     p.gu[l].args.out_bf16 = ctx->hm;
@@ -282,25 +312,8 @@ int enqueue_forward(lopa_ctx* ctx, const Plan& p) {
   cudaStream_t s = ctx->stream;
   CK(launch_embed_norm(p.tok, p.T, ctx->embed, ctx->attn_norm[0], ctx->x, ctx->n, d, m.rms_eps, s));
   for (int l = 0; l < L; ++l) {
-    const bf16* kcl = ctx->kc + (size_t)l * ctx->cache_layer;
-    const bf16* vcl = ctx->vc + (size_t)l * ctx->cache_layer;
     CK(launch_gemm(p.qkv[l], s));  // q, k, v + RoPE; K/V Pre-Write
-    AttnArgs aa;
-    aa.q = ctx->q;
-    aa.out = ctx->attn;
-    aa.kc = kcl;
-    aa.vc = vcl;
-    aa.kb = ctx->ks + (size_t)l * ctx->scr_layer;
-    aa.vb = ctx->vs + (size_t)l * ctx->scr_layer;
-    aa.dP = &ctx->st->P;
-    aa.pk_add = p.kv_to_cache ? p.T : 0;
-    aa.Bq = p.Bq;
-    aa.Bk = p.kv_to_cache ? 0 : p.Bq;
-    aa.Bk_stride = p.Bq;
-    aa.nbq = p.nb;
-    aa.H = H;
-    aa.Hk = Hk;
-    CK(launch_attention(aa, dh, s));
+    CK(launch_attention(p.attn[l], s));
     CK(launch_gemm(p.o[l], s));  // split-K partials of attn . Wo^T
     CK(launch_residual_norm(ctx->x, ctx->part, p.o[l].args.splits, p.o[l].args.split_stride,
                             ctx->mlp_norm[l], ctx->n, p.T, d, m.rms_eps, s));
@@ -325,8 +338,15 @@ int enqueue_step(lopa_ctx* ctx) {
   int r = enqueue_forward(ctx, ctx->step_plan);
   if (r) return r;
   CK(launch_select(ctx->st, B, nb, mask, ctx->branch_tok, ctx->valid, ctx->am_b, ctx->mp_b, s));
-  CK(launch_commit_kv(ctx->st, ctx->ks, ctx->vs, ctx->kc, ctx->vc, ctx->mc.n_layers, nb, B,
-                      ctx->mc.n_kv_heads * ctx->mc.head_dim, ctx->cache_layer, ctx->scr_layer, s));
+  KvStrides kv;
+  kv.k_cache = ctx->cache_layer;
+  kv.k_scr = ctx->scr_layer;
+  kv.v_cache = ctx->vt_cache_layer;
+  kv.v_scr = ctx->scr_layer;
+  kv.ld_cache = ctx->vt_ld;
+  kv.ld_scr = nb * B;
+  CK(launch_commit_kv(ctx->st, ctx->ks, ctx->vs, ctx->kc, ctx->vc, ctx->mc.n_layers, B,
+                      ctx->mc.n_kv_heads * ctx->mc.head_dim, kv, s));
   CK(launch_finalize(ctx->st, B, mask, ctx->out_tokens, s));
   return 0;
 }
@@ -426,6 +446,8 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
   ctx->Tmax = std::max(ctx->nbmax * B, ctx->dc.max_prompt);
   ctx->qkv_rows = (H + 2 * Hk) * dh;
   ctx->cache_layer = (size_t)m.max_seq * Hk * dh;
+  ctx->vt_ld = (m.max_seq + 63) / 64 * 64;
+  ctx->vt_cache_layer = (size_t)Hk * dh * ctx->vt_ld;
   ctx->scr_layer = (size_t)ctx->nbmax * B * Hk * dh;
   ctx->nvt = (V + 255) / 256;
   ctx->part_ld = ctx->nbmax * B;
@@ -433,7 +455,7 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
                               std::max(partial_floats(ctx, B), partial_floats(ctx, ctx->dc.max_prompt)));
   const size_t T = ctx->Tmax;
   int r;
-  if ((r = dalloc(ctx, &ctx->kc, ctx->cache_layer * L)) || (r = dalloc(ctx, &ctx->vc, ctx->cache_layer * L)) ||
+  if ((r = dalloc(ctx, &ctx->kc, ctx->cache_layer * L)) || (r = dalloc(ctx, &ctx->vc, ctx->vt_cache_layer * L)) ||
       (r = dalloc(ctx, &ctx->ks, ctx->scr_layer * L)) || (r = dalloc(ctx, &ctx->vs, ctx->scr_layer * L)) ||
       (r = dalloc(ctx, &ctx->x, T * d)) || (r = dalloc(ctx, &ctx->n, T * d)) ||
       (r = dalloc(ctx, &ctx->part, ctx->part_floats)) || (r = dalloc(ctx, &ctx->q, T * H * dh)) ||
@@ -452,7 +474,9 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
     return r;
   cudaStream_t s = ctx->stream;
   CK(cudaMemsetAsync(ctx->kc, 0, ctx->cache_layer * L * sizeof(bf16), s));
-  CK(cudaMemsetAsync(ctx->vc, 0, ctx->cache_layer * L * sizeof(bf16), s));
+  CK(cudaMemsetAsync(ctx->vc, 0, ctx->vt_cache_layer * L * sizeof(bf16), s));
+  CK(cudaMemsetAsync(ctx->ks, 0, ctx->scr_layer * L * sizeof(bf16), s));
+  CK(cudaMemsetAsync(ctx->vs, 0, ctx->scr_layer * L * sizeof(bf16), s));
   CK(cudaMemsetAsync(ctx->st, 0, sizeof(DevState), s));
   CK(cudaMemsetAsync(ctx->out_tokens, 0, (size_t)m.max_seq * sizeof(int), s));
   CK(launch_rope_table(ctx->cos_t, ctx->sin_t, m.max_seq, dh, (double)m.rope_base, s));
@@ -743,11 +767,18 @@ int lopa_read_kv(lopa_ctx* ctx, int layer, int pos0, int n, uint16_t* k, uint16_
   if (layer < 0 || layer >= ctx->mc.n_layers || pos0 < 0 || n < 0 || pos0 + n > ctx->mc.max_seq)
     return fail(ctx, LOPA_ERR_INVALID_ARG, "layer/position range out of bounds");
   const size_t row = (size_t)ctx->mc.n_kv_heads * ctx->mc.head_dim;
-  const size_t off = (size_t)layer * ctx->cache_layer + (size_t)pos0 * row;
   cudaStream_t s = ctx->stream;
-  if (k) CK(cudaMemcpyAsync(k, ctx->kc + off, n * row * 2, cudaMemcpyDeviceToHost, s));
-  if (v) CK(cudaMemcpyAsync(v, ctx->vc + off, n * row * 2, cudaMemcpyDeviceToHost, s));
+  if (k && n > 0)
+    CK(cudaMemcpyAsync(k, ctx->kc + (size_t)layer * ctx->cache_layer + (size_t)pos0 * row,
+                       n * row * 2, cudaMemcpyDeviceToHost, s));
+  std::vector<uint16_t> vt(v && n > 0 ? row * n : 0);
+  if (!vt.empty())
+    CK(cudaMemcpy2DAsync(vt.data(), (size_t)n * 2,
+                         ctx->vc + (size_t)layer * ctx->vt_cache_layer + pos0,
+                         (size_t)ctx->vt_ld * 2, (size_t)n * 2, row, cudaMemcpyDeviceToHost, s));
   CK(cudaStreamSynchronize(s));
+  for (size_t r = 0; r < vt.size() / (n > 0 ? n : 1) && !vt.empty(); ++r)
+    for (int c = 0; c < n; ++c) v[(size_t)c * row + r] = vt[r * n + c];
   return 0;
 }
 
@@ -756,12 +787,19 @@ int lopa_read_branch_kv(lopa_ctx* ctx, int layer, int branch, uint16_t* k, uint1
   if (layer < 0 || layer >= ctx->mc.n_layers || branch < 0 || branch >= ctx->nbmax)
     return fail(ctx, LOPA_ERR_INVALID_ARG, "layer/branch out of range");
   const size_t row = (size_t)ctx->mc.n_kv_heads * ctx->mc.head_dim;
-  const size_t n = (size_t)ctx->dc.block * row;
-  const size_t off = (size_t)layer * ctx->scr_layer + (size_t)branch * n;
+  const int B = ctx->dc.block;
+  const size_t off = (size_t)layer * ctx->scr_layer;
   cudaStream_t s = ctx->stream;
-  if (k) CK(cudaMemcpyAsync(k, ctx->ks + off, n * 2, cudaMemcpyDeviceToHost, s));
-  if (v) CK(cudaMemcpyAsync(v, ctx->vs + off, n * 2, cudaMemcpyDeviceToHost, s));
+  if (k) CK(cudaMemcpyAsync(k, ctx->ks + off + (size_t)branch * B * row, B * row * 2,
+                            cudaMemcpyDeviceToHost, s));
+  std::vector<uint16_t> vt(v ? row * B : 0);
+  if (v)
+    CK(cudaMemcpy2DAsync(vt.data(), (size_t)B * 2, ctx->vs + off + (size_t)branch * B,
+                         (size_t)ctx->nbmax * B * 2, (size_t)B * 2, row, cudaMemcpyDeviceToHost, s));
   CK(cudaStreamSynchronize(s));
+  if (v)
+    for (size_t r = 0; r < row; ++r)
+      for (int c = 0; c < B; ++c) v[(size_t)c * row + r] = vt[r * B + c];
   return 0;
 }
 
@@ -828,16 +866,18 @@ int lopa_lmhead_argmax(const void* hidden, const void* lm_head, int rows, int d_
   return 0;
 }
 
-int lopa_branch_attention(const void* q, const void* k_prefix, const void* v_prefix, int prefix_len,
-                          const void* k_block, const void* v_block, int n_branches, int block,
-                          int n_heads, int n_kv_heads, int head_dim, void* out, void* stream) {
+int lopa_branch_attention(const void* q, const void* k_prefix, const void* vt_prefix,
+                          int prefix_len, int ld_vt_prefix, const void* k_block,
+                          const void* vt_block, int n_branches, int block, int n_heads,
+                          int n_kv_heads, int head_dim, void* out, void* stream) {
   lopa_ctx* ctx = nullptr;
-  if (!aligned16(q) || !aligned16(k_block) || !aligned16(v_block) || !aligned16(out))
+  if (!aligned16(q) || !aligned16(k_block) || !aligned16(vt_block) || !aligned16(out))
     return fail(ctx, LOPA_ERR_INVALID_ARG, "null or unaligned pointer");
-  if (prefix_len < 0 || (prefix_len > 0 && (!aligned16(k_prefix) || !aligned16(v_prefix))))
-    return fail(ctx, LOPA_ERR_INVALID_ARG, "bad prefix");
-  if (n_branches < 1 || block < 1 || block > 4096 || n_heads < 1 || n_kv_heads < 1 ||
-      n_heads % n_kv_heads)
+  if (prefix_len < 0 || (prefix_len > 0 && (!aligned16(k_prefix) || !aligned16(vt_prefix) ||
+                                            ld_vt_prefix < prefix_len || ld_vt_prefix % 8)))
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "bad prefix (ld_vt_prefix must be >= prefix_len and a multiple of 8)");
+  if (n_branches < 1 || block < 16 || block > 4096 || block % 16 || n_heads < 1 ||
+      n_kv_heads < 1 || n_heads % n_kv_heads)
     return fail(ctx, LOPA_ERR_INVALID_ARG, "bad shape");
   if (head_dim != 32 && head_dim != 64 && head_dim != 128)
     return fail(ctx, LOPA_ERR_UNSUPPORTED, "head_dim must be 32, 64 or 128");
@@ -845,19 +885,25 @@ int lopa_branch_attention(const void* q, const void* k_prefix, const void* v_pre
   a.q = static_cast<const bf16*>(q);
   a.out = static_cast<bf16*>(out);
   a.kc = static_cast<const bf16*>(k_prefix);
-  a.vc = static_cast<const bf16*>(v_prefix);
+  a.vtc = static_cast<const bf16*>(vt_prefix);
   a.kb = static_cast<const bf16*>(k_block);
-  a.vb = static_cast<const bf16*>(v_block);
+  a.vtb = static_cast<const bf16*>(vt_block);
   a.dP = nullptr;
   a.pk_add = prefix_len;
+  a.ldvc = prefix_len > 0 ? ld_vt_prefix : 8;
+  a.ldvb = n_branches * block;
   a.Bq = block;
   a.Bk = block;
   a.Bk_stride = block;
   a.nbq = n_branches;
   a.H = n_heads;
   a.Hk = n_kv_heads;
+  a.err = nullptr;
+  AttnLaunch L;
+  const char* e = plan_attention(&L, a, head_dim, prefix_len, prefix_len);
+  if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s", e);
   CK(attention_set_smem_limits());
-  CK(launch_attention(a, head_dim, static_cast<cudaStream_t>(stream)));
+  CK(launch_attention(L, static_cast<cudaStream_t>(stream)));
   return 0;
 }
 

@@ -215,14 +215,24 @@ int lopa_lmhead_argmax_static(const void* hidden, const void* lm_head, int rows,
 /* Branch-isolated attention (same passage, "attention isolated between branches"):
  * for branch b, query row (i, h) attends to the shared prefix keys [0, prefix_len)
  * and to its own block keys [0, block) only, bidirectionally, with softmax scale
- * 1/sqrt(head_dim) and grouped-query heads (head h uses KV head h / (n_heads/n_kv_heads)).
- * q [nb*block][n_heads][head_dim], k_prefix/v_prefix [prefix_len][n_kv_heads][head_dim],
- * k_block/v_block [nb][block][n_kv_heads][head_dim], out [nb*block][n_heads*head_dim];
- * all bf16, 16-byte aligned.  head_dim in {32, 64, 128}; block <= 4096. */
-int lopa_branch_attention(const void* q, const void* k_prefix, const void* v_prefix,
-                          int prefix_len, const void* k_block, const void* v_block,
-                          int n_branches, int block, int n_heads, int n_kv_heads,
-                          int head_dim, void* out, void* stream);
+ * 1/sqrt(head_dim) and grouped-query heads (head h uses KV head g = h / G, G =
+ * n_heads / n_kv_heads).  Layouts are the ones the verification forward keeps on the
+ * GPU (all bf16, 16-byte aligned):
+ *   q          [n_kv_heads][n_branches*block][G][head_dim]  (query (t, h) at
+ *              [h / G][t][h % G], t = b*block + i)
+ *   k_prefix   [prefix_len][n_kv_heads][head_dim]
+ *   vt_prefix  [n_kv_heads*head_dim][ld_vt_prefix]  values transposed: V[p][g][d] at
+ *              row g*head_dim + d, column p; ld_vt_prefix >= prefix_len, multiple of 8
+ *   k_block    [n_branches][block][n_kv_heads][head_dim]
+ *   vt_block   [n_kv_heads*head_dim][n_branches*block]  (V of branch b position i at
+ *              column b*block + i)
+ *   out        [n_branches*block][n_heads*head_dim]
+ * head_dim in {32, 64, 128}; block a multiple of 16, <= 4096.  prefix_len may be 0
+ * (k_prefix / vt_prefix then unused).  head_dim 128 runs on the tcgen05 tensor cores. */
+int lopa_branch_attention(const void* q, const void* k_prefix, const void* vt_prefix,
+                          int prefix_len, int ld_vt_prefix, const void* k_block,
+                          const void* vt_block, int n_branches, int block, int n_heads,
+                          int n_kv_heads, int head_dim, void* out, void* stream);
 
 /* Diagnostics: launches the verification-step GEMM of one kind (0 = q/k/v, 1 = output
  * projection, 2 = gate/up + SwiGLU, 3 = down, 4 = LM head) `iters` times on the

@@ -36,8 +36,12 @@ def test_dream7b_verification_sampled_parity():
                                            (am[0], mp[0], hid[0]), (am[k], mp[k], hid[k])]):
         e_h = rel_l2(g_h, out.x_final[j])
         e_mp = float(np.abs(g_mp - out.mp[j]).max())
+        # When every probability is within e_mp of the oracle's, the greedy token can only
+        # differ where the oracle's top-2 margin is below 2 * e_mp; a flip at a wider
+        # margin would be an argmax inconsistency.  (e_mp itself is bounded below.)
+        tie = max(cond.tie, 2.0 * e_mp)
         ok, nbad = tokens_ok(g_am[None], type("o", (), {"am": out.am[j:j + 1], "mp": out.mp[j:j + 1],
-                                                         "p2": out.p2[j:j + 1]}), cond.tie)
+                                                         "p2": out.p2[j:j + 1]}), tie)
         print(f"row-set {j}: hidden relL2 {e_h:.2e} (bound {cond.hidden_bound:.1e}) maxp max|d| "
               f"{e_mp:.2e} (bound {cond.mp_bound:.1e}) token flips beyond ties {nbad}")
         assert e_h <= cond.hidden_bound and e_mp <= cond.mp_bound and ok
