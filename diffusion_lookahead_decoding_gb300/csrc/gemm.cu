@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < SX; ++s) {
       mbar_init(smem_u32(&tail->xfull[s]), 1);
-      mbar_init(smem_u32(&tail->xempty[s]), 1);
+      mbar_init(smem_u32(&tail->xempty[s]), a.pair ? 2 : 1);  // paired: both CTAs' MMAs
     }
     mbar_init(smem_u32(&tail->accf), 1);
     if (kCluster) {
@@ -127,14 +127,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (kCluster) cluster_arrive_relaxed();  // this CTA's mbarriers are initialised
+  const bool paired = !kCluster && a.pair != 0;
+  if (kCluster || paired) cluster_arrive_relaxed();  // this CTA's mbarriers are initialised
   const uint32_t tmem = tail->tmem_addr;
   volatile int* abort = &tail->abort;
   pdl_trigger();
 
+  // Paired CTAs (cluster of 2 along x): each loads half of the activation tile and
+  // multicasts it to both; an activation slot is refilled only after both CTAs' MMAs
+  // released it (xempty counts two arrivals, committed to both CTAs).
+  const uint32_t crank = paired ? cluster_ctarank() : 0u;
   if (warp == 0 || warp == 2 + kEpiWarps) {
     // Producers: warp 0 streams the weight operand, the last warp the activation operand.
     const bool weights = warp == 0;
+    if (paired && !weights) cluster_wait();  // the peer's mbarriers are initialised
     if (lane == 0) {
       if (!weights) pdl_wait();  // activations are written by the previous kernel
       const int S = weights ? SW : SX;
@@ -163,6 +169,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int y1 = packed ? ((a_row[1] >> 7) * a.k_blocks + kb) * 128 : a_row[1];
           if (a_ok[0]) tma_load_2d(dst, &mapA, fb, kx, y0, pol);
           if (a_ok[1]) tma_load_2d(dst + a.a_tile_bytes, &mapA, fb, kx, y1, pol);
+        } else if (paired) {
+          const int hb = a.nbox / 2;  // rows of each CTA's half
+          tma_load_2d_mc(dst + crank * (uint32_t)hb * 128u, &mapB, fb, kx, b_row + (int)crank * hb,
+                         (uint16_t)0x3, pol);
         } else {
           const int y = packed ? ((b_row / a.nbox) * a.k_blocks + kb) * a.nbox : b_row;
           tma_load_2d(dst, &mapB, fb, kx, y, pol);
@@ -170,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
+    if (paired) cluster_wait();  // the peer's mbarriers are initialised
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(128, a.nbox);
       bool ok = true;
@@ -198,7 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         mma_commit(smem_u32(&tail->wempty[sw]));
-        mma_commit(smem_u32(&tail->xempty[sx]));
+        if (paired)
+          mma_commit_mc(smem_u32(&tail->xempty[sx]), (uint16_t)0x3);
+        else
+          mma_commit(smem_u32(&tail->xempty[sx]));
       }
       if (ok) mma_commit(smem_u32(&tail->accf));
     }
@@ -513,6 +527,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  if (paired) {
+    // Neither CTA leaves while the other may still signal or fill its shared memory:
+    // every MMA of both has completed once both pass this point (their accumulators were
+    // waited for), so all cross-CTA arrivals and copies have landed.
+    if (warp != 1 && warp != 2 + kEpiWarps) cluster_wait();  // (closes the start phase)
+    cluster_arrive_release();
+    cluster_wait();
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -627,7 +649,7 @@ int gemm_cluster_capacity(int mode, int cs, size_t smem) {
 // act: [act_rows_alloc][K] bf16 activations (T valid rows); w: [n_rows_w][K] bf16.
 const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_alloc, int T,
                       const void* w, int n_rows_w, int K, int na, int splits, int tok_box,
-                      int num_sms, bool w_packed) {
+                      int num_sms, bool w_packed, bool pair) {
   static thread_local char err[256];
   // Packed weights are viewed as [tiles * K/64 * tile_rows][64]: one box = one tile.
   auto weight_map = [&](CUtensorMap* map, int tile_rows) {
@@ -673,9 +695,16 @@ const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_all
       a.splits = a.k_blocks;
     }
     if (!weight_map(&L->mapA, 128)) return err;
-    if (!make_tmap_bf16(&L->mapB, act, act_rows_alloc, K, tok_box, err, sizeof(err))) return err;
+    if (!make_tmap_bf16(&L->mapB, act, act_rows_alloc, K, pair ? tok_box / 2 : tok_box, err,
+                        sizeof(err)))
+      return err;
     const int gx = (mode == GEMM_SWIGLU) ? (n_rows_w / 2) / 128 : (n_rows_w + a.na * 128 - 1) / (a.na * 128);
     L->grid = dim3(gx, a.splits, (T + tok_box - 1) / tok_box);
+    if (pair) {
+      if (gemm_mode_clustered(mode) || mode == GEMM_LMSTATS || a.na != 1 || gx % 2 != 0)
+        return "paired GEMM needs one 128-row tile per CTA and an even tile count";
+      a.pair = 1;
+    }
     a.w_slot_bytes = round1k(a.na * a.a_tile_bytes);
     a.x_slot_bytes = round1k(a.nbox * 128);
   }
@@ -699,14 +728,16 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   const dim3 blk(kThreads);
   switch (L.args.mode) {
     case GEMM_RED_ADD:
-      return launch_pdl(gemm_kernel<GEMM_RED_ADD>, L.grid, blk, L.smem, s, L.mapA, L.mapB, L.args);
+      return launch_pdl_cluster(gemm_kernel<GEMM_RED_ADD>, L.grid, blk, L.smem, s,
+                                L.args.pair ? dim3(2, 1, 1) : dim3(0, 0, 0), L.mapA, L.mapB, L.args);
     case GEMM_SWIGLU:
-      return launch_pdl(gemm_kernel<GEMM_SWIGLU>, L.grid, blk, L.smem, s, L.mapA, L.mapB, L.args);
+      return launch_pdl_cluster(gemm_kernel<GEMM_SWIGLU>, L.grid, blk, L.smem, s,
+                                L.args.pair ? dim3(2, 1, 1) : dim3(0, 0, 0), L.mapA, L.mapB, L.args);
     case GEMM_LMSTATS:
       return launch_pdl(gemm_kernel<GEMM_LMSTATS>, L.grid, blk, L.smem, s, L.mapA, L.mapB, L.args);
     case GEMM_QKV:
-      return launch_pdl_cluster(gemm_kernel<GEMM_QKV>, L.grid, blk, L.smem, s, L.args.splits,
-                                L.mapA, L.mapB, L.args);
+      return launch_pdl_cluster(gemm_kernel<GEMM_QKV>, L.grid, blk, L.smem, s,
+                                dim3(1, L.args.splits, 1), L.mapA, L.mapB, L.args);
     default:
       return cudaErrorInvalidValue;
   }

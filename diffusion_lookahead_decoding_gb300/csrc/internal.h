@@ -16,12 +16,12 @@ typedef __nv_bfloat16 bf16;
 void set_global_error(const char* msg);
 
 // Launches `kern` with programmatic stream serialization (the kernels call pdl_wait
-// before reading their predecessor's outputs) and, when cluster_y > 0, as thread-block
-// clusters of (1, cluster_y, 1) CTAs.
+// before reading their predecessor's outputs) and, when cluster.x > 0, as thread-block
+// clusters of `cluster` CTAs.
 bool pdl_enabled();
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                               cudaStream_t s, int cluster_y, Args... args) {
+                               cudaStream_t s, dim3 cluster, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -32,11 +32,11 @@ cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, si
   attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cluster_y > 0) {
+  if (cluster.x > 0) {
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 1;
-    attr[1].val.clusterDim.y = (unsigned)cluster_y;
-    attr[1].val.clusterDim.z = 1;
+    attr[1].val.clusterDim.x = cluster.x;
+    attr[1].val.clusterDim.y = cluster.y;
+    attr[1].val.clusterDim.z = cluster.z;
     cfg.numAttrs = 2;
   }
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
@@ -45,7 +45,7 @@ cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, si
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t s, Args... args) {
-  return launch_pdl_cluster(kern, grid, block, smem, s, 0, args...);
+  return launch_pdl_cluster(kern, grid, block, smem, s, dim3(0, 0, 0), args...);
 }
 
 // ------------------------------------------------------------------ GEMM (tcgen05)
@@ -76,6 +76,8 @@ struct GemmArgs {
   float scale;       // LMSTATS logit scale
   float* out_f32;    int ldo;
   int atomic;        // RED_ADD: 1 = atomicAdd into out_f32, 0 = store partial of split y
+  int pair;          // RED_ADD/SWIGLU: CTAs 2i, 2i+1 form a cluster sharing the activation
+                     // tile (each loads half and multicasts it); grid.x even, na = 1
   size_t split_stride;  // RED_ADD partials: elements between splits
   bf16* out_bf16;    int ldh;
   float* part_m; float* part_s; int* part_i; int part_ld;
@@ -106,10 +108,11 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 
 // Fills `L` for one GEMM.  Returns an empty string on success, else a reason.  With
 // w_packed the weight is in the tile-major layout written by launch_pack_tiles (tiles of
-// 128 rows, 256 for the LM head); otherwise it is row-major [n_rows_w][K].
+// 128 rows, 256 for the LM head); otherwise it is row-major [n_rows_w][K].  With pair
+// (RED_ADD / SWIGLU, na = 1, even tile count) neighbouring CTAs share the activation tile.
 const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_alloc, int T,
                       const void* w, int n_rows_w, int K, int na, int splits, int tok_box,
-                      int num_sms, bool w_packed = false);
+                      int num_sms, bool w_packed = false, bool pair = false);
 
 // Tile-major weight packing: [rows][K] row-major -> [ceil(rows/tile_rows)][K/64][tile_rows][64].
 size_t packed_elems(int rows, int K, int tile_rows);
