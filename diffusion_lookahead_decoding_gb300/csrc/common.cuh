@@ -269,8 +269,8 @@ __device__ __forceinline__ void pdl_trigger() {
 }
 
 // ---------------------------------------------------------------- thread-block clusters
-// Distributed shared memory: a CTA reads its cluster peers' shared memory through
-// shared::cluster addresses (mapa) and signals them through their mbarriers.
+// A CTA signals its cluster peers through their mbarriers, addressed with shared::cluster
+// addresses (mapa).
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -325,14 +325,6 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t
       return false;
     }
   }
-}
-__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
 }
 
 // ---------------------------------------------------------------- misc

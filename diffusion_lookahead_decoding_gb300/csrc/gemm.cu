@@ -10,10 +10,10 @@
 //             fp32 partial [split][T][N] (summed in a fixed order by the consumer) or,
 //             for the standalone call, adds it atomically into an fp32 [T][N] output.
 //   QKV     : the q/k/v projection.  The K-splits of one output tile form a thread-block
-//             cluster; each CTA stages its fp32 partial tile in shared memory and CTA r
-//             of the cluster sums token slice r over all splits (fixed split order)
-//             through distributed shared memory, applies RoPE to q/k and writes bf16 q,
-//             K and V (the Pre-Write).  These partial sums never leave the cluster.
+//             cluster; each CTA writes its fp32 partial tile to an L2 exchange region and
+//             CTA r of the cluster sums token slice r over all splits (fixed split order),
+//             applies RoPE to q/k and writes bf16 q, K and V (the Pre-Write).  Only the
+//             cluster's CTAs read these partials, right after they are written.
 //   SWIGLU  : two accumulators (gate rows f, up rows F+f) and an epilogue that writes
 //             bf16 silu(gate)*up for the down projection.
 //   LMSTATS : tokens on M (two 128-row tiles), 256 vocab rows on N; the epilogue keeps
@@ -50,12 +50,12 @@ struct SmemTail {
   uint64_t wfull[kMaxStages], wempty[kMaxStages];
   uint64_t xfull[kMaxStages], xempty[kMaxStages];
   uint64_t accf;
-  uint64_t cfull, cdone;  // clustered modes: all splits staged / all slices read
+  uint64_t cfull;  // clustered mode: every split's partial tile is in the exchange workspace
   uint32_t tmem_addr;
   int abort;
 };
 
-template <int MODE>
+template <int MODE, bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const GemmArgs a) {
@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool a_ok[2];
   int b_row;
   constexpr bool kCluster = MODE == GEMM_QKV;
+  constexpr bool paired = PAIR && MODE == GEMM_RED_ADD;  // a separate instantiation
   if (MODE == GEMM_RED_ADD || kCluster) {
     a_row[0] = blockIdx.x * a.na * 128;
     a_row[1] = a_row[0] + 128;
@@ -108,13 +109,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < SX; ++s) {
       mbar_init(smem_u32(&tail->xfull[s]), 1);
-      mbar_init(smem_u32(&tail->xempty[s]), a.pair ? 2 : 1);  // paired: both CTAs' MMAs
+      mbar_init(smem_u32(&tail->xempty[s]), paired ? 2 : 1);  // paired: both CTAs' MMAs
     }
     mbar_init(smem_u32(&tail->accf), 1);
-    if (kCluster) {
-      mbar_init(smem_u32(&tail->cfull), a.splits);
-      mbar_init(smem_u32(&tail->cdone), a.splits);
-    }
+    if (kCluster) mbar_init(smem_u32(&tail->cfull), a.splits);
     tail->abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&mapA);
@@ -127,7 +125,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const bool paired = !kCluster && a.pair != 0;
   if (kCluster || paired) cluster_arrive_relaxed();  // this CTA's mbarriers are initialised
   const uint32_t tmem = tail->tmem_addr;
   volatile int* abort = &tail->abort;
@@ -256,36 +253,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       return *abort == 0;
     };
     if (kCluster) {
-      // Split-K sum inside the cluster.  Per 128-row accumulator ("round"): every CTA
-      // stages its partial tile in its (now idle) smem rings and signals all peers' cfull;
-      // CTA `rank` then sums tokens [tlo, tlo + ntok) of the tile over the splits in split
-      // order, reading the peers' stages through distributed shared memory, and signals
-      // cdone so that peers may overwrite (or release) their stage.
+      // Split-K sum inside the cluster, through L2.  Per 128-row accumulator ("round"):
+      // every CTA writes its fp32 partial tile [token][128 columns] straight from TMEM to
+      // its region of the exchange workspace (coalesced: a warp covers a 128-byte row
+      // segment) and signals all peers' cfull (release, cluster scope); CTA `rank` then
+      // sums tokens [tlo, tlo + ntok) of the tile over the splits in split order with
+      // 16-byte L2 loads.  Regions are per round, so nothing is overwritten while read.
       const bool ok = nk > 0 && accum_ready();
       tc_fence_after();
-      float* stage = reinterpret_cast<float*>(smem);
       const int S = a.splits;
       const int rank = (int)cluster_ctarank();
-      uint32_t peer[kMaxClusterSplits];
-#pragma unroll
-      for (int c = 0; c < kMaxClusterSplits; ++c)
-        peer[c] = c < S ? mapa_shared(smem_u32(stage), (uint32_t)c) : 0u;
       const int tlo = rank * a.nbox / S, ntok = (rank + 1) * a.nbox / S - tlo;
-      const uint32_t cfull = smem_u32(&tail->cfull), cdone = smem_u32(&tail->cdone);
+      const uint32_t cfull = smem_u32(&tail->cfull);
       const int P = a.dP ? *a.dP : 0;
+      // Exchange region of split c, round i for this cluster (tile x, token block z).
+      auto region = [&](int i, int c) {
+        return a.xws + ((((size_t)blockIdx.z * gridDim.x + blockIdx.x) * 2 + i) * S + c) *
+                           (size_t)a.nbox * 128;
+      };
       cluster_wait();  // every peer's mbarriers are initialised
       int round = 0;
       for (int i = 0; i < 2; ++i) {
         if (!a_ok[i]) continue;  // the same for every CTA of the cluster
-        if (round > 0)
-          mbar_wait_cluster_bounded(cdone, (uint32_t)(round - 1) & 1u, abort, a.err,
-                                    DEV_TIMEOUT_CLUSTER);
-        if (ok) stage_acc(i, stage);
+        if (ok) {
+          float* mine = region(i, rank);
+          for (int ci = half; ci < nchunk; ci += 2) {
+            float v[16];
+            tmem_ld16(lane_base + (uint32_t)(i * 256 + ci * 16), v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) __stcg(mine + (size_t)(ci * 16 + j) * 128 + r, v[j]);
+          }
+          __threadfence();
+        }
         epilogue_sync();
         if (te == 0)
           for (int c = 0; c < S; ++c) mbar_arrive_cluster(mapa_shared(cfull, (uint32_t)c));
         if (mbar_wait_cluster_bounded(cfull, (uint32_t)round & 1u, abort, a.err,
                                       DEV_TIMEOUT_CLUSTER)) {
+          const float* src[kMaxClusterSplits];
+#pragma unroll
+          for (int c = 0; c < kMaxClusterSplits; ++c) src[c] = region(i, c < S ? c : 0);
           const int dh = a.dh, hdh = dh >> 1, per_head = dh >> 3;
           const int G = a.H / a.Hk;
           const int head0 = a_row[i] / dh;  // first head of this 128-row tile
@@ -301,13 +308,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int e = e0 + h * kStep;
               const int tt = tlo + (e >> 4), u = e & 15;
               const int hd = u / per_head, j = (u - hd * per_head) * 4;
-              const uint32_t off = (uint32_t)(tt * 128 + hd * dh + j) * 4u;
+              const int off = tt * 128 + hd * dh + j;
               if (e < nitem && head0 + hd < vfirst) {
 #pragma unroll
                 for (int c = 0; c < kMaxClusterSplits; ++c)
                   if (c < S) {
-                    v[h][0][c] = ld_dsmem_f4(peer[c] + off);
-                    v[h][1][c] = ld_dsmem_f4(peer[c] + off + (uint32_t)hdh * 4u);
+                    v[h][0][c] = __ldcg(reinterpret_cast<const float4*>(src[c] + off));
+                    v[h][1][c] = __ldcg(reinterpret_cast<const float4*>(src[c] + off + hdh));
                   }
               }
             }
@@ -356,11 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int k = 0; k < 8; ++k) {
                 acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (tt0 + k >= tlo + ntok) continue;
-                const uint32_t off = (uint32_t)((tt0 + k) * 128 + f) * 4u;
+                const int off = (tt0 + k) * 128 + f;
                 float4 w[kMaxClusterSplits];
 #pragma unroll
                 for (int c = 0; c < kMaxClusterSplits; ++c)
-                  if (c < S) w[c] = ld_dsmem_f4(peer[c] + off);
+                  if (c < S) w[c] = __ldcg(reinterpret_cast<const float4*>(src[c] + off));
                 acc[k] = w[0];
 #pragma unroll
                 for (int c = 1; c < kMaxClusterSplits; ++c)
@@ -398,15 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        epilogue_sync();
-        if (te == 0)
-          for (int c = 0; c < S; ++c) mbar_arrive_cluster(mapa_shared(cdone, (uint32_t)c));
         ++round;
       }
-      // Stay resident until every peer has finished reading this CTA's stage.
-      if (round > 0)
-        mbar_wait_cluster_bounded(cdone, (uint32_t)(round - 1) & 1u, abort, a.err,
-                                  DEV_TIMEOUT_CLUSTER);
     } else if (nk > 0 && accum_ready()) {
       tc_fence_after();
       float* stage = reinterpret_cast<float*>(smem);
@@ -600,13 +600,15 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 
 int gemm_max_smem() { return kMaxSmem; }
 
-template <int MODE>
+template <int MODE, bool PAIR = false>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(gemm_kernel<MODE>);
+  return reinterpret_cast<const void*>(gemm_kernel<MODE, PAIR>);
 }
 
+// Indexed by mode; the paired split-K instantiation last.
 const void* const kKernels[] = {kernel_ptr<GEMM_RED_ADD>(), kernel_ptr<GEMM_SWIGLU>(),
-                                kernel_ptr<GEMM_LMSTATS>(), kernel_ptr<GEMM_QKV>()};
+                                kernel_ptr<GEMM_LMSTATS>(), kernel_ptr<GEMM_QKV>(),
+                                kernel_ptr<GEMM_RED_ADD, true>()};
 
 cudaError_t gemm_set_smem_limits() {
   for (const void* k : kKernels) {
@@ -701,8 +703,8 @@ const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_all
     const int gx = (mode == GEMM_SWIGLU) ? (n_rows_w / 2) / 128 : (n_rows_w + a.na * 128 - 1) / (a.na * 128);
     L->grid = dim3(gx, a.splits, (T + tok_box - 1) / tok_box);
     if (pair) {
-      if (gemm_mode_clustered(mode) || mode == GEMM_LMSTATS || a.na != 1 || gx % 2 != 0)
-        return "paired GEMM needs one 128-row tile per CTA and an even tile count";
+      if (mode != GEMM_RED_ADD || a.na != 1 || gx % 2 != 0)
+        return "paired GEMM needs the split-K mode, one 128-row tile per CTA, an even tile count";
       a.pair = 1;
     }
     a.w_slot_bytes = round1k(a.na * a.a_tile_bytes);
@@ -728,11 +730,12 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   const dim3 blk(kThreads);
   switch (L.args.mode) {
     case GEMM_RED_ADD:
-      return launch_pdl_cluster(gemm_kernel<GEMM_RED_ADD>, L.grid, blk, L.smem, s,
-                                L.args.pair ? dim3(2, 1, 1) : dim3(0, 0, 0), L.mapA, L.mapB, L.args);
+      if (L.args.pair)
+        return launch_pdl_cluster(gemm_kernel<GEMM_RED_ADD, true>, L.grid, blk, L.smem, s,
+                                  dim3(2, 1, 1), L.mapA, L.mapB, L.args);
+      return launch_pdl(gemm_kernel<GEMM_RED_ADD>, L.grid, blk, L.smem, s, L.mapA, L.mapB, L.args);
     case GEMM_SWIGLU:
-      return launch_pdl_cluster(gemm_kernel<GEMM_SWIGLU>, L.grid, blk, L.smem, s,
-                                L.args.pair ? dim3(2, 1, 1) : dim3(0, 0, 0), L.mapA, L.mapB, L.args);
+      return launch_pdl(gemm_kernel<GEMM_SWIGLU>, L.grid, blk, L.smem, s, L.mapA, L.mapB, L.args);
     case GEMM_LMSTATS:
       return launch_pdl(gemm_kernel<GEMM_LMSTATS>, L.grid, blk, L.smem, s, L.mapA, L.mapB, L.args);
     case GEMM_QKV:

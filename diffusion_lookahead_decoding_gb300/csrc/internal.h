@@ -60,6 +60,11 @@ enum GemmMode : int {
 // shared memory; such a cluster has 1, 2 or 4 CTAs.
 inline bool gemm_mode_clustered(int mode) { return mode == GEMM_QKV; }
 constexpr int kMaxClusterSplits = 4;
+// Floats of the QKV exchange workspace a launch with grid (gx, splits, gz) and token box
+// nbox needs: per (tile, token block) two rounds x splits regions of nbox x 128 floats.
+inline size_t qkv_exchange_floats(int gx, int splits, int gz, int nbox) {
+  return (size_t)gx * gz * 2 * splits * nbox * 128;
+}
 
 struct GemmArgs {
   int mode;
@@ -76,8 +81,8 @@ struct GemmArgs {
   float scale;       // LMSTATS logit scale
   float* out_f32;    int ldo;
   int atomic;        // RED_ADD: 1 = atomicAdd into out_f32, 0 = store partial of split y
-  int pair;          // RED_ADD/SWIGLU: CTAs 2i, 2i+1 form a cluster sharing the activation
-                     // tile (each loads half and multicasts it); grid.x even, na = 1
+  int pair;          // RED_ADD: CTAs 2i, 2i+1 form a cluster sharing the activation tile
+                     // (each loads half and multicasts it); grid.x even, na = 1
   size_t split_stride;  // RED_ADD partials: elements between splits
   bf16* out_bf16;    int ldh;
   float* part_m; float* part_s; int* part_i; int part_ld;
@@ -89,6 +94,7 @@ struct GemmArgs {
   const float* cos_t; const float* sin_t;  // [positions][dh/2]
   const int* dP;
   int H, Hk, dh, Bq, kv_to_cache;
+  float* xws;        // QKV: split-K exchange workspace (see qkv_exchange_floats)
   int* err;
   int w_packed;      // weight operand in tile-major layout (see launch_pack_tiles)
 };
@@ -109,7 +115,7 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 // Fills `L` for one GEMM.  Returns an empty string on success, else a reason.  With
 // w_packed the weight is in the tile-major layout written by launch_pack_tiles (tiles of
 // 128 rows, 256 for the LM head); otherwise it is row-major [n_rows_w][K].  With pair
-// (RED_ADD / SWIGLU, na = 1, even tile count) neighbouring CTAs share the activation tile.
+// (RED_ADD, na = 1, even tile count) neighbouring CTAs share the activation tile.
 const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_alloc, int T,
                       const void* w, int n_rows_w, int K, int na, int splits, int tok_box,
                       int num_sms, bool w_packed = false, bool pair = false);

@@ -80,6 +80,8 @@ struct lopa_ctx {
   bf16* n = nullptr;
   float* part = nullptr;  // split-K partial sums [split][T][d] of the O and down projections
   size_t part_floats = 0;
+  float* xws = nullptr;   // q/k/v split-K exchange workspace
+  size_t xws_floats = 0;
   bf16 *q = nullptr, *attn = nullptr, *hm = nullptr;
   float *pm = nullptr, *ps = nullptr;
   int* pi = nullptr;
@@ -271,6 +273,9 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
     qa.dh = dh;
     qa.Bq = Bq;
     qa.kv_to_cache = kv_to_cache;
+    qa.xws = ctx->xws;
+    if (qkv_exchange_floats(p.qkv[l].grid.x, qa.splits, p.qkv[l].grid.z, qa.nbox) > ctx->xws_floats)
+      return fail(ctx, LOPA_ERR_UNSUPPORTED, "q/k/v exchange workspace too small");
     AttnArgs aa;
     aa.q = ctx->q;
     aa.out = ctx->attn;
@@ -464,11 +469,25 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
   ctx->part_floats = std::max(partial_floats(ctx, ctx->nbmax * B),
                               std::max(partial_floats(ctx, B), partial_floats(ctx, ctx->dc.max_prompt)));
   const size_t T = ctx->Tmax;
+  {
+    // q/k/v exchange workspace: the largest any forward needs (1..nbmax branches of one
+    // block, or the prompt).
+    auto need = [&](int T2) {
+      int na, cs;
+      qkv_tiling(ctx, ctx->qkv_rows, d, T2, &na, &cs);
+      const int nbox = std::min(256, round16(T2));
+      const int gx = (ctx->qkv_rows + na * 128 - 1) / (na * 128);
+      return qkv_exchange_floats(gx, cs, (T2 + nbox - 1) / nbox, nbox);
+    };
+    ctx->xws_floats = need(ctx->dc.max_prompt);
+    for (int nb = 1; nb <= ctx->nbmax; ++nb) ctx->xws_floats = std::max(ctx->xws_floats, need(nb * B));
+  }
   int r;
   if ((r = dalloc(ctx, &ctx->kc, ctx->cache_layer * L)) || (r = dalloc(ctx, &ctx->vc, ctx->vt_cache_layer * L)) ||
       (r = dalloc(ctx, &ctx->ks, ctx->scr_layer * L)) || (r = dalloc(ctx, &ctx->vs, ctx->scr_layer * L)) ||
       (r = dalloc(ctx, &ctx->x, T * d)) || (r = dalloc(ctx, &ctx->n, T * d)) ||
       (r = dalloc(ctx, &ctx->part, ctx->part_floats)) || (r = dalloc(ctx, &ctx->q, T * H * dh)) ||
+      (r = dalloc(ctx, &ctx->xws, ctx->xws_floats)) ||
       (r = dalloc(ctx, &ctx->attn, T * H * dh)) || (r = dalloc(ctx, &ctx->hm, T * F)) ||
       (r = dalloc(ctx, &ctx->pm, (size_t)ctx->nvt * ctx->part_ld)) ||
       (r = dalloc(ctx, &ctx->ps, (size_t)ctx->nvt * ctx->part_ld)) ||
