@@ -170,6 +170,20 @@ def gemm_flops(shape, T, kind):
     return 2 * n * T
 
 
+def verify_bytes_flops(shape, T, P, B):
+    """Algorithmic bytes and flops of one verification forward over T token rows (blocks
+    of B) at prefix P: every weight read once (projections and LM head, bf16), the prefix
+    K/V read once and the block K/V written once (bf16); 2 flops per weight per row plus
+    the attention's q.k and p.v (4 per query, key and dimension, P + B keys per query)."""
+    L, d, H, Hk, dh, F, V = (shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads,
+                             shape.head_dim, shape.ffn, shape.vocab)
+    params = L * (d * H * dh + 2 * d * Hk * dh + H * dh * d + 3 * d * F) + V * d
+    kv = L * 2 * Hk * dh * 2
+    by = 2 * params + P * kv + T * kv
+    fl = 2 * params * T + 4 * L * H * dh * T * (P + B)
+    return by, fl
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -266,7 +280,9 @@ def main():
     value = world * tokens / elapsed
     tpf = tokens / forwards
     ms_per_forward = elapsed * 1e3 / forwards
-    launches_per_forward = 8 * shape.n_layers + 3
+    # per layer: q/k/v, attention, O, residual+norm, gate/up, down, residual+norm; then
+    # embedding, LM head, merge
+    launches_per_forward = 7 * shape.n_layers + 3
     gpu_launches = forwards * launches_per_forward + iters * 4
 
     # Per-kernel timing of the projection GEMMs in the step's launch configuration.
@@ -287,6 +303,23 @@ def main():
     roofline = {"kernel": "gemm_kernel<SWIGLU> (gate/up + SwiGLU)", "bound": "hbm",
                 "achieved": dom["GB/s"], "peak": peak_bw, "unit": "GB/s",
                 "frac": dom["GB/s"] / peak_bw, "traffic": None, "peak_source": peak_src}
+
+    # Verification-step latency: the forward-only graph of the 8-branch verification (and
+    # of the block-start forward), median of 50 back-to-back launches, at a mid-decode
+    # prefix; against the step's algorithmic bytes (every weight once, the prefix K/V
+    # once, the block K/V written once) and flops.
+    Pv = P0 + (gen // 2 // B) * B
+    dec.rewind(Pv)
+    v_med, v_mean = dec.time_forward(1, 50)
+    s_med, _ = dec.time_forward(0, 50)
+    vb, vf = verify_bytes_flops(shape, T, Pv, B)
+    peak_tc = float(peaks.get("bf16_tflops_sustained", 1700.0)) if peaks else 1700.0
+    t_hbm, t_tc = vb / peak_bw / 1e6, vf / peak_tc / 1e9
+    verify = {"ms_median": v_med, "ms_mean": v_mean, "prefix": Pv, "rows": T,
+              "bytes": vb, "flops": vf, "hbm_roofline_ms": t_hbm, "tensor_roofline_ms": t_tc,
+              "frac_hbm_roofline": t_hbm / v_med, "frac_roofline": max(t_hbm, t_tc) / v_med,
+              "block_start_forward_ms_median": s_med,
+              "peaks": {"hbm_gbs": peak_bw, "bf16_tflops_sustained": peak_tc, "source": peak_src}}
 
     # End to end through the public API with host buffers: prompt H2D, tokens D2H.
     import torch as _t
@@ -325,6 +358,7 @@ def main():
                        "l2": "inputs larger than L2 (15 GB weights re-streamed per forward)"},
             "tpf": tpf, "ms_per_forward": ms_per_forward,
             "lopa_iterations": iters, "blocks": blocks, "forwards": forwards,
+            "verify_step": verify,
             "kernels": kern, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": gpu_launches, "clocks": clocks.summary(),
             "weight_gen_s": t_gen,

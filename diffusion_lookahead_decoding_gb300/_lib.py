@@ -74,6 +74,8 @@ SIGNATURES = {
     "lopa_read_branch_kv": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.POINTER(C.c_uint16),
                                       C.POINTER(C.c_uint16)]),
     "lopa_time_gemm": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.POINTER(C.c_float)]),
+    "lopa_time_forward": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.POINTER(C.c_float),
+                                    C.POINTER(C.c_float)]),
     "lopa_linear_accumulate": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
                                          C.c_int, C.c_void_p]),
     "lopa_lmhead_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int]),

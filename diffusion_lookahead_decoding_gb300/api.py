@@ -114,6 +114,14 @@ class LopaDecoder:
         L.check(self.lib.lopa_time_gemm(self.ctx, kind, iters, C.byref(ms)), self.ctx)
         return ms.value
 
+    def time_forward(self, kind: int, iters: int):
+        """(median, mean) ms per launch of the forward-only graph: kind 1 = verification
+        forward of all branches, 0 = block-start forward."""
+        med, mean = C.c_float(), C.c_float()
+        L.check(self.lib.lopa_time_forward(self.ctx, kind, iters, C.byref(med), C.byref(mean)),
+                self.ctx)
+        return med.value, mean.value
+
     # -- inspection -----------------------------------------------------------------
     def get_block_state(self):
         B = self.block

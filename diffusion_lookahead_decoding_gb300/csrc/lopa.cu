@@ -99,6 +99,10 @@ struct lopa_ctx {
   // graphs
   Plan step_plan, start_plan;
   cudaGraphExec_t step_exec = nullptr, start_exec = nullptr;
+  // lopa_time_forward: forward-only graphs (0 block start, 1 verification), built lazily
+  Plan time_start_plan;
+  const Plan* fwd_plan = nullptr;
+  cudaGraphExec_t fwd_exec[2] = {nullptr, nullptr};
   cudaEvent_t ev0 = nullptr, ev1 = nullptr;
   lopa_step_result* h_res = nullptr;  // pinned
   // host-side view of the decode
@@ -544,6 +548,8 @@ void destroy(lopa_ctx* ctx) {
   if (!ctx) return;
   if (ctx->stream) cudaStreamSynchronize(ctx->stream);
   if (ctx->step_exec) cudaGraphExecDestroy(ctx->step_exec);
+  for (auto e : ctx->fwd_exec)
+    if (e) cudaGraphExecDestroy(e);
   if (ctx->start_exec) cudaGraphExecDestroy(ctx->start_exec);
   if (ctx->ev0) cudaEventDestroy(ctx->ev0);
   if (ctx->ev1) cudaEventDestroy(ctx->ev1);
@@ -731,6 +737,52 @@ int lopa_time_gemm(lopa_ctx* ctx, int kind, int iters, float* avg_ms) {
   cudaGraphExecDestroy(ge);
   if (ce != cudaSuccess) return fail(ctx, LOPA_ERR_CUDA, "timed GEMMs: %s", cudaGetErrorString(ce));
   *avg_ms = ms / iters;
+  return check_device_error(ctx);
+}
+
+int lopa_time_forward(lopa_ctx* ctx, int kind, int iters, float* median_ms, float* mean_ms) {
+  if (!ctx) return fail(nullptr, LOPA_ERR_INVALID_ARG, "ctx is null");
+  if ((kind != 0 && kind != 1) || iters < 1 || iters > 10000 || !median_ms)
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "bad kind/iters");
+  if (!ctx->prefilled) return fail(ctx, LOPA_ERR_BAD_STATE, "time_forward before lopa_prefill");
+  if (ctx->P + ctx->dc.block > ctx->mc.max_seq)
+    return fail(ctx, LOPA_ERR_BAD_STATE, "no room for a block at prefix %d (max_seq %d)", ctx->P,
+                ctx->mc.max_seq);
+  cudaStream_t s = ctx->stream;
+  if (!ctx->fwd_exec[kind]) {
+    // Forward-only graphs.  The block-start one writes its logit summary to the branch
+    // buffers (not the block state), so neither changes the decoding state.
+    Plan& p = kind == 1 ? ctx->step_plan : ctx->time_start_plan;
+    int r;
+    if (kind == 0 && (r = build_plan(ctx, p, 1, ctx->dc.block, 0, true, ctx->st->tok, ctx->am_b,
+                                     ctx->mp_b)))
+      return r;
+    ctx->fwd_plan = &p;
+    if ((r = capture(ctx, [](lopa_ctx* c) { return enqueue_forward(c, *c->fwd_plan); },
+                     &ctx->fwd_exec[kind])))
+      return r;
+  }
+  std::vector<cudaEvent_t> ev(iters + 1, nullptr);
+  cudaError_t ce = cudaSuccess;
+  for (auto& e : ev)
+    if (ce == cudaSuccess) ce = cudaEventCreate(&e);
+  if (ce == cudaSuccess) ce = cudaGraphLaunch(ctx->fwd_exec[kind], s);  // warm-up
+  if (ce == cudaSuccess) ce = cudaEventRecord(ev[0], s);
+  for (int i = 0; i < iters && ce == cudaSuccess; ++i) {
+    ce = cudaGraphLaunch(ctx->fwd_exec[kind], s);
+    if (ce == cudaSuccess) ce = cudaEventRecord(ev[i + 1], s);
+  }
+  if (ce == cudaSuccess) ce = cudaEventSynchronize(ev[iters]);
+  std::vector<float> ms(iters, 0.f);
+  for (int i = 0; i < iters && ce == cudaSuccess; ++i) ce = cudaEventElapsedTime(&ms[i], ev[i], ev[i + 1]);
+  for (auto e : ev)
+    if (e) cudaEventDestroy(e);
+  if (ce != cudaSuccess) return fail(ctx, LOPA_ERR_CUDA, "timed forward: %s", cudaGetErrorString(ce));
+  double sum = 0;
+  for (float v : ms) sum += v;
+  std::sort(ms.begin(), ms.end());
+  *median_ms = ms[iters / 2];
+  if (mean_ms) *mean_ms = (float)(sum / iters);
   return check_device_error(ctx);
 }
 

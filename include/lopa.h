@@ -63,9 +63,12 @@ typedef struct {
   float logit_scale; /* logits = logit_scale * (final_hidden . lm_head_row) */
 } lopa_model_config;
 
-/* Borrowed device pointers (bf16), which must outlive the context.  Per-layer entries
- * are HOST arrays of n_layers device pointers; the arrays themselves are copied at
- * init and need not outlive the call. */
+/* Device pointers (bf16).  Per-layer entries are HOST arrays of n_layers device
+ * pointers; the arrays themselves are copied at init and need not outlive the call.
+ * lopa_init_model copies the projection matrices (wqkv, wo, wgu, wd) and lm_head into
+ * context-owned tile-major copies (the layout the GEMMs stream); the embedding and the
+ * norm gains stay borrowed and must outlive the context.  The caller may free the
+ * projection matrices and lm_head after init. */
 typedef struct {
   const void* embed;              /* [vocab][d_model] */
   const void* lm_head;            /* [vocab][d_model] */
@@ -107,10 +110,12 @@ typedef struct {
   double seconds;     /* device time of the decode (CUDA events), prefill excluded */
 } lopa_stats;
 
-/* Validates the configs, records the borrowed weight pointers, allocates the static KV
- * cache [L][max_seq][Hk][dh] (K and V), the per-branch Pre-Write scratch, activations
- * and state, precomputes RoPE tables and captures the iteration into CUDA graphs.
- * stream: cudaStream_t to enqueue on (borrowed).  *out receives the context. */
+/* Validates the configs, copies the projection weights into tile-major owned copies,
+ * records the borrowed embedding / norm pointers, allocates the static KV cache (K as
+ * [L][max_seq][Hk][dh], V transposed as [L][Hk*dh][positions]), the per-branch Pre-Write
+ * scratch, activations and state, precomputes RoPE tables and captures the iteration
+ * into CUDA graphs.  stream: cudaStream_t to enqueue on (borrowed).  *out receives the
+ * context.  Weight memory: about the size of the projection weights plus lm_head. */
 int lopa_init_model(const lopa_model_config* cfg, const lopa_weights* w,
                     const lopa_decode_config* dcfg, void* stream, lopa_ctx** out);
 
@@ -140,7 +145,8 @@ int lopa_rewind(lopa_ctx* ctx, int pos);
 /* Message of the last failed call on ctx (or of the last failed init when ctx is NULL). */
 const char* lopa_last_error(const lopa_ctx* ctx);
 
-/* Frees everything the context owns (not the borrowed weights or stream). */
+/* Frees everything the context owns (including the weight copies; not the borrowed
+ * embedding / norm gains or the stream). */
 void lopa_free(lopa_ctx* ctx);
 
 /* ---- inspection (used by parity tests) ---------------------------------------- */
@@ -240,6 +246,16 @@ int lopa_branch_attention(const void* q, const void* k_prefix, const void* vt_pr
  * in milliseconds (CUDA events) to *avg_ms.  The decoding state is not changed; the
  * activation buffers hold garbage afterwards until the next forward rewrites them. */
 int lopa_time_gemm(lopa_ctx* ctx, int kind, int iters, float* avg_ms);
+
+/* Verification-step latency: launches the captured forward of one kind (1 = the
+ * (1+k)-branch verification forward of a LoPA iteration, steps a3-a8 over the current
+ * branch tokens; 0 = the block-start forward of the current block) `iters` times back to
+ * back (1 <= iters <= 10000) on the context stream, each bracketed by CUDA events, and
+ * writes the median (and, if mean_ms is not NULL, the mean) per-launch milliseconds.
+ * Needs a prefilled context with room for a block at the current prefix (else
+ * LOPA_ERR_BAD_STATE).  The forwards write only activations, the Pre-Write scratch and
+ * the per-branch logit summaries: the decoding state is unchanged. */
+int lopa_time_forward(lopa_ctx* ctx, int kind, int iters, float* median_ms, float* mean_ms);
 
 /* Library version (major*10000 + minor*100 + patch). */
 int lopa_version(void);

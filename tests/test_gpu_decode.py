@@ -211,3 +211,32 @@ def test_state_errors_leave_state_unchanged():
     dec.rewind(dshape.prompt_len)
     toks2, _ = dec.decode(dshape.gen_len)  # a rewound decode reproduces the tokens
     np.testing.assert_array_equal(toks2, toks)
+
+
+@pytest.mark.parametrize("wl", ["tiny", "small"])
+def test_timed_forwards_leave_the_decode_unchanged(wl):
+    """lopa_time_forward runs the forward-only graphs (verification and block start) in the
+    middle of a decode; the decode then continues exactly as an untimed one, and the call
+    refuses a context without room for a block."""
+    from diffusion_lookahead_decoding_gb300 import _lib as L
+    shape, dshape, w = workload_weights(wl)
+    prompt = synth.make_prompt(shape, dshape.prompt_len, seed=1)
+    ref = make_decoder(wl)
+    ref.prefill(prompt)
+    ref_toks, _ = ref.decode(dshape.gen_len)
+    dec = make_decoder(wl)
+    dec.prefill(prompt)
+    dec.step()
+    before = dec.get_block_state()
+    for kind in (1, 0):
+        med, mean = dec.time_forward(kind, 3)
+        assert 0 < med and 0 < mean
+    after = dec.get_block_state()
+    for x, y in zip(before, after):
+        np.testing.assert_array_equal(x, y)
+    dec.rewind(dshape.prompt_len)
+    toks, _ = dec.decode(dshape.gen_len)
+    np.testing.assert_array_equal(toks, ref_toks)
+    with pytest.raises(L.LopaError) as e:
+        dec.time_forward(1, 1)  # the decode filled the cache
+    assert e.value.code == L.ERR_BAD_STATE
