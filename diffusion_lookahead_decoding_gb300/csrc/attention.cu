@@ -49,14 +49,15 @@ __device__ __forceinline__ KeySched key_sched(const AttnArgs& a, int b_lo, int b
   KeySched k;
   k.Pk = a.pk_add + (a.dP ? *a.dP : 0);
   k.n_pre = (k.Pk + kKeyTile - 1) / kKeyTile;
-  k.kb_lo = b_lo * a.Bk_stride;
+  k.kb_lo = (a.causal ? 0 : b_lo) * a.Bk_stride;
   const int kb_end = b_hi * a.Bk_stride + a.Bk;
   k.n_br = a.Bk > 0 ? (kb_end - k.kb_lo + kKeyTile - 1) / kKeyTile : 0;
   return k;
 }
 
 // Key columns [lo, hi) of tile j (tile-local) that a row of branch br may see: the
-// committed prefix, or the br-th branch's own block keys.
+// committed prefix, or the br-th branch's own block keys (with `causal`, the keys of
+// blocks 0..br).
 __device__ __forceinline__ void visible_range(const AttnArgs& a, const KeySched& k, int j, int br,
                                               int& lo, int& hi) {
   if (j < k.n_pre) {
@@ -64,8 +65,9 @@ __device__ __forceinline__ void visible_range(const AttnArgs& a, const KeySched&
     hi = k.Pk - j * kKeyTile;
     return;
   }
-  lo = br * a.Bk_stride - (k.kb_lo + (j - k.n_pre) * kKeyTile);
-  hi = lo + a.Bk;
+  const int col0 = k.kb_lo + (j - k.n_pre) * kKeyTile;
+  lo = (a.causal ? 0 : br * a.Bk_stride) - col0;
+  hi = br * a.Bk_stride + a.Bk - col0;
 }
 
 // 2^x on the special-function unit (ex2.approx: relative error about 2^-22; 2^-inf = 0).
@@ -714,6 +716,7 @@ const char* plan_attention(AttnLaunch* L, const AttnArgs& a, int dh, int kc_rows
   const int T = a.nbq * a.Bq;
   if (a.H % a.Hk || T < 1) return "attention: bad head grouping or empty batch";
   if (a.Bk > a.Bk_stride || (a.Bk > 0 && a.Bk_stride % 8)) return "attention: block stride must be a multiple of 8";
+  if (a.causal && a.Bk != a.Bk_stride) return "attention: block-causal keys must be contiguous";
   if (a.ldvc % 8 || a.ldvb % 8 || (a.Bk > 0 && a.ldvb < a.nbq * a.Bk_stride))
     return "attention: V^T row lengths must be multiples of 8 covering every branch";
   if (dh == 32 || dh == 64) {

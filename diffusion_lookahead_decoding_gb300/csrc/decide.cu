@@ -62,15 +62,31 @@ __global__ void decide_kernel(DevState* st, int B, int k, float tau, int mask_id
     if (rank < nl) s_cand[rank] = i;
   }
   __syncthreads();
+  // The iteration completes the block when no position stays masked after the anchor
+  // fill (the anchor completes it) or exactly one does and lookahead branch 1 fills it.
+  // A completing branch has confidence 1.0 and every other branch less (its mean covers
+  // at least one masked position), so the lowest completing branch wins whatever the
+  // forward returns: final_w.  Only it is evaluated: its tokens go to slot 0, and slot 1
+  // becomes a blank block for a block-start forward merged into the same pass.
+  const int final_w = nrem == 0 ? 0 : (nrem == 1 && nl >= 1 ? 1 : -1);
   if (i < B) {
-    for (int b = 0; b < nb; ++b) {
-      const bool extra = b >= 1 && s_cand[b - 1] == i;
-      branch_tok[b * B + i] = extra ? am : anchor;
+    if (final_w >= 0) {
+      const bool extra = final_w == 1 && s_cand[0] == i;
+      branch_tok[i] = extra ? am : anchor;
+      branch_tok[B + i] = mask_id;
+    } else {
+      for (int b = 0; b < nb; ++b) {
+        const bool extra = b >= 1 && s_cand[b - 1] == i;
+        branch_tok[b * B + i] = extra ? am : anchor;
+      }
     }
   }
-  if (i < nb) valid[i] = (i == 0) || (i - 1 < nl);
+  if (i < nb) valid[i] = final_w >= 0 ? i == 0 : (i == 0) || (i - 1 < nl);
   if (i < LOPA_MAX_BRANCHES) st->cand[i] = s_cand[i];
-  if (i == 0) st->n_valid = 1 + nl;
+  if (i == 0) {
+    st->n_valid = 1 + nl;
+    st->final_w = final_w;
+  }
 }
 
 __global__ void select_kernel(DevState* st, int B, int nb, int mask_id,
@@ -127,8 +143,12 @@ __global__ void select_kernel(DevState* st, int B, int nb, int mask_id,
       }
       if (s_new[j] == mask_id) done = 0;
     }
-    for (int b = 0; b < LOPA_MAX_BRANCHES; ++b) r.conf[b] = b < nb ? s_conf[b] : -INFINITY;
-    r.winner = w;
+    // In a completing iteration only the winner (slot 0) was evaluated: it is reported
+    // under its branch index, every other branch as -inf.
+    const int fw = st->final_w;
+    for (int b = 0; b < LOPA_MAX_BRANCHES; ++b)
+      r.conf[b] = fw >= 0 ? (b == fw ? s_conf[0] : -INFINITY) : (b < nb ? s_conf[b] : -INFINITY);
+    r.winner = fw >= 0 ? fw : w;
     r.n_filled = nf;
     r.block_done = done;
     r.n_valid_branches = st->n_valid;
@@ -169,7 +189,10 @@ __global__ void commit_kv_kernel(const DevState* st, const bf16* __restrict__ ks
   }
 }
 
-__global__ void finalize_kernel(DevState* st, int B, int mask_id, int* __restrict__ out_tokens) {
+// With am_next / mp_next (the logit summary of a block-start forward run in the same
+// pass) a finished block is followed by the next block with its first logits in place.
+__global__ void finalize_kernel(DevState* st, int B, int mask_id, int* __restrict__ out_tokens,
+                                const int* __restrict__ am_next, const float* __restrict__ mp_next) {
   pdl_wait();
   pdl_trigger();
   const int i = threadIdx.x;
@@ -180,6 +203,10 @@ __global__ void finalize_kernel(DevState* st, int B, int mask_id, int* __restric
   if (i < B) {
     out_tokens[P - P0 + i] = st->tok[i];
     st->tok[i] = mask_id;
+    if (am_next) {
+      st->am[i] = am_next[i];
+      st->mp[i] = mp_next[i];
+    }
   }
   if (i == 0) st->P = P + B;
 }
@@ -199,6 +226,7 @@ __global__ void state_reset_kernel(DevState* st, int P, int B, int mask_id) {
     st->block_done = 0;
     st->err = 0;
     st->n_valid = 0;
+    st->final_w = -1;
   }
 }
 
@@ -237,9 +265,10 @@ cudaError_t launch_commit_kv(const void* st, const bf16* ks, const bf16* vts, bf
                     static_cast<const DevState*>(st), ks, vts, kc, vtc, B, row_elems, kv);
 }
 
-cudaError_t launch_finalize(void* st, int B, int mask_id, int* out_tokens, cudaStream_t s) {
+cudaError_t launch_finalize(void* st, int B, int mask_id, int* out_tokens, const int* am_next,
+                            const float* mp_next, cudaStream_t s) {
   return launch_pdl(finalize_kernel, dim3(1), dim3(LOPA_MAX_BLOCK), 0, s,
-                    static_cast<DevState*>(st), B, mask_id, out_tokens);
+                    static_cast<DevState*>(st), B, mask_id, out_tokens, am_next, mp_next);
 }
 
 cudaError_t launch_state_reset(void* st, int P, int B, int mask_id, cudaStream_t s) {

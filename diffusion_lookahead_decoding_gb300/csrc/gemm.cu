@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   x2.x += v[h][1][c].x; x2.y += v[h][1][c].y; x2.z += v[h][1][c].z; x2.w += v[h][1][c].w;
                 }
               // RoPE, rotate-half form, at absolute position P + bi.
-              const int bi = t % a.Bq;
+              const int bi = a.pos_linear ? t : t % a.Bq;
               const float4 cs = *reinterpret_cast<const float4*>(a.cos_t + (size_t)(P + bi) * hdh + j);
               const float4 sn = *reinterpret_cast<const float4*>(a.sin_t + (size_t)(P + bi) * hdh + j);
               const float4 y1 = make_float4(x1.x * cs.x - x2.x * sn.x, x1.y * cs.y - x2.y * sn.y,

@@ -94,6 +94,8 @@ struct GemmArgs {
   const float* cos_t; const float* sin_t;  // [positions][dh/2]
   const int* dP;
   int H, Hk, dh, Bq, kv_to_cache;
+  int pos_linear;    // QKV: token row t sits at position *dP + t (consecutive blocks), not
+                     // *dP + t % Bq (parallel branches of one block)
   float* xws;        // QKV: split-K exchange workspace (see qkv_exchange_floats)
   int* err;
   int w_packed;      // weight operand in tile-major layout (see launch_pack_tiles)
@@ -151,6 +153,8 @@ struct AttnArgs {
   const int* dP;       // device prefix length (may be null -> 0)
   int pk_add;          // prefix keys = *dP + pk_add
   int ldvc, ldvb;      // row lengths of vtc and vtb (multiples of 8)
+  int causal;          // 0: branch b sees its own block keys; 1: blocks 0..b (consecutive
+                       // blocks of one sequence, e.g. a finished block and the next one)
   int Bq, Bk, Bk_stride, nbq, H, Hk;
   int* err;            // device error word (bounded waits), may be null
 };
@@ -187,7 +191,9 @@ struct DevState {
   int block_done;   // 1 when the last iteration completed the block
   int err;          // device error word (DeviceError)
   int n_valid;      // 1 + number of lookahead branches built by the last decide
-  int pad[2];
+  int final_w;      // the last decide's iteration completes the block with this branch
+                    // (its tokens in slot 0, a blank block in slot 1), else -1
+  int pad;
   int tok[LOPA_MAX_BLOCK];   // current block tokens ([MASK] where unfilled)
   int am[LOPA_MAX_BLOCK];    // greedy token of the logits that produced `tok`
   float mp[LOPA_MAX_BLOCK];  // its probability
@@ -195,6 +201,8 @@ struct DevState {
   lopa_step_result res;
 };
 
+// branch_tok holds max(k + 1, 2) blocks of B tokens: a completing iteration writes its
+// winner to block 0 and a blank block to block 1 whatever k is.
 cudaError_t launch_decide(void* st, int B, int k, float tau, int mask_id, int* branch_tok,
                           int* valid, cudaStream_t s);
 cudaError_t launch_select(void* st, int B, int nb, int mask_id, const int* branch_tok,
@@ -209,7 +217,8 @@ struct KvStrides {
 cudaError_t launch_commit_kv(const void* st, const bf16* ks, const bf16* vts, bf16* kc,
                              bf16* vtc, int L, int B, int row_elems, const KvStrides& kv,
                              cudaStream_t s);
-cudaError_t launch_finalize(void* st, int B, int mask_id, int* out_tokens, cudaStream_t s);
+cudaError_t launch_finalize(void* st, int B, int mask_id, int* out_tokens, const int* am_next,
+                            const float* mp_next, cudaStream_t s);
 cudaError_t launch_state_reset(void* st, int P, int B, int mask_id, cudaStream_t s);
 
 }  // namespace lopa

@@ -92,21 +92,35 @@ struct lopa_ctx {
   int* out_tokens = nullptr;
   DevState* st = nullptr;
   int Tmax = 0, nbmax = 0, qkv_rows = 0;
-  // K cache [L][max_seq][Hk*dh], K scratch [L][nbmax*B][Hk*dh]; values transposed:
-  // V^T cache [L][Hk*dh][vt_ld], V^T scratch [L][Hk*dh][nbmax*B].
+  int nslots = 0;  // branch rows the block buffers hold: nbmax, at least 2 (a merged pass)
+  // K cache [L][max_seq][Hk*dh], K scratch [L][nslots*B][Hk*dh]; values transposed:
+  // V^T cache [L][Hk*dh][vt_ld], V^T scratch [L][Hk*dh][nslots*B].
   size_t cache_layer = 0, scr_layer = 0, vt_cache_layer = 0;
   int vt_ld = 0;
   // graphs
-  Plan step_plan, start_plan;
-  cudaGraphExec_t step_exec = nullptr, start_exec = nullptr;
+  // step_plans[nb]: verification forward of nb branches (nb = 1..1+k; step_plan is the
+  // full one); merged_plan: [completing branch ; blank next block] with block-causal
+  // attention; start_plan: the block-start forward of a fresh block.
+  std::vector<Plan> step_plans;
+  Plan& step_plan() { return step_plans.back(); }
+  Plan merged_plan, start_plan;
+  std::vector<cudaGraphExec_t> step_execs;
+  cudaGraphExec_t merged_exec = nullptr, start_exec = nullptr;
+  int cur_nb = 0;  // branch count of the graph being captured
   // lopa_time_forward: forward-only graphs (0 block start, 1 verification), built lazily
   Plan time_start_plan;
   const Plan* fwd_plan = nullptr;
   cudaGraphExec_t fwd_exec[2] = {nullptr, nullptr};
   cudaEvent_t ev0 = nullptr, ev1 = nullptr;
   lopa_step_result* h_res = nullptr;  // pinned
+  int* h_next = nullptr;              // pinned: {n_valid, final_w} of the last decide
   // host-side view of the decode
-  bool prefilled = false, block_fresh = true;
+  // block_fresh: the current block has no logits yet (needs its block-start forward);
+  // in_block: it has had at least one iteration; next_nv / next_final: the branches the
+  // last decide built for the coming iteration (valid when !block_fresh).
+  bool prefilled = false, block_fresh = true, in_block = false;
+  int next_nv = 0, next_final = -1;
+  bool allow_merge = true;  // the completing iteration may run the next block's start
   int P = 0, P0 = 0;
   std::string err;
 };
@@ -216,7 +230,7 @@ void qkv_tiling(const lopa_ctx* ctx, int nrows, int K, int T, int* na, int* cs) 
 }
 
 int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm, const int* tok,
-               int* am_out, float* mp_out) {
+               int* am_out, float* mp_out, bool causal = false) {
   const lopa_model_config& m = ctx->mc;
   const int L = m.n_layers, d = m.d_model, H = m.n_heads, dh = m.head_dim, F = m.ffn;
   p.nb = nb;
@@ -268,7 +282,7 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
     bf16* vsl = ctx->vs + (size_t)l * ctx->scr_layer;
     qa.kdst = kv_to_cache ? kcl : ksl;
     qa.vdst = kv_to_cache ? vcl : vsl;
-    qa.ldv = kv_to_cache ? ctx->vt_ld : ctx->nbmax * ctx->dc.block;
+    qa.ldv = kv_to_cache ? ctx->vt_ld : ctx->nslots * ctx->dc.block;
     qa.cos_t = ctx->cos_t;
     qa.sin_t = ctx->sin_t;
     qa.dP = &ctx->st->P;
@@ -277,10 +291,11 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
     qa.dh = dh;
     qa.Bq = Bq;
     qa.kv_to_cache = kv_to_cache;
+    qa.pos_linear = causal ? 1 : 0;
     qa.xws = ctx->xws;
     if (qkv_exchange_floats(p.qkv[l].grid.x, qa.splits, p.qkv[l].grid.z, qa.nbox) > ctx->xws_floats)
       return fail(ctx, LOPA_ERR_UNSUPPORTED, "q/k/v exchange workspace too small");
-    AttnArgs aa;
+    AttnArgs aa = {};
     aa.q = ctx->q;
     aa.out = ctx->attn;
     aa.kc = kcl;
@@ -290,11 +305,12 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
     aa.dP = &ctx->st->P;
     aa.pk_add = kv_to_cache ? p.T : 0;
     aa.ldvc = ctx->vt_ld;
-    aa.ldvb = ctx->nbmax * ctx->dc.block;
+    aa.ldvb = ctx->nslots * ctx->dc.block;
     aa.Bq = Bq;
     aa.Bk = kv_to_cache ? 0 : Bq;
     aa.Bk_stride = Bq;
     aa.nbq = nb;
+    aa.causal = causal ? 1 : 0;
     aa.H = H;
     aa.Hk = m.n_kv_heads;
     aa.err = &ctx->st->err;
@@ -350,25 +366,35 @@ int enqueue_forward(lopa_ctx* ctx, const Plan& p) {
   return 0;
 }
 
-int enqueue_step(lopa_ctx* ctx) {
-  const int B = ctx->dc.block, nb = ctx->nbmax, mask = ctx->mc.mask_id;
+// One LoPA iteration after its decide: the verification forward of plan p (nb branches),
+// select, Commit-Winner, finalize (with next-block logits for the merged plan), then the
+// decide of the coming iteration, whose branch count and completion flag the host reads
+// back with the step result.
+int enqueue_iteration(lopa_ctx* ctx, const Plan& p, int nb_select, bool merged) {
+  const int B = ctx->dc.block, mask = ctx->mc.mask_id;
   cudaStream_t s = ctx->stream;
-  CK(launch_decide(ctx->st, B, ctx->dc.k, ctx->dc.tau, mask, ctx->branch_tok, ctx->valid, s));
-  int r = enqueue_forward(ctx, ctx->step_plan);
+  int r = enqueue_forward(ctx, p);
   if (r) return r;
-  CK(launch_select(ctx->st, B, nb, mask, ctx->branch_tok, ctx->valid, ctx->am_b, ctx->mp_b, s));
+  CK(launch_select(ctx->st, B, nb_select, mask, ctx->branch_tok, ctx->valid, ctx->am_b, ctx->mp_b, s));
   KvStrides kv;
   kv.k_cache = ctx->cache_layer;
   kv.k_scr = ctx->scr_layer;
   kv.v_cache = ctx->vt_cache_layer;
   kv.v_scr = ctx->scr_layer;
   kv.ld_cache = ctx->vt_ld;
-  kv.ld_scr = nb * B;
+  kv.ld_scr = ctx->nslots * B;
   CK(launch_commit_kv(ctx->st, ctx->ks, ctx->vs, ctx->kc, ctx->vc, ctx->mc.n_layers, B,
                       ctx->mc.n_kv_heads * ctx->mc.head_dim, kv, s));
-  CK(launch_finalize(ctx->st, B, mask, ctx->out_tokens, s));
+  CK(launch_finalize(ctx->st, B, mask, ctx->out_tokens, merged ? ctx->am_b + B : nullptr,
+                     merged ? ctx->mp_b + B : nullptr, s));
+  CK(launch_decide(ctx->st, B, ctx->dc.k, ctx->dc.tau, mask, ctx->branch_tok, ctx->valid, s));
   return 0;
 }
+
+int step_fn(lopa_ctx* ctx) {
+  return enqueue_iteration(ctx, ctx->step_plans[ctx->cur_nb], ctx->cur_nb, false);
+}
+int merged_fn(lopa_ctx* ctx) { return enqueue_iteration(ctx, ctx->merged_plan, 1, true); }
 
 int capture(lopa_ctx* ctx, int (*fn)(lopa_ctx*), cudaGraphExec_t* exec) {
   cudaGraph_t g = nullptr;
@@ -387,7 +413,13 @@ int capture(lopa_ctx* ctx, int (*fn)(lopa_ctx*), cudaGraphExec_t* exec) {
   return 0;
 }
 
-int start_fn(lopa_ctx* ctx) { return enqueue_forward(ctx, ctx->start_plan); }
+int start_fn(lopa_ctx* ctx) {
+  int r = enqueue_forward(ctx, ctx->start_plan);
+  if (r) return r;
+  CK(launch_decide(ctx->st, ctx->dc.block, ctx->dc.k, ctx->dc.tau, ctx->mc.mask_id, ctx->branch_tok,
+                   ctx->valid, ctx->stream));
+  return 0;
+}
 
 int check_device_error(lopa_ctx* ctx) {
   int e = 0;
@@ -462,19 +494,20 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
   }
   // buffers
   ctx->nbmax = ctx->dc.k + 1;
-  ctx->Tmax = std::max(ctx->nbmax * B, ctx->dc.max_prompt);
+  ctx->nslots = std::max(ctx->nbmax, 2);
+  ctx->Tmax = std::max(ctx->nslots * B, ctx->dc.max_prompt);
   ctx->qkv_rows = (H + 2 * Hk) * dh;
   ctx->cache_layer = (size_t)m.max_seq * Hk * dh;
   ctx->vt_ld = (m.max_seq + 63) / 64 * 64;
   ctx->vt_cache_layer = (size_t)Hk * dh * ctx->vt_ld;
-  ctx->scr_layer = (size_t)ctx->nbmax * B * Hk * dh;
+  ctx->scr_layer = (size_t)ctx->nslots * B * Hk * dh;
   ctx->nvt = (V + 255) / 256;
-  ctx->part_ld = ctx->nbmax * B;
-  ctx->part_floats = std::max(partial_floats(ctx, ctx->nbmax * B),
+  ctx->part_ld = ctx->nslots * B;
+  ctx->part_floats = std::max(partial_floats(ctx, ctx->nslots * B),
                               std::max(partial_floats(ctx, B), partial_floats(ctx, ctx->dc.max_prompt)));
   const size_t T = ctx->Tmax;
   {
-    // q/k/v exchange workspace: the largest any forward needs (1..nbmax branches of one
+    // q/k/v exchange workspace: the largest any forward needs (1..nslots branch slots of one
     // block, or the prompt).
     auto need = [&](int T2) {
       int na, cs;
@@ -484,7 +517,7 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
       return qkv_exchange_floats(gx, cs, (T2 + nbox - 1) / nbox, nbox);
     };
     ctx->xws_floats = need(ctx->dc.max_prompt);
-    for (int nb = 1; nb <= ctx->nbmax; ++nb) ctx->xws_floats = std::max(ctx->xws_floats, need(nb * B));
+    for (int nb = 1; nb <= ctx->nslots; ++nb) ctx->xws_floats = std::max(ctx->xws_floats, need(nb * B));
   }
   int r;
   if ((r = dalloc(ctx, &ctx->kc, ctx->cache_layer * L)) || (r = dalloc(ctx, &ctx->vc, ctx->vt_cache_layer * L)) ||
@@ -498,10 +531,10 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
       (r = dalloc(ctx, &ctx->pi, (size_t)ctx->nvt * ctx->part_ld)) ||
       (r = dalloc(ctx, &ctx->cos_t, (size_t)m.max_seq * dh / 2)) ||
       (r = dalloc(ctx, &ctx->sin_t, (size_t)m.max_seq * dh / 2)) ||
-      (r = dalloc(ctx, &ctx->branch_tok, (size_t)ctx->nbmax * B)) ||
+      (r = dalloc(ctx, &ctx->branch_tok, (size_t)ctx->nslots * B)) ||
       (r = dalloc(ctx, &ctx->valid, (size_t)LOPA_MAX_BRANCHES)) ||
-      (r = dalloc(ctx, &ctx->am_b, (size_t)ctx->nbmax * B)) ||
-      (r = dalloc(ctx, &ctx->mp_b, (size_t)ctx->nbmax * B)) ||
+      (r = dalloc(ctx, &ctx->am_b, (size_t)ctx->nslots * B)) ||
+      (r = dalloc(ctx, &ctx->mp_b, (size_t)ctx->nslots * B)) ||
       (r = dalloc(ctx, &ctx->tok_rows, T)) || (r = dalloc(ctx, &ctx->out_tokens, (size_t)m.max_seq)) ||
       (r = dalloc(ctx, &ctx->st, 1)))
     return r;
@@ -533,13 +566,24 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
   CK(cudaEventCreate(&ctx->ev0));
   CK(cudaEventCreate(&ctx->ev1));
   CK(cudaMallocHost(&ctx->h_res, sizeof(lopa_step_result)));
+  CK(cudaMallocHost(&ctx->h_next, 2 * sizeof(int)));
   // plans and graphs
-  if ((r = build_plan(ctx, ctx->step_plan, ctx->nbmax, B, 0, true, ctx->branch_tok, ctx->am_b, ctx->mp_b)))
+  ctx->step_plans.resize(ctx->nbmax + 1);
+  for (int nb = 1; nb <= ctx->nbmax; ++nb)
+    if ((r = build_plan(ctx, ctx->step_plans[nb], nb, B, 0, true, ctx->branch_tok, ctx->am_b, ctx->mp_b)))
+      return r;
+  if ((r = build_plan(ctx, ctx->merged_plan, 2, B, 0, true, ctx->branch_tok, ctx->am_b, ctx->mp_b,
+                      /*causal=*/true)))
     return r;
   if ((r = build_plan(ctx, ctx->start_plan, 1, B, 0, true, ctx->st->tok, ctx->st->am, ctx->st->mp)))
     return r;
   CK(cudaStreamSynchronize(s));
-  if ((r = capture(ctx, enqueue_step, &ctx->step_exec))) return r;
+  ctx->step_execs.assign(ctx->nbmax + 1, nullptr);
+  for (int nb = 1; nb <= ctx->nbmax; ++nb) {
+    ctx->cur_nb = nb;
+    if ((r = capture(ctx, step_fn, &ctx->step_execs[nb]))) return r;
+  }
+  if ((r = capture(ctx, merged_fn, &ctx->merged_exec))) return r;
   if ((r = capture(ctx, start_fn, &ctx->start_exec))) return r;
   return 0;
 }
@@ -547,39 +591,72 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
 void destroy(lopa_ctx* ctx) {
   if (!ctx) return;
   if (ctx->stream) cudaStreamSynchronize(ctx->stream);
-  if (ctx->step_exec) cudaGraphExecDestroy(ctx->step_exec);
+  for (auto e : ctx->step_execs)
+    if (e) cudaGraphExecDestroy(e);
+  if (ctx->merged_exec) cudaGraphExecDestroy(ctx->merged_exec);
   for (auto e : ctx->fwd_exec)
     if (e) cudaGraphExecDestroy(e);
   if (ctx->start_exec) cudaGraphExecDestroy(ctx->start_exec);
   if (ctx->ev0) cudaEventDestroy(ctx->ev0);
   if (ctx->ev1) cudaEventDestroy(ctx->ev1);
   if (ctx->h_res) cudaFreeHost(ctx->h_res);
+  if (ctx->h_next) cudaFreeHost(ctx->h_next);
   for (void* p : ctx->allocs) cudaFree(p);
   if (ctx->own_stream) cudaStreamDestroy(ctx->stream);
   delete ctx;
 }
 
-// Runs one iteration (plus the block-start forward when the block is fresh).
-int step_impl(lopa_ctx* ctx, lopa_step_result* out) {
-  if (!ctx->prefilled) return fail(ctx, LOPA_ERR_BAD_STATE, "lopa_step before lopa_prefill");
-  int fwd = 0;
-  if (ctx->block_fresh) {
-    if (ctx->P + ctx->dc.block > ctx->mc.max_seq)
-      return fail(ctx, LOPA_ERR_BAD_STATE, "KV cache full: next block would end at %d > max_seq %d",
-                  ctx->P + ctx->dc.block, ctx->mc.max_seq);
-    CK(cudaGraphLaunch(ctx->start_exec, ctx->stream));
-    fwd = 1;
-  }
-  CK(cudaGraphLaunch(ctx->step_exec, ctx->stream));
-  CK(cudaMemcpyAsync(ctx->h_res, &ctx->st->res, sizeof(lopa_step_result), cudaMemcpyDeviceToHost,
+// Reads back the branch count and completion flag of the last decide (synchronises).
+int read_next(lopa_ctx* ctx) {
+  static_assert(offsetof(DevState, final_w) == offsetof(DevState, n_valid) + sizeof(int),
+                "n_valid and final_w are adjacent");
+  CK(cudaMemcpyAsync(ctx->h_next, &ctx->st->n_valid, 2 * sizeof(int), cudaMemcpyDeviceToHost,
                      ctx->stream));
   CK(cudaStreamSynchronize(ctx->stream));
-  lopa_step_result& r = *ctx->h_res;
-  r.forwards = 1 + fwd;
-  if (r.device_error) return fail(ctx, LOPA_ERR_DEVICE_TIMEOUT, "device-side wait gave up (code %d)", r.device_error);
-  ctx->block_fresh = r.block_done != 0;
-  if (r.block_done) ctx->P += ctx->dc.block;
-  if (out) *out = r;
+  ctx->next_nv = ctx->h_next[0];
+  ctx->next_final = ctx->h_next[1];
+  if (ctx->next_nv < 1 || ctx->next_nv > ctx->nbmax || ctx->next_final < -1 || ctx->next_final > 1)
+    return fail(ctx, LOPA_ERR_BAD_STATE, "decide produced %d branches (final %d)", ctx->next_nv,
+                ctx->next_final);
+  return 0;
+}
+
+// Runs one iteration (plus the block-start forward when the block has no logits yet).
+// The branches were built by the decide at the end of the previous graph; the host picks
+// the forward that evaluates them: only the valid branches (nb = 1 + lookaheads); or, when
+// the iteration completes the block, only the completing branch - together with the next
+// block's block-start rows (block-causal attention) when a next block fits.
+int step_impl(lopa_ctx* ctx, lopa_step_result* out) {
+  if (!ctx->prefilled) return fail(ctx, LOPA_ERR_BAD_STATE, "lopa_step before lopa_prefill");
+  const int B = ctx->dc.block;
+  if (ctx->P + B > ctx->mc.max_seq)
+    return fail(ctx, LOPA_ERR_BAD_STATE, "KV cache full: next block would end at %d > max_seq %d",
+                ctx->P + B, ctx->mc.max_seq);
+  int fwd = 0, r;
+  if (ctx->block_fresh) {
+    CK(cudaGraphLaunch(ctx->start_exec, ctx->stream));  // block-start forward + decide
+    if ((r = read_next(ctx))) return r;
+    fwd = 1;
+  }
+  const bool merge = ctx->next_final >= 0 && ctx->allow_merge && ctx->P + 2 * B <= ctx->mc.max_seq;
+  cudaGraphExec_t g = merge ? ctx->merged_exec
+                            : ctx->step_execs[ctx->next_final >= 0 ? 1 : ctx->next_nv];
+  CK(cudaGraphLaunch(g, ctx->stream));
+  CK(cudaMemcpyAsync(ctx->h_res, &ctx->st->res, sizeof(lopa_step_result), cudaMemcpyDeviceToHost,
+                     ctx->stream));
+  if ((r = read_next(ctx))) return r;
+  lopa_step_result& res = *ctx->h_res;
+  res.forwards = 1 + fwd;
+  if (res.device_error)
+    return fail(ctx, LOPA_ERR_DEVICE_TIMEOUT, "device-side wait gave up (code %d)", res.device_error);
+  ctx->in_block = res.block_done == 0;
+  if (res.block_done) {
+    ctx->P += B;
+    ctx->block_fresh = !merge;  // a merged iteration leaves the next block's logits ready
+  } else {
+    ctx->block_fresh = false;
+  }
+  if (out) *out = res;
   return 0;
 }
 
@@ -634,6 +711,7 @@ int lopa_prefill(lopa_ctx* ctx, const int32_t* prompt, int n) {
   if ((r = check_device_error(ctx))) return r;
   ctx->prefilled = true;
   ctx->block_fresh = true;
+  ctx->in_block = false;
   ctx->P = ctx->P0 = n;
   return 0;
 }
@@ -648,7 +726,7 @@ int lopa_decode(lopa_ctx* ctx, int gen_len, int32_t* out_tokens, lopa_stats* out
   if (!ctx->prefilled) return fail(ctx, LOPA_ERR_BAD_STATE, "lopa_decode before lopa_prefill");
   const int B = ctx->dc.block;
   if (gen_len < 0 || gen_len % B) return fail(ctx, LOPA_ERR_INVALID_ARG, "gen_len must be a multiple of %d", B);
-  if (!ctx->block_fresh) return fail(ctx, LOPA_ERR_BAD_STATE, "a block is in progress; finish it with lopa_step");
+  if (ctx->in_block) return fail(ctx, LOPA_ERR_BAD_STATE, "a block is in progress; finish it with lopa_step");
   if (ctx->P + gen_len > ctx->mc.max_seq)
     return fail(ctx, LOPA_ERR_BAD_STATE, "decode would end at %d > max_seq %d", ctx->P + gen_len, ctx->mc.max_seq);
   const int start = ctx->P - ctx->P0;
@@ -656,16 +734,23 @@ int lopa_decode(lopa_ctx* ctx, int gen_len, int32_t* out_tokens, lopa_stats* out
   CK(cudaEventRecord(ctx->ev0, ctx->stream));
   for (int b = 0; b < gen_len / B; ++b) {
     int iters = 0;
+    // The last block of this decode does not start the block after it.
+    ctx->allow_merge = b + 1 < gen_len / B;
     while (true) {
       lopa_step_result r;
       int rc = step_impl(ctx, &r);
+      ctx->allow_merge = true;
       if (rc) return rc;
+      ctx->allow_merge = b + 1 < gen_len / B;
       st.forwards += r.forwards;
       st.steps += 1;
       if (r.block_done) break;
-      if (++iters > B)
+      if (++iters > B) {
+        ctx->allow_merge = true;
         return fail(ctx, LOPA_ERR_BAD_STATE, "block did not finish within %d iterations", B);
+      }
     }
+    ctx->allow_merge = true;
     st.blocks += 1;
     st.tokens += B;
   }
@@ -697,13 +782,14 @@ int lopa_rewind(lopa_ctx* ctx, int pos) {
   CK(cudaStreamSynchronize(ctx->stream));
   ctx->P = pos;
   ctx->block_fresh = true;
+  ctx->in_block = false;
   return 0;
 }
 
 int lopa_time_gemm(lopa_ctx* ctx, int kind, int iters, float* avg_ms) {
   if (!ctx) return fail(nullptr, LOPA_ERR_INVALID_ARG, "ctx is null");
   if (kind < 0 || kind > 4 || iters < 1 || !avg_ms) return fail(ctx, LOPA_ERR_INVALID_ARG, "bad kind/iters");
-  const Plan& p = ctx->step_plan;
+  const Plan& p = ctx->step_plan();
   const int L = ctx->mc.n_layers;
   cudaStream_t s = ctx->stream;
   // The launches are captured into a graph (as in the decoding step), so host launch
@@ -752,7 +838,7 @@ int lopa_time_forward(lopa_ctx* ctx, int kind, int iters, float* median_ms, floa
   if (!ctx->fwd_exec[kind]) {
     // Forward-only graphs.  The block-start one writes its logit summary to the branch
     // buffers (not the block state), so neither changes the decoding state.
-    Plan& p = kind == 1 ? ctx->step_plan : ctx->time_start_plan;
+    Plan& p = kind == 1 ? ctx->step_plan() : ctx->time_start_plan;
     int r;
     if (kind == 0 && (r = build_plan(ctx, p, 1, ctx->dc.block, 0, true, ctx->st->tok, ctx->am_b,
                                      ctx->mp_b)))
@@ -815,8 +901,11 @@ int lopa_set_block_state(lopa_ctx* ctx, const int32_t* tok, const int32_t* am, c
   CK(cudaMemcpyAsync(ctx->st->tok, tok, sizeof(int) * B, cudaMemcpyHostToDevice, s));
   CK(cudaMemcpyAsync(ctx->st->am, am, sizeof(int) * B, cudaMemcpyHostToDevice, s));
   CK(cudaMemcpyAsync(ctx->st->mp, mp, sizeof(float) * B, cudaMemcpyHostToDevice, s));
-  CK(cudaStreamSynchronize(s));
+  CK(launch_decide(ctx->st, B, ctx->dc.k, ctx->dc.tau, ctx->mc.mask_id, ctx->branch_tok, ctx->valid, s));
+  int r = read_next(ctx);
+  if (r) return r;
   ctx->block_fresh = false;
+  ctx->in_block = true;
   return 0;
 }
 
@@ -876,7 +965,7 @@ int lopa_read_branch_kv(lopa_ctx* ctx, int layer, int branch, uint16_t* k, uint1
   std::vector<uint16_t> vt(v ? row * B : 0);
   if (v)
     CK(cudaMemcpy2DAsync(vt.data(), (size_t)B * 2, ctx->vs + off + (size_t)branch * B,
-                         (size_t)ctx->nbmax * B * 2, (size_t)B * 2, row, cudaMemcpyDeviceToHost, s));
+                         (size_t)ctx->nslots * B * 2, (size_t)B * 2, row, cudaMemcpyDeviceToHost, s));
   CK(cudaStreamSynchronize(s));
   if (v)
     for (size_t r = 0; r < row; ++r)
@@ -962,7 +1051,7 @@ int lopa_branch_attention(const void* q, const void* k_prefix, const void* vt_pr
     return fail(ctx, LOPA_ERR_INVALID_ARG, "bad shape");
   if (head_dim != 32 && head_dim != 64 && head_dim != 128)
     return fail(ctx, LOPA_ERR_UNSUPPORTED, "head_dim must be 32, 64 or 128");
-  AttnArgs a;
+  AttnArgs a = {};
   a.q = static_cast<const bf16*>(q);
   a.out = static_cast<bf16*>(out);
   a.kc = static_cast<const bf16*>(k_prefix);

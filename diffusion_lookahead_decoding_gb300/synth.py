@@ -78,12 +78,17 @@ DREAM7B = (ModelShape(28, 3584, 28, 4, 128, 18944, 152064, 1e6),
            DecodeShape(block=32, k=7, tau=0.9, prompt_len=512, gen_len=256))
 DREAM7B_SCALING = (DREAM7B[0], DecodeShape(block=32, k=7, tau=0.9, prompt_len=2048, gen_len=512))
 
+# Dream-7B's head geometry (head_dim 128, 7 query heads per KV head) in a 2-layer model the
+# oracle decodes in seconds: the decode-level parity case of the tensor-core attention.
+HEADS128 = (ModelShape(2, 896, 7, 1, 128, 2048, 8192, 1e6),
+            DecodeShape(block=32, k=7, tau=0.9, prompt_len=96, gen_len=128))
+
 # One layer with the Dream-7B layer and vocabulary sizes: a few GB on the device, used to
 # profile single kernels in isolation.
 DREAM7B_LAYER = (ModelShape(1, 3584, 28, 4, 128, 18944, 152064, 1e6), DREAM7B[1])
 
-WORKLOADS = {"tiny": TINY, "small": SMALL, "dream7b": DREAM7B, "dream7b_scaling": DREAM7B_SCALING,
-             "dream7b_layer": DREAM7B_LAYER}
+WORKLOADS = {"tiny": TINY, "small": SMALL, "heads128": HEADS128, "dream7b": DREAM7B,
+             "dream7b_scaling": DREAM7B_SCALING, "dream7b_layer": DREAM7B_LAYER}
 
 LAYER_TENSORS = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
 

@@ -97,14 +97,17 @@ typedef struct {
   int forwards;          /* forward passes run by this call (1, or 2 when a block-start forward ran) */
   int prefix_len;        /* committed prefix length P when the iteration ran */
   int device_error;      /* 0, or a device-side error code */
-  float conf[LOPA_MAX_BRANCHES]; /* branch confidences; -inf for padded (invalid) branches */
+  float conf[LOPA_MAX_BRANCHES]; /* branch confidences; -inf for invalid branches, and for
+                                    every branch but the winner in a completing iteration */
   int filled_pos[LOPA_MAX_BLOCK]; /* first n_filled entries: positions in the block, ascending */
   int filled_tok[LOPA_MAX_BLOCK]; /* tokens written at those positions */
 } lopa_step_result;
 
 typedef struct {
   long long tokens;   /* generated tokens */
-  long long forwards; /* forward passes (block-start + one per iteration; prefill excluded) */
+  long long forwards; /* forward passes: one per iteration, plus the first block's start
+                         forward (later blocks start inside the completing iteration's
+                         pass); prefill excluded */
   long long steps;    /* LoPA iterations */
   long long blocks;   /* completed blocks */
   double seconds;     /* device time of the decode (CUDA events), prefill excluded */
@@ -126,13 +129,19 @@ int lopa_prefill(lopa_ctx* ctx, const int32_t* prompt, int n);
 
 /* One LoPA iteration on the current block (running the block-start forward first when
  * the block is fresh): anchor fill, lookahead branches, one isolated verification
- * forward over all branches, confidences, winner, Commit-Winner of the winner's K/V,
- * logit reuse.  out (host, may be NULL) receives the outcome.  Synchronizes.
- * BAD_STATE before prefill or when the next block would exceed max_seq. */
+ * forward over the valid branches, confidences, winner, Commit-Winner of the winner's
+ * K/V, logit reuse.  An iteration that completes the block (nothing masked after the
+ * anchor fill, or one position that lookahead branch 1 fills) has its winner fixed before
+ * the forward (confidence 1.0, lowest index): only that branch is evaluated, and when the
+ * next block fits in max_seq its all-[MASK] start rows run in the same pass
+ * (block-causal attention), so the next block starts with its logits in place.  out
+ * (host, may be NULL) receives the outcome.  Synchronizes.  BAD_STATE before prefill or
+ * when the next block would exceed max_seq. */
 int lopa_step(lopa_ctx* ctx, lopa_step_result* out);
 
 /* Decodes gen_len tokens (a multiple of the block length) from a block boundary:
- * for each block, the block-start forward then iterations until no [MASK] is left.
+ * for each block, the block-start forward then iterations until no [MASK] is left (the
+ * last block of the call does not start the block after it).
  * out_tokens: host int32[gen_len] (may be NULL); out: host stats (may be NULL). */
 int lopa_decode(lopa_ctx* ctx, int gen_len, int32_t* out_tokens, lopa_stats* out);
 

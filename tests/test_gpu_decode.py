@@ -16,7 +16,7 @@ from tests.gpu_util import (f32, make_decoder, oracle_forward_pair, rel_l2, seed
                             tokens_ok, workload_weights)
 
 pytestmark = pytest.mark.gpu
-WORKLOADS = ["tiny", "small"]
+WORKLOADS = ["tiny", "small", "heads128"]
 _COND = {}
 
 
@@ -55,16 +55,30 @@ def _cond(name, shape, w, prompt, B, P):
 
 @pytest.mark.parametrize("name", WORKLOADS)
 def test_branches_are_isolated_on_gpu(name):
-    """Each branch's outputs in the batched pass equal a separate single-branch pass."""
+    """Each branch's outputs in the batched pass equal a separate single-branch pass.  The
+    mma.sync attention (head_dim 32/64) gives the same bits; the tensor-core attention
+    may sum a row's keys in another order inside the MMA when its query tile holds rows of
+    two branches, so there the bound is the oracle's own summation-order sensitivity (a
+    leak between branches would move the outputs by far more)."""
     shape, dshape, w, dec, prompt = _setup(name)
     B, nb = dshape.block, dshape.k + 1
     br = seeded_branches(shape, nb, B, seed=6)
     am, mp, hid = dec.verify_forward(br, want_hidden=True)
+    if shape.head_dim == 128:
+        _, _, out, cond = oracle_forward_pair(shape, w, prompt, br, dshape.prompt_len + B)
+        h_tol, p_tol = 2.0 * cond.hidden, 2.0 * cond.mp
+        print(f"{name}: isolation bounds hidden {h_tol:.1e}, maxp {p_tol:.1e}")
     for b in range(nb):
         am1, mp1, hid1 = dec.verify_forward(br[b:b + 1], want_hidden=True)
-        assert rel_l2(hid1[0], hid[b]) < 1e-5
-        assert np.abs(mp1[0] - mp[b]).max() < 1e-5
-        np.testing.assert_array_equal(am1[0], am[b])
+        if shape.head_dim != 128:
+            assert rel_l2(hid1[0], hid[b]) < 1e-5
+            assert np.abs(mp1[0] - mp[b]).max() < 1e-5
+            np.testing.assert_array_equal(am1[0], am[b])
+            continue
+        assert rel_l2(hid1[0], hid[b]) < h_tol
+        assert np.abs(mp1[0] - mp[b]).max() < p_tol
+        flip = (am1[0] != am[b]) & ((out.mp[b] - out.p2[b]) >= cond.tie)
+        assert not flip.any(), np.nonzero(flip)
 
 
 @pytest.mark.parametrize("name", WORKLOADS)
@@ -88,7 +102,12 @@ def test_iteration_from_seeded_states(name):
         st = O.lopa_step(m, cache, P, tok, am, f32(mp), k, float(np.float32(tau)))
         assert res.n_valid_branches == len(st.branches)
         conf_o = np.array(st.conf)
-        assert np.abs(res.conf[:len(conf_o)] - conf_o).max() <= cond.mp_bound
+        # A completing iteration evaluates only its winner (confidence 1.0); the other
+        # branches are reported as -inf.
+        seen = np.isfinite(res.conf[:len(conf_o)])
+        if not seen.all():
+            assert res.block_done and seen.sum() == 1 and res.conf[res.winner] == 1.0
+        assert np.abs(res.conf[:len(conf_o)][seen] - conf_o[seen]).max() <= cond.mp_bound
         assert np.isneginf(res.conf[len(conf_o):k + 1]).all()
         wg = res.winner
         if wg != st.winner:
@@ -112,7 +131,8 @@ def _first_divergence(a, b):
     return int(d[0]) if len(d) else None
 
 
-@pytest.mark.parametrize("name,k", [("tiny", None), ("small", None), ("tiny", 0), ("small", 0)])
+@pytest.mark.parametrize("name,k", [("tiny", None), ("small", None), ("heads128", None),
+                                    ("tiny", 0), ("small", 0)])
 def test_decode_trajectory_matches_oracle(name, k):
     """Whole decode on the GPU vs the oracle's decode from the same seeded prompt.
     Identical, or else the oracle met a near-tie in the block where they first
@@ -124,19 +144,81 @@ def test_decode_trajectory_matches_oracle(name, k):
     m = O.OracleModel(shape, w, act="bf16")
     otoks, ofw, _, log = O.decode(m, prompt, dshape.block, kk, dshape.tau, dshape.gen_len,
                                   record=True)
+    # The GPU runs each block's block-start forward inside the previous block's
+    # completing iteration (one pass), so it counts one forward less per block boundary.
+    nblk = dshape.gen_len // dshape.block
     print(f"{name} k={kk}: GPU TPF {stats['tokens'] / stats['forwards']:.2f} "
-          f"({stats['forwards']} fwd), oracle TPF {len(otoks) / ofw:.2f} ({ofw} fwd)")
-    assert stats["tokens"] == dshape.gen_len and stats["blocks"] == dshape.gen_len // dshape.block
+          f"({stats['forwards']} fwd), oracle TPF {len(otoks) / ofw:.2f} ({ofw} fwd, "
+          f"{ofw - (nblk - 1)} with merged block starts)")
+    assert stats["tokens"] == dshape.gen_len and stats["blocks"] == nblk
     assert (toks != shape.mask_id).all()
     div = _first_divergence(toks, otoks)
     if div is None:
-        assert stats["forwards"] == ofw
+        assert stats["forwards"] == ofw - (nblk - 1)
         return
     blk_start = dshape.prompt_len + (div // dshape.block) * dshape.block
     margins = [min(st.margins.values()) for (P, st) in log if P <= blk_start]
     print(f"diverged at token {div}; smallest oracle margin up to that block {min(margins):.2e} "
           f"(tie window {cond.tie:.1e})")
     assert min(margins) < cond.tie, "diverged without an oracle near-tie"
+
+
+def completing_state(shape, B, tau, seed, via):
+    """A block state whose next iteration completes the block: via the anchor fill (every
+    masked position reaches tau) or via lookahead branch 1 (one masked position stays
+    below tau after the anchor fill and is the branch's candidate)."""
+    tok, am, mp = synth.make_block_state(shape, B, seed=seed, masked_frac=0.0)
+    rng = np.random.default_rng(seed + 1)
+    masked = np.nonzero(tok == shape.mask_id)[0]
+    mp[masked] = np.float32(0.5 * (1.0 + tau))
+    if via == "lookahead":
+        free = np.setdiff1d(np.arange(B), masked)
+        j = int(rng.choice(free))
+        tok[j] = shape.mask_id
+        mp[j] = np.float32(0.5 * tau)
+    winner = tok.copy()
+    winner[tok == shape.mask_id] = am[tok == shape.mask_id]
+    return tok, am, mp, winner
+
+
+@pytest.mark.parametrize("via", ["anchor", "lookahead"])
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_completing_iteration_starts_the_next_block(name, via):
+    """An iteration that completes the block evaluates only its (already known) winner and,
+    in the same pass, the next block's all-[MASK] start rows.  Against the oracle's
+    unmerged order - the finished block's forward, its commit, then the block-start forward
+    of the next block: the reported winner and tokens are exact, the next block's first
+    (argmax, maxp) summary is within the forward's bounds, and a separate block-start
+    forward on the GPU agrees with it as well."""
+    shape, dshape, w, dec, prompt = _setup(name)
+    B, tau, P, mask = dshape.block, dshape.tau, dshape.prompt_len, shape.mask_id
+    cond = _cond(name, shape, w, prompt, B, P)
+    tok, am, mp, winner = completing_state(shape, B, tau, seed=11, via=via)
+    dec.set_block_state(tok, am, mp)
+    res = dec.step()
+    w_expect = 0 if via == "anchor" else 1
+    assert res.block_done and res.winner == w_expect and res.forwards == 1
+    assert res.conf[w_expect] == 1.0 and np.isneginf(np.delete(res.conf, w_expect)).all()
+    tok2, am2, mp2, P2 = dec.get_block_state()
+    assert P2 == P + B and (tok2 == mask).all()
+
+    m = O.OracleModel(shape, w, act="bf16")
+    cache = O.prefill(m, prompt, P + 2 * B)
+    out1 = O.forward(m, cache, P, winner[None, :])
+    for l in range(shape.n_layers):
+        cache.k[l][P:P + B] = out1.block_k[l][0]
+        cache.v[l][P:P + B] = out1.block_v[l][0]
+    out2 = O.forward(m, cache, P + B, np.full((1, B), mask))
+    e_mp = float(np.abs(mp2 - out2.mp[0]).max())
+    ok, nbad = tokens_ok(am2[None], out2, cond.tie)
+    am_s, mp_s, _ = dec.verify_forward(np.full((1, B), mask, np.int32))
+    e_sep = float(np.abs(mp_s[0] - mp2).max())
+    print(f"{name}/{via}: next-block maxp vs oracle {e_mp:.2e} (bound {cond.mp_bound:.1e}), "
+          f"vs a separate block-start forward {e_sep:.2e}; flips beyond ties {nbad}")
+    assert e_mp <= cond.mp_bound and ok
+    assert e_sep <= cond.mp_bound
+    ok_s, _ = tokens_ok(am_s, out2, cond.tie)
+    assert ok_s
 
 
 @pytest.mark.parametrize("name", WORKLOADS)

@@ -56,4 +56,7 @@ def test_dream7b_verification_sampled_parity():
     for j, b in enumerate(pick):
         conf_o = O.branch_confidence(sb[b], o2.mp[j], mask)
         print(f"branch {b}: conf GPU {res.conf[b]:.4f} oracle {conf_o:.4f}")
+        if not np.isfinite(res.conf[b]):  # a completing iteration evaluates only its winner
+            assert res.block_done and b != res.winner
+            continue
         assert abs(res.conf[b] - conf_o) <= cond.mp_bound
