@@ -77,36 +77,69 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction (three-input max of sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
 // ================================================================ tcgen05 path (dh = 128)
 constexpr int kTcRows = 128;
-constexpr int kTcStages = 3;
+constexpr int kTcStages = 6;     // K / V^T ring depth
+constexpr int kTcSBufs = 3;      // S / P buffers in TMEM
 constexpr int kTcSoftWarps = 8;  // two per TMEM lane quarter, each on half the columns
 constexpr int kTcThreads = (2 + kTcSoftWarps) * 32;  // warp 0 TMA, warp 1 MMA, softmax
-constexpr uint32_t kTcQBytes = 128 * 128 * 2;   // two 64-column SW128 atoms of 16 KB
-constexpr uint32_t kTcKBytes = 64 * 128 * 2;    // two atoms of 8 KB
+constexpr uint32_t kTcKBytes = 64 * 128 * 2;    // K tile: 64 keys x 128 (two SW128 atoms)
 constexpr uint32_t kTcVBytes = 128 * 64 * 2;    // V^T tile: 128 rows (dh) x 64 keys
-constexpr uint32_t kTcPBytes = 128 * 64 * 2;    // one P half (head or tail)
 constexpr uint32_t kTcStageBytes = kTcKBytes + kTcVBytes;
-constexpr uint32_t kTcOffKV = kTcQBytes;
-constexpr uint32_t kTcOffP = kTcOffKV + kTcStages * kTcStageBytes;
-constexpr uint32_t kTcOffTail = kTcOffP + 2 * 2 * kTcPBytes;
+constexpr uint32_t kTcOffTail = kTcStages * kTcStageBytes;
+// TMEM columns: Q (bf16, two per column) [0, 64); S / P buffer b at 64 + 64 b (S as 64
+// fp32 columns, overwritten in place by P: bf16 head in the first 32 columns, tail in the
+// next 32); O (fp32) [256, 384).
+constexpr uint32_t kTmQ = 0, kTmS = 64, kTmO = 256, kTmCols = 512;
 constexpr float kLazyRescale = 8.0f;  // log2 units
 
 struct TcTail {
   uint64_t qfull;
   uint64_t kvfull[kTcStages], kvempty[kTcStages];
-  uint64_t sfull[2], sempty[2], pfull[2], pempty[2];
+  uint64_t sfull[kTcSBufs], pfull[kTcSBufs], pempty[kTcSBufs];
   uint64_t odone;
-  float xmax[2][2][kTcRows];  // [tile parity][column half][row]: half-row maxima
-  float xsum[2][kTcRows];     // [column half][row]: half-row sums of P
+  float xmax[kTcSBufs][2][kTcRows];  // [buffer][column half][row]: half-row maxima
+  float xsum[2][kTcRows];            // [column half][row]: half-row sums of P
   uint32_t tmem;
   int abort;
 };
 constexpr size_t kTcSmem = 1024 + kTcOffTail + sizeof(TcTail);
 
+// The q map is not read by the kernel (the softmax warps load Q rows into TMEM); it is
+// the valid stand-in address of the maps a launch does not use.
 struct TcMaps {
   CUtensorMap q, kc, vtc, kb, vtb;
 };
+
+// Stores 16 32-bit words into consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T: A's 128 rows are the TMEM lanes, its K bf16
+// values two per 32-bit column (element 2c in the low half of column c).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ TcMaps m, const AttnArgs a) {
@@ -124,28 +157,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int b_hi = (min(R0 + kTcRows, rows) - 1) / G / a.Bq;
 
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&tail->qfull), 1);
+    mbar_init(smem_u32(&tail->qfull), kTcSoftWarps * 32);
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(smem_u32(&tail->kvfull[s]), 1);
       mbar_init(smem_u32(&tail->kvempty[s]), 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kTcSBufs; ++s) {
       mbar_init(smem_u32(&tail->sfull[s]), 1);
-      mbar_init(smem_u32(&tail->sempty[s]), kTcSoftWarps * 32);
       mbar_init(smem_u32(&tail->pfull[s]), kTcSoftWarps * 32);
       mbar_init(smem_u32(&tail->pempty[s]), 1);
     }
     mbar_init(smem_u32(&tail->odone), 1);
     tail->abort = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&m.q);
     tma_prefetch_desc(&m.kc);
     tma_prefetch_desc(&m.vtc);
     tma_prefetch_desc(&m.kb);
     tma_prefetch_desc(&m.vtb);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&tail->tmem), 256);  // S0 [0,64), S1 [64,128), O [128,256)
+    tmem_alloc(smem_u32(&tail->tmem), kTmCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -160,12 +191,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      const uint64_t keep = policy_evict_last(), once = policy_evict_first();
-      const uint32_t qf = smem_u32(&tail->qfull);
-      mbar_arrive_expect_tx(qf, kTcQBytes);
-      const int qy = g * rows + R0;
-      tma_load_2d(smem_u32(smem), &m.q, qf, 0, qy, once);
-      tma_load_2d(smem_u32(smem + kTcQBytes / 2), &m.q, qf, 64, qy, once);
+      const uint64_t keep = policy_evict_last();
       for (int j = 0; j < n; ++j) {
         const int s = j % kTcStages;
         if (j >= kTcStages &&
@@ -173,7 +199,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                abort, a.err, DEV_TIMEOUT_PRODUCER))
           break;
         const uint32_t fb = smem_u32(&tail->kvfull[s]);
-        const uint32_t kdst = smem_u32(smem + kTcOffKV + s * kTcStageBytes);
+        const uint32_t kdst = smem_u32(smem + s * kTcStageBytes);
         const uint32_t vdst = kdst + kTcKBytes;
         mbar_arrive_expect_tx(fb, kTcStageBytes);
         if (j < ks.n_pre) {
@@ -191,53 +217,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      // S_j = Q K_j^T runs two tiles ahead of O += P_i V_i: S_j goes into buffer j % 3
+      // once P_{j-3} V has been read from it.
       const uint32_t idesc_s = idesc_bf16(128, kKeyTile);
       const uint32_t idesc_o = idesc_bf16(128, 128);
       bool ok = mbar_wait_bounded(smem_u32(&tail->qfull), 0, abort, a.err, DEV_TIMEOUT_MMA);
-      const uint32_t qs = smem_u32(smem);
-      for (int j = 0; ok && j <= n; ++j) {
-        if (j < n) {  // S_j = Q K_j^T
-          const int s = j % kTcStages, sb = j & 1;
-          if (!mbar_wait_bounded(smem_u32(&tail->kvfull[s]), (uint32_t)(j / kTcStages) & 1u, abort,
-                                 a.err, DEV_TIMEOUT_MMA) ||
-              (j >= 2 && !mbar_wait_bounded(smem_u32(&tail->sempty[sb]),
-                                            (uint32_t)((j >> 1) - 1) & 1u, abort, a.err,
-                                            DEV_TIMEOUT_MMA))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t kbase = smem_u32(smem + kTcOffKV + s * kTcStageBytes);
+      auto issue_s = [&](int j) {
+        const int s = j % kTcStages, sb = j % kTcSBufs;
+        ok = ok && mbar_wait_bounded(smem_u32(&tail->kvfull[s]), (uint32_t)(j / kTcStages) & 1u,
+                                     abort, a.err, DEV_TIMEOUT_MMA);
+        ok = ok && (j < kTcSBufs ||
+                    mbar_wait_bounded(smem_u32(&tail->pempty[sb]), (uint32_t)(j / kTcSBufs - 1) & 1u,
+                                      abort, a.err, DEV_TIMEOUT_MMA));
+        if (!ok) return;
+        tc_fence_after();
+        const uint32_t kbase = smem_u32(smem + s * kTcStageBytes);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = sw128_desc(qs + (kk >> 2) * (kTcQBytes / 2)) + 2 * (kk & 3);
-            const uint64_t bd = sw128_desc(kbase + (kk >> 2) * (kTcKBytes / 2)) + 2 * (kk & 3);
-            mma_bf16(tmem + (uint32_t)(sb * kKeyTile), ad, bd, idesc_s, kk > 0);
-          }
-          mma_commit(smem_u32(&tail->sfull[sb]));
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bd = sw128_desc(kbase + (kk >> 2) * (kTcKBytes / 2)) + 2 * (kk & 3);
+          mma_bf16_ts(tmem + kTmS + 64u * sb, tmem + kTmQ + 8u * kk, bd, idesc_s, kk > 0);
         }
-        if (j >= 1) {  // O += P_i V_i for i = j - 1, P as head + tail
-          const int i = j - 1, pb = i & 1, si = i % kTcStages;
-          if (!mbar_wait_bounded(smem_u32(&tail->pfull[pb]), (uint32_t)(i >> 1) & 1u, abort, a.err,
-                                 DEV_TIMEOUT_MMA)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t vbase = smem_u32(smem + kTcOffKV + si * kTcStageBytes + kTcKBytes);
-          const uint32_t pbase = smem_u32(smem + kTcOffP + pb * 2 * kTcPBytes);
+        mma_commit(smem_u32(&tail->sfull[sb]));
+      };
+      if (ok) tc_fence_after();
+      for (int j = 0; j < 2 && j < n; ++j) issue_s(j);
+      for (int i = 0; ok && i < n; ++i) {
+        const int pb = i % kTcSBufs, si = i % kTcStages;
+        ok = mbar_wait_bounded(smem_u32(&tail->pfull[pb]), (uint32_t)(i / kTcSBufs) & 1u, abort,
+                               a.err, DEV_TIMEOUT_MMA);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vbase = smem_u32(smem + si * kTcStageBytes + kTcKBytes);
+        const uint32_t pcol = tmem + kTmS + 64u * pb;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < 2; ++h) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = sw128_desc(pbase + h * kTcPBytes) + 2 * kk;
-              const uint64_t bd = sw128_desc(vbase) + 2 * kk;
-              mma_bf16(tmem + 128u, ad, bd, idesc_o, (i | h | kk) != 0);
-            }
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = sw128_desc(vbase) + 2 * kk;
+            mma_bf16_ts(tmem + kTmO, pcol + 32u * h + 8u * kk, bd, idesc_o, (i | h | kk) != 0);
           }
-          mma_commit(smem_u32(&tail->kvempty[si]));
-          mma_commit(smem_u32(&tail->pempty[pb]));
         }
+        mma_commit(smem_u32(&tail->kvempty[si]));
+        mma_commit(smem_u32(&tail->pempty[pb]));
+        if (i + 2 < n) issue_s(i + 2);
       }
       if (ok) mma_commit(smem_u32(&tail->odone));
     }
@@ -256,8 +278,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int hg = row_ok ? R - t * G : 0;
     const int br = t / a.Bq;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    const uint32_t o_base = lane_base + 128u + (uint32_t)(h * 64);
+    const uint32_t o_base = lane_base + kTmO + (uint32_t)(h * 64);
     const float sl2 = 1.4426950408889634f / sqrtf(128.0f);  // log2(e) / sqrt(dh)
+    // Q row R, columns [64h, 64h + 64), into TMEM (bf16 pairs; rows past the end as 0).
+    {
+      const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((size_t)g * rows + R) * 128 + h * 64);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint4 v = row_ok ? qrow[c * 4 + e] : make_uint4(0, 0, 0, 0);
+          w[4 * e] = v.x;
+          w[4 * e + 1] = v.y;
+          w[4 * e + 2] = v.z;
+          w[4 * e + 3] = v.w;
+        }
+        tmem_st16u(lane_base + kTmQ + (uint32_t)(h * 32 + c * 16), w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&tail->qfull));
+    }
     // Both warps of a quarter pass the same number of pair barriers: after a failed
     // (bounded) wait a warp keeps iterating with its waits and TMEM accesses skipped
     // (`ok` stays warp-uniform), so its partner is never left at a barrier.
@@ -269,25 +311,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                     DEV_TIMEOUT_EPILOGUE));
     };
     for (int j = 0; j < n; ++j) {
-      const int sb = j & 1;
-      wait_all(&tail->sfull[sb], (uint32_t)(j >> 1) & 1u);
+      const int sb = j % kTcSBufs;
+      const uint32_t s_col = lane_base + kTmS + 64u * sb;
+      wait_all(&tail->sfull[sb], (uint32_t)(j / kTcSBufs) & 1u);
       float sv[32];
       if (ok) {
         tc_fence_after();
         float x0[16], x1[16];
-        tmem_ld16x2(lane_base + (uint32_t)(sb * 64 + h * 32), lane_base + (uint32_t)(sb * 64 + h * 32 + 16),
-                    x0, x1);
+        tmem_ld16x2(s_col + (uint32_t)(h * 32), s_col + (uint32_t)(h * 32 + 16), x0, x1);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           sv[c] = x0[c];
           sv[16 + c] = x1[c];
         }
-        tc_fence_before();
       } else {
 #pragma unroll
         for (int c = 0; c < 32; ++c) sv[c] = -INFINITY;
       }
-      mbar_arrive(smem_u32(&tail->sempty[sb]));  // S buffer may be overwritten
       // Mask only where the tile is not wholly visible (the last prefix tile, block keys).
       if (j >= ks.n_pre - 1) {
         int vlo, vhi;
@@ -298,11 +338,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int c = 0; c < 32; ++c)
           if (c < vlo || c >= vhi) sv[c] = -INFINITY;
       }
-      float hm = -INFINITY;
+      float m0 = sv[0], m1 = sv[1], m2 = sv[2], m3 = sv[3];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) hm = fmaxf(hm, sv[c]);
+      for (int c = 4; c < 28; c += 8) {
+        m0 = fmax3(m0, sv[c], sv[c + 1]);
+        m1 = fmax3(m1, sv[c + 2], sv[c + 3]);
+        m2 = fmax3(m2, sv[c + 4], sv[c + 5]);
+        m3 = fmax3(m3, sv[c + 6], sv[c + 7]);
+      }
+      m0 = fmax3(m0, sv[28], sv[29]);
+      m1 = fmax3(m1, sv[30], sv[31]);
+      const float hm = fmax3(m0, m1, fmaxf(m2, m3));
       tail->xmax[sb][h][r] = hm;
+      // Both halves of S are in registers past this barrier, so P may overwrite S.
+      tc_fence_before();
       pair_sync();
+      tc_fence_after();
       const float mx = fmaxf(hm, tail->xmax[sb][h ^ 1][r]) * sl2;  // row max, log2 units
       // Lazy rescale: a row moves its reference maximum only when the tile maximum
       // exceeds it by more than 2^8 (also at its first visible key).  O then holds
@@ -311,7 +362,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool need = mx > m_ref + kLazyRescale;
       const bool need_o = need && m_ref != -INFINITY;  // only for j >= 1
       const float alpha = need_o ? exp2f(m_ref - mx) : 1.f;
-      if (ok && __any_sync(kAll, need_o)) wait_all(&tail->pempty[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u);
+      if (ok && __any_sync(kAll, need_o))
+        wait_all(&tail->pempty[(j - 1) % kTcSBufs], (uint32_t)((j - 1) / kTcSBufs) & 1u);
       if (ok && __any_sync(kAll, need_o)) {
         tc_fence_after();
 #pragma unroll
@@ -326,39 +378,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tmem_st16(o_base + c, u);
           tmem_st16(o_base + c + 16, w);
         }
-        tmem_st_wait();
       }
       if (need_o) l *= alpha;
       if (need) m_ref = mx;
-      // P = 2^(s * sl2 - m_ref) (masked s = -inf gives 0) as bf16 head + bf16 tail, in the
-      // 128-byte-swizzled K-major layout of an MMA A operand (16-byte chunk c of row r at
-      // chunk c ^ (r % 8)).
-      if (j >= 2) wait_all(&tail->pempty[sb], (uint32_t)((j - 2) >> 1) & 1u);
-      uint8_t* ph = smem + kTcOffP + sb * 2 * kTcPBytes + r * 128;
-      uint8_t* pt = ph + kTcPBytes;
+      // P = 2^(s * sl2 - m_ref) (masked s = -inf gives 0) as a bf16 head and a bf16 tail
+      // (two MMAs keep P's fp32 accuracy), written over this thread's S columns: keys
+      // [32h, 32h + 32) are head columns [16h, 16h + 16) and tail columns 32 + [16h, 16h + 16).
+      // Pairs of keys go through the packed two-lane FMA / add.
       const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
+      const float2 sl2x2 = make_float2(sl2, sl2), nmx2 = make_float2(nm, nm);
+      float2 l2 = make_float2(0.f, 0.f);
+      uint32_t hw[16], tw[16];
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        uint4 hv, tv;
-        uint32_t* hw = reinterpret_cast<uint32_t*>(&hv);
-        uint32_t* tw = reinterpret_cast<uint32_t*>(&tv);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = ex2_approx(fmaf(sv[c8 * 8 + 2 * e], sl2, nm));
-          const float p1 = ex2_approx(fmaf(sv[c8 * 8 + 2 * e + 1], sl2, nm));
-          l += p0 + p1;
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-          const float2 hf = __bfloat1622float2(h2);
-          const __nv_bfloat162 t2 = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
-          hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
-          tw[e] = *reinterpret_cast<const uint32_t*>(&t2);
-        }
-        const int off = ((h * 4 + c8) ^ (r & 7)) << 4;
-        *reinterpret_cast<uint4*>(ph + off) = hv;
-        *reinterpret_cast<uint4*>(pt + off) = tv;
+      for (int e = 0; e < 16; ++e) {
+        const float2 x = __ffma2_rn(make_float2(sv[2 * e], sv[2 * e + 1]), sl2x2, nmx2);
+        const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        l2 = __fadd2_rn(l2, p);
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(p.x, p.y);
+        const float2 tl = __ffma2_rn(__bfloat1622float2(h2), make_float2(-1.f, -1.f), p);
+        const __nv_bfloat162 t2 = __floats2bfloat162_rn(tl.x, tl.y);
+        hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
+        tw[e] = *reinterpret_cast<const uint32_t*>(&t2);
       }
-      fence_proxy_async_smem();
-      tc_fence_before();  // orders any O rescale (tcgen05.st) before the P V MMAs
+      l += l2.x + l2.y;
+      if (ok) {
+        tmem_st16u(s_col + (uint32_t)(16 * h), hw);
+        tmem_st16u(s_col + (uint32_t)(32 + 16 * h), tw);
+      }
+      tmem_st_wait();  // also covers the O rescale's stores
+      tc_fence_before();
       mbar_arrive(smem_u32(&tail->pfull[sb]));
     }
     // Epilogue: out row = O / l in bf16 (a row that saw no key is written as zeros); l is
@@ -400,7 +448,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, kTmCols);
   }
 }
 
