@@ -19,14 +19,14 @@
 // CTA's rows belong to, with a per-row branch mask.
 //
 // head_dim 128 runs on the 5th-generation tensor cores (tcgen05): a CTA owns 128 query
-// rows (= TMEM lanes).  One warp streams Q once and K / V^T tiles of 64 keys with TMA;
-// one warp issues S = Q K^T into a double-buffered TMEM tile and O += P V into a TMEM
-// accumulator; the softmax warps (one thread per row and column half) run the online
-// softmax - reading S from
-// TMEM, writing P as a bf16 head and a bf16 tail (two MMAs keep P's fp32 accuracy) into
-// shared memory, and rescaling O in TMEM only when a row's running maximum grows by more
-// than 2^8 (the result is unchanged: O and the normaliser share the same reference).
-// Eight softmax warps: two per TMEM lane quarter, each on half of the 64 key columns.
+// rows (= TMEM lanes).  The softmax warps load Q into TMEM; one warp streams K / V^T tiles
+// of 128 keys with TMA; one warp issues S = Q K^T (Q from TMEM) into a double-buffered TMEM
+// tile and O += P V into a TMEM accumulator, with P read from TMEM as well: the softmax
+// warps (one thread per row and key half) read S, compute P as a bf16 head and a bf16 tail
+// (two MMAs keep P's fp32 accuracy), write it over S, and rescale O in TMEM only when a
+// row's running maximum grows by more than 2^8 (the result is unchanged: O and the
+// normaliser share the same reference).  Shared memory holds only the K / V^T ring.
+// Eight softmax warps: two per TMEM lane quarter, each on half of the 128 keys.
 // head_dim 32 and 64 run on bf16 mma.sync with the same layouts.
 #include <cstring>
 
@@ -39,33 +39,36 @@ namespace {
 
 constexpr int kKeyTile = 64;
 
-// Key-tile schedule shared by both kernels: prefix tiles [0, n_pre), then block-key
-// tiles covering the scratch columns [kb_lo, kb_end) of the branches in [b_lo, b_hi].
+// Key-tile schedule shared by both kernels (KT keys per tile: 128 on the tensor-core path,
+// 64 on mma.sync): prefix tiles [0, n_pre), then block-key tiles covering the scratch
+// columns [kb_lo, kb_end) of the branches in [b_lo, b_hi].
 struct KeySched {
   int Pk, n_pre, kb_lo, n_br;
 };
 
+template <int KT>
 __device__ __forceinline__ KeySched key_sched(const AttnArgs& a, int b_lo, int b_hi) {
   KeySched k;
   k.Pk = a.pk_add + (a.dP ? *a.dP : 0);
-  k.n_pre = (k.Pk + kKeyTile - 1) / kKeyTile;
+  k.n_pre = (k.Pk + KT - 1) / KT;
   k.kb_lo = (a.causal ? 0 : b_lo) * a.Bk_stride;
   const int kb_end = b_hi * a.Bk_stride + a.Bk;
-  k.n_br = a.Bk > 0 ? (kb_end - k.kb_lo + kKeyTile - 1) / kKeyTile : 0;
+  k.n_br = a.Bk > 0 ? (kb_end - k.kb_lo + KT - 1) / KT : 0;
   return k;
 }
 
 // Key columns [lo, hi) of tile j (tile-local) that a row of branch br may see: the
 // committed prefix, or the br-th branch's own block keys (with `causal`, the keys of
 // blocks 0..br).
+template <int KT>
 __device__ __forceinline__ void visible_range(const AttnArgs& a, const KeySched& k, int j, int br,
                                               int& lo, int& hi) {
   if (j < k.n_pre) {
     lo = 0;
-    hi = k.Pk - j * kKeyTile;
+    hi = k.Pk - j * KT;
     return;
   }
-  const int col0 = k.kb_lo + (j - k.n_pre) * kKeyTile;
+  const int col0 = k.kb_lo + (j - k.n_pre) * KT;
   lo = (a.causal ? 0 : br * a.Bk_stride) - col0;
   hi = br * a.Bk_stride + a.Bk - col0;
 }
@@ -86,27 +89,27 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 
 // ================================================================ tcgen05 path (dh = 128)
 constexpr int kTcRows = 128;
-constexpr int kTcStages = 6;     // K / V^T ring depth
-constexpr int kTcSBufs = 3;      // S / P buffers in TMEM
-constexpr int kTcSoftWarps = 8;  // two per TMEM lane quarter, each on half the columns
+constexpr int kTcKeys = 128;     // keys per tile (the N of S = Q K^T)
+constexpr int kTcStages = 3;     // K / V^T ring depth
+constexpr int kTcSoftWarps = 8;  // two per TMEM lane quarter, each on half the keys
 constexpr int kTcThreads = (2 + kTcSoftWarps) * 32;  // warp 0 TMA, warp 1 MMA, softmax
-constexpr uint32_t kTcKBytes = 64 * 128 * 2;    // K tile: 64 keys x 128 (two SW128 atoms)
-constexpr uint32_t kTcVBytes = 128 * 64 * 2;    // V^T tile: 128 rows (dh) x 64 keys
+constexpr uint32_t kTcAtom = 128 * 64 * 2;  // one 128-byte-swizzled atom: 128 rows x 64 bf16
+constexpr uint32_t kTcKBytes = 2 * kTcAtom;  // K tile: 128 keys x (two 64-wide halves of dh)
+constexpr uint32_t kTcVBytes = 2 * kTcAtom;  // V^T tile: 128 (dh) x (two 64-key halves)
 constexpr uint32_t kTcStageBytes = kTcKBytes + kTcVBytes;
 constexpr uint32_t kTcOffTail = kTcStages * kTcStageBytes;
-// TMEM columns: Q (bf16, two per column) [0, 64); S / P buffer b at 64 + 64 b (S as 64
-// fp32 columns, overwritten in place by P: bf16 head in the first 32 columns, tail in the
-// next 32); O (fp32) [256, 384).
-constexpr uint32_t kTmQ = 0, kTmS = 64, kTmO = 256, kTmCols = 512;
+// TMEM columns: Q (bf16, two per column) [0, 64); S / P buffer b at 128 + 128 b (S as 128
+// fp32 columns, overwritten in place by P); O (fp32) [384, 512).
+constexpr uint32_t kTmQ = 0, kTmS = 128, kTmO = 384, kTmCols = 512;
 constexpr float kLazyRescale = 8.0f;  // log2 units
 
 struct TcTail {
   uint64_t qfull;
   uint64_t kvfull[kTcStages], kvempty[kTcStages];
-  uint64_t sfull[kTcSBufs], pfull[kTcSBufs], pempty[kTcSBufs];
+  uint64_t sfull[2], pfull[2], pempty[2];
   uint64_t odone;
-  float xmax[kTcSBufs][2][kTcRows];  // [buffer][column half][row]: half-row maxima
-  float xsum[2][kTcRows];            // [column half][row]: half-row sums of P
+  float xmax[2][2][kTcRows];  // [buffer][key half][row]: half-row maxima
+  float xsum[2][kTcRows];     // [key half][row]: half-row sums of P
   uint32_t tmem;
   int abort;
 };
@@ -118,7 +121,13 @@ struct TcMaps {
   CUtensorMap q, kc, vtc, kb, vtb;
 };
 
-// Stores 16 32-bit words into consecutive TMEM columns of this thread's lane.
+// Stores 8 / 16 32-bit words into consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+               "r"(v[7])
+               : "memory");
+}
 __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -127,6 +136,48 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[1
       "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
       "r"(v[15])
       : "memory");
+}
+
+// Loads 64 consecutive fp32 TMEM columns of this thread's lane (two 32x32b.x32 loads,
+// one wait; threading the registers through the wait keeps every use after it).
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, float (&v)[64]) {
+  uint32_t x[32], y[32];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+               "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+               "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]),
+                 "=r"(x[7]), "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]),
+                 "=r"(x[14]), "=r"(x[15]), "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]),
+                 "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]), "=r"(x[24]), "=r"(x[25]),
+                 "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31])
+               : "r"(ta));
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+               "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+               "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(y[0]), "=r"(y[1]), "=r"(y[2]), "=r"(y[3]), "=r"(y[4]), "=r"(y[5]), "=r"(y[6]),
+                 "=r"(y[7]), "=r"(y[8]), "=r"(y[9]), "=r"(y[10]), "=r"(y[11]), "=r"(y[12]), "=r"(y[13]),
+                 "=r"(y[14]), "=r"(y[15]), "=r"(y[16]), "=r"(y[17]), "=r"(y[18]), "=r"(y[19]),
+                 "=r"(y[20]), "=r"(y[21]), "=r"(y[22]), "=r"(y[23]), "=r"(y[24]), "=r"(y[25]),
+                 "=r"(y[26]), "=r"(y[27]), "=r"(y[28]), "=r"(y[29]), "=r"(y[30]), "=r"(y[31])
+               : "r"(ta + 32u));
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(x[0]), "+r"(x[1]), "+r"(x[2]), "+r"(x[3]), "+r"(x[4]), "+r"(x[5]), "+r"(x[6]),
+                 "+r"(x[7]), "+r"(x[8]), "+r"(x[9]), "+r"(x[10]), "+r"(x[11]), "+r"(x[12]), "+r"(x[13]),
+                 "+r"(x[14]), "+r"(x[15]), "+r"(x[16]), "+r"(x[17]), "+r"(x[18]), "+r"(x[19]),
+                 "+r"(x[20]), "+r"(x[21]), "+r"(x[22]), "+r"(x[23]), "+r"(x[24]), "+r"(x[25]),
+                 "+r"(x[26]), "+r"(x[27]), "+r"(x[28]), "+r"(x[29]), "+r"(x[30]), "+r"(x[31]),
+                 "+r"(y[0]), "+r"(y[1]), "+r"(y[2]), "+r"(y[3]), "+r"(y[4]), "+r"(y[5]), "+r"(y[6]),
+                 "+r"(y[7]), "+r"(y[8]), "+r"(y[9]), "+r"(y[10]), "+r"(y[11]), "+r"(y[12]), "+r"(y[13]),
+                 "+r"(y[14]), "+r"(y[15]), "+r"(y[16]), "+r"(y[17]), "+r"(y[18]), "+r"(y[19]),
+                 "+r"(y[20]), "+r"(y[21]), "+r"(y[22]), "+r"(y[23]), "+r"(y[24]), "+r"(y[25]),
+                 "+r"(y[26]), "+r"(y[27]), "+r"(y[28]), "+r"(y[29]), "+r"(y[30]), "+r"(y[31])
+               :
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = __uint_as_float(x[i]);
+    v[32 + i] = __uint_as_float(y[i]);
+  }
 }
 
 // D[tmem] (+)= A[tmem] * B[smem desc]^T: A's 128 rows are the TMEM lanes, its K bf16
@@ -162,7 +213,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(smem_u32(&tail->kvfull[s]), 1);
       mbar_init(smem_u32(&tail->kvempty[s]), 1);
     }
-    for (int s = 0; s < kTcSBufs; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&tail->sfull[s]), 1);
       mbar_init(smem_u32(&tail->pfull[s]), kTcSoftWarps * 32);
       mbar_init(smem_u32(&tail->pempty[s]), 1);
@@ -186,7 +237,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* abort = &tail->abort;
   pdl_trigger();
   pdl_wait();  // q and the block keys come from the previous kernel; out may be read by it
-  const KeySched ks = key_sched(a, b_lo, b_hi);
+  const KeySched ks = key_sched<kTcKeys>(a, b_lo, b_hi);
   const int n = ks.n_pre + ks.n_br;
 
   if (warp == 0) {
@@ -202,70 +253,70 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t kdst = smem_u32(smem + s * kTcStageBytes);
         const uint32_t vdst = kdst + kTcKBytes;
         mbar_arrive_expect_tx(fb, kTcStageBytes);
-        if (j < ks.n_pre) {
-          const int k0 = j * kKeyTile;
-          tma_load_2d(kdst, &m.kc, fb, g * 128, k0, keep);
-          tma_load_2d(kdst + kTcKBytes / 2, &m.kc, fb, g * 128 + 64, k0, keep);
-          tma_load_2d(vdst, &m.vtc, fb, k0, g * 128, keep);
-        } else {
-          const int c0 = ks.kb_lo + (j - ks.n_pre) * kKeyTile;
-          tma_load_2d(kdst, &m.kb, fb, g * 128, c0, keep);
-          tma_load_2d(kdst + kTcKBytes / 2, &m.kb, fb, g * 128 + 64, c0, keep);
-          tma_load_2d(vdst, &m.vtb, fb, c0, g * 128, keep);
-        }
+        const bool pre = j < ks.n_pre;
+        const CUtensorMap* km = pre ? &m.kc : &m.kb;
+        const CUtensorMap* vm = pre ? &m.vtc : &m.vtb;
+        const int k0 = pre ? j * kTcKeys : ks.kb_lo + (j - ks.n_pre) * kTcKeys;
+        tma_load_2d(kdst, km, fb, g * 128, k0, keep);
+        tma_load_2d(kdst + kTcAtom, km, fb, g * 128 + 64, k0, keep);
+        tma_load_2d(vdst, vm, fb, k0, g * 128, keep);
+        tma_load_2d(vdst + kTcAtom, vm, fb, k0 + 64, g * 128, keep);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // S_j = Q K_j^T runs two tiles ahead of O += P_i V_i: S_j goes into buffer j % 3
-      // once P_{j-3} V has been read from it.
-      const uint32_t idesc_s = idesc_bf16(128, kKeyTile);
+      // S_{j+1} = Q K_{j+1}^T is issued before O += P_j V_j, into the buffer that
+      // P_{j-1} V_{j-1} has finished reading.
+      const uint32_t idesc_s = idesc_bf16(128, kTcKeys);
       const uint32_t idesc_o = idesc_bf16(128, 128);
       bool ok = mbar_wait_bounded(smem_u32(&tail->qfull), 0, abort, a.err, DEV_TIMEOUT_MMA);
       auto issue_s = [&](int j) {
-        const int s = j % kTcStages, sb = j % kTcSBufs;
+        const int s = j % kTcStages, sb = j & 1;
         ok = ok && mbar_wait_bounded(smem_u32(&tail->kvfull[s]), (uint32_t)(j / kTcStages) & 1u,
                                      abort, a.err, DEV_TIMEOUT_MMA);
-        ok = ok && (j < kTcSBufs ||
-                    mbar_wait_bounded(smem_u32(&tail->pempty[sb]), (uint32_t)(j / kTcSBufs - 1) & 1u,
-                                      abort, a.err, DEV_TIMEOUT_MMA));
+        ok = ok && (j < 2 || mbar_wait_bounded(smem_u32(&tail->pempty[sb]),
+                                               (uint32_t)((j >> 1) - 1) & 1u, abort, a.err,
+                                               DEV_TIMEOUT_MMA));
         if (!ok) return;
         tc_fence_after();
         const uint32_t kbase = smem_u32(smem + s * kTcStageBytes);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = sw128_desc(kbase + (kk >> 2) * (kTcKBytes / 2)) + 2 * (kk & 3);
-          mma_bf16_ts(tmem + kTmS + 64u * sb, tmem + kTmQ + 8u * kk, bd, idesc_s, kk > 0);
+          const uint64_t bd = sw128_desc(kbase + (kk >> 2) * kTcAtom) + 2 * (kk & 3);
+          mma_bf16_ts(tmem + kTmS + 128u * sb, tmem + kTmQ + 8u * kk, bd, idesc_s, kk > 0);
         }
         mma_commit(smem_u32(&tail->sfull[sb]));
       };
-      if (ok) tc_fence_after();
-      for (int j = 0; j < 2 && j < n; ++j) issue_s(j);
+      if (ok && n > 0) {
+        tc_fence_after();
+        issue_s(0);
+      }
       for (int i = 0; ok && i < n; ++i) {
-        const int pb = i % kTcSBufs, si = i % kTcStages;
-        ok = mbar_wait_bounded(smem_u32(&tail->pfull[pb]), (uint32_t)(i / kTcSBufs) & 1u, abort,
-                               a.err, DEV_TIMEOUT_MMA);
+        if (i + 1 < n) issue_s(i + 1);
+        const int pb = i & 1, si = i % kTcStages;
+        ok = ok && mbar_wait_bounded(smem_u32(&tail->pfull[pb]), (uint32_t)(i >> 1) & 1u, abort,
+                                     a.err, DEV_TIMEOUT_MMA);
         if (!ok) break;
         tc_fence_after();
         const uint32_t vbase = smem_u32(smem + si * kTcStageBytes + kTcKBytes);
-        const uint32_t pcol = tmem + kTmS + 64u * pb;
+        const uint32_t pcol = tmem + kTmS + 128u * pb;
+        // Keys [16c, 16c + 16): half hh = c / 4 of the tile, P head columns 64 hh + 8 mq
+        // and tail columns 64 hh + 32 + 8 mq (mq = c % 4), V^T atom hh at key offset 16 mq.
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = sw128_desc(vbase) + 2 * kk;
-            mma_bf16_ts(tmem + kTmO, pcol + 32u * h + 8u * kk, bd, idesc_o, (i | h | kk) != 0);
-          }
+        for (int c = 0; c < 8; ++c) {
+          const int hh = c >> 2, mq = c & 3;
+          const uint64_t bd = sw128_desc(vbase + hh * kTcAtom) + 2 * mq;
+          mma_bf16_ts(tmem + kTmO, pcol + 64u * hh + 8u * mq, bd, idesc_o, (i | c) != 0);
+          mma_bf16_ts(tmem + kTmO, pcol + 64u * hh + 32u + 8u * mq, bd, idesc_o, 1u);
         }
         mma_commit(smem_u32(&tail->kvempty[si]));
         mma_commit(smem_u32(&tail->pempty[pb]));
-        if (i + 2 < n) issue_s(i + 2);
       }
       if (ok) mma_commit(smem_u32(&tail->odone));
     }
   } else {
     // Softmax + epilogue.  Warp w serves TMEM lane quarter q = w % 4 (query rows
-    // 32q..32q+31, one per lane) and column half h: S columns [32h, 32h+32) and O columns
+    // 32q..32q+31, one per lane) and key half h: S columns [64h, 64h+64) and O columns
     // [64h, 64h+64); the two warps of a quarter exchange their half-row maxima through
     // shared memory (named barrier 1 + q).  tcgen05.ld/st are warp-wide, so every decision
     // guarding one is made uniform across the warp.
@@ -311,49 +362,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                     DEV_TIMEOUT_EPILOGUE));
     };
     for (int j = 0; j < n; ++j) {
-      const int sb = j % kTcSBufs;
-      const uint32_t s_col = lane_base + kTmS + 64u * sb;
-      wait_all(&tail->sfull[sb], (uint32_t)(j / kTcSBufs) & 1u);
-      float sv[32];
+      const int sb = j & 1;
+      const uint32_t s_col = lane_base + kTmS + 128u * sb + (uint32_t)(h * 64);
+      wait_all(&tail->sfull[sb], (uint32_t)(j >> 1) & 1u);
+      float sv[64];
       if (ok) {
         tc_fence_after();
-        float x0[16], x1[16];
-        tmem_ld16x2(s_col + (uint32_t)(h * 32), s_col + (uint32_t)(h * 32 + 16), x0, x1);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          sv[c] = x0[c];
-          sv[16 + c] = x1[c];
-        }
+        tmem_ld32x2(s_col, sv);
       } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) sv[c] = -INFINITY;
+        for (int c = 0; c < 64; ++c) sv[c] = -INFINITY;
       }
       // Mask only where the tile is not wholly visible (the last prefix tile, block keys).
       if (j >= ks.n_pre - 1) {
         int vlo, vhi;
-        visible_range(a, ks, j, br, vlo, vhi);
-        vlo -= h * 32;
-        vhi -= h * 32;
+        visible_range<kTcKeys>(a, ks, j, br, vlo, vhi);
+        vlo -= h * 64;
+        vhi -= h * 64;
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
+        for (int c = 0; c < 64; ++c)
           if (c < vlo || c >= vhi) sv[c] = -INFINITY;
       }
       float m0 = sv[0], m1 = sv[1], m2 = sv[2], m3 = sv[3];
 #pragma unroll
-      for (int c = 4; c < 28; c += 8) {
+      for (int c = 4; c < 60; c += 8) {
         m0 = fmax3(m0, sv[c], sv[c + 1]);
         m1 = fmax3(m1, sv[c + 2], sv[c + 3]);
         m2 = fmax3(m2, sv[c + 4], sv[c + 5]);
         m3 = fmax3(m3, sv[c + 6], sv[c + 7]);
       }
-      m0 = fmax3(m0, sv[28], sv[29]);
-      m1 = fmax3(m1, sv[30], sv[31]);
+      m0 = fmax3(m0, sv[60], sv[61]);
+      m1 = fmax3(m1, sv[62], sv[63]);
       const float hm = fmax3(m0, m1, fmaxf(m2, m3));
       tail->xmax[sb][h][r] = hm;
-      // Both halves of S are in registers past this barrier, so P may overwrite S.
-      tc_fence_before();
       pair_sync();
-      tc_fence_after();
       const float mx = fmaxf(hm, tail->xmax[sb][h ^ 1][r]) * sl2;  // row max, log2 units
       // Lazy rescale: a row moves its reference maximum only when the tile maximum
       // exceeds it by more than 2^8 (also at its first visible key).  O then holds
@@ -362,49 +404,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool need = mx > m_ref + kLazyRescale;
       const bool need_o = need && m_ref != -INFINITY;  // only for j >= 1
       const float alpha = need_o ? exp2f(m_ref - mx) : 1.f;
-      if (ok && __any_sync(kAll, need_o))
-        wait_all(&tail->pempty[(j - 1) % kTcSBufs], (uint32_t)((j - 1) / kTcSBufs) & 1u);
       if (ok && __any_sync(kAll, need_o)) {
-        tc_fence_after();
+        wait_all(&tail->pempty[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u);
+        if (ok) {
+          tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) {
-          float u[16], w[16];
-          tmem_ld16x2(o_base + c, o_base + c + 16, u, w);
+          for (int c = 0; c < 64; c += 32) {
+            float u[16], w[16];
+            tmem_ld16x2(o_base + c, o_base + c + 16, u, w);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            u[e] *= alpha;
-            w[e] *= alpha;
+            for (int e = 0; e < 16; ++e) {
+              u[e] *= alpha;
+              w[e] *= alpha;
+            }
+            tmem_st16(o_base + c, u);
+            tmem_st16(o_base + c + 16, w);
           }
-          tmem_st16(o_base + c, u);
-          tmem_st16(o_base + c + 16, w);
         }
       }
       if (need_o) l *= alpha;
       if (need) m_ref = mx;
       // P = 2^(s * sl2 - m_ref) (masked s = -inf gives 0) as a bf16 head and a bf16 tail
-      // (two MMAs keep P's fp32 accuracy), written over this thread's S columns: keys
-      // [32h, 32h + 32) are head columns [16h, 16h + 16) and tail columns 32 + [16h, 16h + 16).
-      // Pairs of keys go through the packed two-lane FMA / add.
+      // (two MMAs keep P's fp32 accuracy), written over this warp's own S columns: keys
+      // 64h + 16mq + [0, 16) go to head columns 8mq + [0, 8) and tail columns
+      // 32 + 8mq + [0, 8) of the half.  Pairs of keys use the packed two-lane FMA / add.
       const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
       const float2 sl2x2 = make_float2(sl2, sl2), nmx2 = make_float2(nm, nm);
       float2 l2 = make_float2(0.f, 0.f);
-      uint32_t hw[16], tw[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float2 x = __ffma2_rn(make_float2(sv[2 * e], sv[2 * e + 1]), sl2x2, nmx2);
-        const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-        l2 = __fadd2_rn(l2, p);
-        const __nv_bfloat162 h2 = __floats2bfloat162_rn(p.x, p.y);
-        const float2 tl = __ffma2_rn(__bfloat1622float2(h2), make_float2(-1.f, -1.f), p);
-        const __nv_bfloat162 t2 = __floats2bfloat162_rn(tl.x, tl.y);
-        hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
-        tw[e] = *reinterpret_cast<const uint32_t*>(&t2);
+      for (int mq = 0; mq < 4; ++mq) {
+        uint32_t hw[8], tw[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int c = mq * 16 + 2 * e;
+          const float2 x = __ffma2_rn(make_float2(sv[c], sv[c + 1]), sl2x2, nmx2);
+          const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          l2 = __fadd2_rn(l2, p);
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(p.x, p.y);
+          const float2 tl = __ffma2_rn(__bfloat1622float2(h2), make_float2(-1.f, -1.f), p);
+          const __nv_bfloat162 t2 = __floats2bfloat162_rn(tl.x, tl.y);
+          hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          tw[e] = *reinterpret_cast<const uint32_t*>(&t2);
+        }
+        if (ok) {
+          tmem_st8u(s_col + 8u * mq, hw);
+          tmem_st8u(s_col + 32u + 8u * mq, tw);
+        }
       }
       l += l2.x + l2.y;
-      if (ok) {
-        tmem_st16u(s_col + (uint32_t)(16 * h), hw);
-        tmem_st16u(s_col + (uint32_t)(32 + 16 * h), tw);
-      }
       tmem_st_wait();  // also covers the O rescale's stores
       tc_fence_before();
       mbar_arrive(smem_u32(&tail->pfull[sb]));
@@ -514,7 +561,7 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnArgs a) {
   const int G = a.H / a.Hk;
   const int T = a.nbq * a.Bq;
   const int rows = a.Bq * G;  // rows of this (branch, KV head)
-  const KeySched ks = key_sched(a, b, b);
+  const KeySched ks = key_sched<kKeyTile>(a, b, b);
   const int ntiles = ks.n_pre + ks.n_br;
   const int my_tiles = ntiles > kg ? (ntiles - kg + 1) / 2 : 0;
   const float sl2 = 1.4426950408889634f / sqrtf((float)DH);  // log2(e) / sqrt(dh)
@@ -601,7 +648,7 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnArgs a) {
       }
     }
     int vlo, vhi;
-    visible_range(a, ks, tile, b, vlo, vhi);
+    visible_range<kKeyTile>(a, ks, tile, b, vlo, vhi);
     float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int ng = 0; ng < 8; ++ng) {
@@ -779,13 +826,13 @@ const char* plan_attention(AttnLaunch* L, const AttnArgs& a, int dh, int kc_rows
   // at the query array so that every map is valid.
   if (!make_tmap_bf16(&maps[0], a.q, (uint64_t)a.Hk * T * G, 128, 128, err, sizeof(err)) ||
       !make_tmap_bf16(&maps[1], kc_rows > 0 ? (const void*)a.kc : (const void*)a.q,
-                      kc_rows > 0 ? kc_rows : T, kc_rows > 0 ? (uint64_t)a.Hk * 128 : 128, 64,
+                      kc_rows > 0 ? kc_rows : T, kc_rows > 0 ? (uint64_t)a.Hk * 128 : 128, kTcKeys,
                       err, sizeof(err)) ||
       !make_tmap_bf16(&maps[2], vtc_cols > 0 ? (const void*)a.vtc : (const void*)a.q,
                       vtc_cols > 0 ? (uint64_t)a.Hk * 128 : T, vtc_cols > 0 ? vtc_cols : 128, 128,
                       err, sizeof(err), vtc_cols > 0 ? (uint64_t)a.ldvc : 0) ||
       !make_tmap_bf16(&maps[3], a.Bk > 0 ? (const void*)a.kb : (const void*)a.q,
-                      a.Bk > 0 ? kbr : T, a.Bk > 0 ? (uint64_t)a.Hk * 128 : 128, 64, err,
+                      a.Bk > 0 ? kbr : T, a.Bk > 0 ? (uint64_t)a.Hk * 128 : 128, kTcKeys, err,
                       sizeof(err)) ||
       !make_tmap_bf16(&maps[4], a.Bk > 0 ? (const void*)a.vtb : (const void*)a.q,
                       a.Bk > 0 ? (uint64_t)a.Hk * 128 : T, a.Bk > 0 ? kbr : 128, 128, err,
