@@ -192,6 +192,14 @@ def verify_bytes_flops(shape, T, P, B):
     return by, fl
 
 
+def prefill_flops(shape, P):
+    """Flops of the prompt forward over P tokens: 2 per projection weight per token (no LM
+    head) plus q.k and p.v over the P x P bidirectional prompt block."""
+    L = shape.n_layers
+    proj = sum(gemm_flops(shape, P, kind) for kind in range(4))
+    return L * (proj + 4 * shape.n_heads * shape.head_dim * P * P)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -206,8 +214,12 @@ def main():
                     help="only launch this projection GEMM kind 3 times (for ncu captures)")
     ap.add_argument("--profile-decode", action="store_true",
                     help="prefill + warmup decodes + steps decodes, no timing (for ncu launch lists)")
+    ap.add_argument("--profile-attention", type=int, default=None, metavar="PREFIX",
+                    help="only the branch attention of the workload's verification step over a "
+                         "PREFIX-key prefix: 3 + 20 launches, CUDA-event time (small ncu case)")
     args = ap.parse_args()
-    if args.warmup < 3 and args.impl == "ours" and not (args.profile_decode or args.profile_gemm is not None):
+    profiling = args.profile_decode or args.profile_gemm is not None or args.profile_attention is not None
+    if args.warmup < 3 and args.impl == "ours" and not profiling:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
@@ -226,6 +238,23 @@ def main():
         import dataclasses
         dshape = dataclasses.replace(dshape, k=args.k)
     B, P0, gen = dshape.block, dshape.prompt_len, dshape.gen_len
+    if args.profile_attention is not None:
+        nb = dshape.k + 1
+        ins = [x.cuda() for x in synth.make_attention_inputs(
+            nb, B, args.profile_attention, shape.n_heads, shape.n_kv_heads, shape.head_dim, seed=7)]
+        pack = api.attention_layouts(*ins)
+        for _ in range(3):
+            api.branch_attention_call(pack)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(20):
+            api.branch_attention_call(pack)
+        e1.record()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_attention": {"prefix": args.profile_attention, "rows": nb * B,
+                                                "us": e0.elapsed_time(e1) / 20 * 1e3}}), flush=True)
+        return
     t_gen = time.perf_counter()
     weights = synth.make_weights(shape, 0)
     dev_w = api.upload_weights(shape, weights)
@@ -330,6 +359,22 @@ def main():
               "block_start_forward_ms_median": s_med,
               "peaks": {"hbm_gbs": peak_bw, "bf16_tflops_sustained": peak_tc, "source": peak_src}}
 
+    # Prompt forward (the step before the decode): CUDA-event time of lopa_prefill
+    # (synchronous, so the events bracket it), median of 3, against the tensor roofline.
+    pre_ms = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(dec.stream)
+        dec.prefill(prompt)
+        e1.record(dec.stream)
+        torch.cuda.synchronize()
+        pre_ms.append(e0.elapsed_time(e1))
+    pf = prefill_flops(shape, P0)
+    prefill = {"ms_median": statistics.median(pre_ms), "tokens": P0, "flops": pf,
+               "tensor_roofline_ms": pf / peak_tc / 1e9,
+               "frac_tensor_roofline": pf / peak_tc / 1e9 / statistics.median(pre_ms)}
+
     # End to end through the public API with host buffers: prompt H2D, tokens D2H.
     import torch as _t
     pin_prompt = _t.from_numpy(prompt.astype(np.int32)).pin_memory()
@@ -368,7 +413,7 @@ def main():
             "tpf": tpf, "tpf_unmerged": tokens / (iters + blocks),
             "ms_per_forward": ms_per_forward,
             "lopa_iterations": iters, "blocks": blocks, "forwards": forwards,
-            "verify_step": verify,
+            "verify_step": verify, "prefill": prefill,
             "kernels": kern, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": gpu_launches, "clocks": clocks.summary(),
             "weight_gen_s": t_gen,

@@ -214,13 +214,11 @@ def lmhead_argmax(hidden: torch.Tensor, lm_head: torch.Tensor, logit_scale: floa
     return am, mp
 
 
-def branch_attention(q, k_prefix, v_prefix, k_block, v_block):
-    """Branch-isolated attention on natural layouts: q [nb*B, H, dh], k/v_prefix [P, Hk, dh],
-    k/v_block [nb, B, Hk, dh] (bf16, cuda).  Returns out [nb*B, H*dh].
-
-    The library works on the verification forward's layouts (group-major q, values
-    transposed); this wrapper only rearranges the tensors (torch copies) before the call.
-    """
+def attention_layouts(q, k_prefix, v_prefix, k_block, v_block):
+    """Rearranges natural-layout attention inputs - q [nb*B, H, dh], k/v_prefix [P, Hk, dh],
+    k/v_block [nb, B, Hk, dh] (bf16, cuda) - into the library's layouts (group-major q,
+    values transposed; torch copies only) and allocates the output.  Returns the argument
+    pack for branch_attention_call."""
     nb, B, Hk, dh = k_block.shape
     H = q.shape[1]
     G = H // Hk
@@ -233,7 +231,22 @@ def branch_attention(q, k_prefix, v_prefix, k_block, v_block):
     vtb = v_block.reshape(nb * B, Hk * dh).t().contiguous()
     kp, kb = k_prefix.contiguous(), k_block.contiguous()
     out = torch.empty(nb * B, H * dh, dtype=torch.bfloat16, device=q.device)
+    return dict(q=qg, kp=kp, vtp=vtp, P=P, ld=ld, kb=kb, vtb=vtb, nb=nb, B=B, H=H, Hk=Hk,
+                dh=dh, out=out)
+
+
+def branch_attention_call(a: dict):
+    """One lopa_branch_attention launch on an argument pack from attention_layouts;
+    returns its output tensor [nb*B, H*dh]."""
+    P = a["P"]
     L.check(L.load().lopa_branch_attention(
-        qg.data_ptr(), kp.data_ptr() if P else None, vtp.data_ptr() if P else None, P, ld,
-        kb.data_ptr(), vtb.data_ptr(), nb, B, H, Hk, dh, out.data_ptr(), _stream_ptr()))
-    return out
+        a["q"].data_ptr(), a["kp"].data_ptr() if P else None, a["vtp"].data_ptr() if P else None,
+        P, a["ld"], a["kb"].data_ptr(), a["vtb"].data_ptr(), a["nb"], a["B"], a["H"], a["Hk"],
+        a["dh"], a["out"].data_ptr(), _stream_ptr()))
+    return a["out"]
+
+
+def branch_attention(q, k_prefix, v_prefix, k_block, v_block):
+    """Branch-isolated attention on natural layouts (see attention_layouts).  Returns out
+    [nb*B, H*dh]."""
+    return branch_attention_call(attention_layouts(q, k_prefix, v_prefix, k_block, v_block))
