@@ -36,6 +36,10 @@ UNIT = "tokens/s"
 # 8.4 on average over eight prompts; the parity tests show both sides take the same
 # decisions.
 REF_TPF = {"dream7b": 8.4, "dream7b_scaling": 8.4, "small": 4.0, "tiny": 1.5}
+# DRAM bytes (read + write) of one gemm_kernel<SWIGLU> launch at the 7B step shape, from
+# the ncu launch list of the decode (271.60 MB read + 1.11 MB written).  It describes the
+# kernel as it was profiled and must be re-taken (or set to None) when the kernel changes.
+SWIGLU_TRAFFIC_BYTES = 272.71e6
 
 
 def dist_env():
@@ -340,7 +344,10 @@ def main():
     dom = kern["gate_up_swiglu"]
     roofline = {"kernel": "gemm_kernel<SWIGLU> (gate/up + SwiGLU)", "bound": "hbm",
                 "achieved": dom["GB/s"], "peak": peak_bw, "unit": "GB/s",
-                "frac": dom["GB/s"] / peak_bw, "traffic": None, "peak_source": peak_src}
+                "frac": dom["GB/s"] / peak_bw, "traffic": SWIGLU_TRAFFIC_BYTES,
+                "traffic_source": "ncu launch list of the decode: dram__bytes_read.sum + "
+                                  "dram__bytes_write.sum per launch",
+                "peak_source": peak_src}
 
     # Verification-step latency: the forward-only graph of the 8-branch verification (and
     # of the block-start forward), median of 50 back-to-back launches, at a mid-decode
