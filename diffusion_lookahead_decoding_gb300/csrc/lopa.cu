@@ -120,7 +120,6 @@ struct lopa_ctx {
   // last decide built for the coming iteration (valid when !block_fresh).
   bool prefilled = false, block_fresh = true, in_block = false;
   int next_nv = 0, next_final = -1;
-  bool allow_merge = true;  // the completing iteration may run the next block's start
   int P = 0, P0 = 0;
   std::string err;
 };
@@ -343,7 +342,7 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
 // Enqueues one forward of plan p on the context stream (also used inside capture).
 int enqueue_forward(lopa_ctx* ctx, const Plan& p) {
   const lopa_model_config& m = ctx->mc;
-  const int L = m.n_layers, d = m.d_model, H = m.n_heads, Hk = m.n_kv_heads, dh = m.head_dim;
+  const int L = m.n_layers, d = m.d_model;
   cudaStream_t s = ctx->stream;
   CK(launch_embed_norm(p.tok, p.T, ctx->embed, ctx->attn_norm[0], ctx->x, ctx->n, d, m.rms_eps, s));
   for (int l = 0; l < L; ++l) {
@@ -626,7 +625,7 @@ int read_next(lopa_ctx* ctx) {
 // the forward that evaluates them: only the valid branches (nb = 1 + lookaheads); or, when
 // the iteration completes the block, only the completing branch - together with the next
 // block's block-start rows (block-causal attention) when a next block fits.
-int step_impl(lopa_ctx* ctx, lopa_step_result* out) {
+int step_impl(lopa_ctx* ctx, lopa_step_result* out, bool allow_merge) {
   if (!ctx->prefilled) return fail(ctx, LOPA_ERR_BAD_STATE, "lopa_step before lopa_prefill");
   const int B = ctx->dc.block;
   if (ctx->P + B > ctx->mc.max_seq)
@@ -638,7 +637,7 @@ int step_impl(lopa_ctx* ctx, lopa_step_result* out) {
     if ((r = read_next(ctx))) return r;
     fwd = 1;
   }
-  const bool merge = ctx->next_final >= 0 && ctx->allow_merge && ctx->P + 2 * B <= ctx->mc.max_seq;
+  const bool merge = ctx->next_final >= 0 && allow_merge && ctx->P + 2 * B <= ctx->mc.max_seq;
   cudaGraphExec_t g = merge ? ctx->merged_exec
                             : ctx->step_execs[ctx->next_final >= 0 ? 1 : ctx->next_nv];
   CK(cudaGraphLaunch(g, ctx->stream));
@@ -718,7 +717,7 @@ int lopa_prefill(lopa_ctx* ctx, const int32_t* prompt, int n) {
 
 int lopa_step(lopa_ctx* ctx, lopa_step_result* out) {
   if (!ctx) return fail(nullptr, LOPA_ERR_INVALID_ARG, "ctx is null");
-  return step_impl(ctx, out);
+  return step_impl(ctx, out, /*allow_merge=*/true);
 }
 
 int lopa_decode(lopa_ctx* ctx, int gen_len, int32_t* out_tokens, lopa_stats* out) {
@@ -735,22 +734,16 @@ int lopa_decode(lopa_ctx* ctx, int gen_len, int32_t* out_tokens, lopa_stats* out
   for (int b = 0; b < gen_len / B; ++b) {
     int iters = 0;
     // The last block of this decode does not start the block after it.
-    ctx->allow_merge = b + 1 < gen_len / B;
+    const bool allow_merge = b + 1 < gen_len / B;
     while (true) {
       lopa_step_result r;
-      int rc = step_impl(ctx, &r);
-      ctx->allow_merge = true;
+      int rc = step_impl(ctx, &r, allow_merge);
       if (rc) return rc;
-      ctx->allow_merge = b + 1 < gen_len / B;
       st.forwards += r.forwards;
       st.steps += 1;
       if (r.block_done) break;
-      if (++iters > B) {
-        ctx->allow_merge = true;
-        return fail(ctx, LOPA_ERR_BAD_STATE, "block did not finish within %d iterations", B);
-      }
+      if (++iters > B) return fail(ctx, LOPA_ERR_BAD_STATE, "block did not finish within %d iterations", B);
     }
-    ctx->allow_merge = true;
     st.blocks += 1;
     st.tokens += B;
   }
