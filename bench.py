@@ -47,6 +47,30 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def replica_barrier(world: int):
+    """Barrier over the replicas (gloo), a no-op for one process."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(seconds: float, world: int) -> float:
+    """The job's time: the slowest replica's (every rank gets the same value)."""
+    if world <= 1:
+        return seconds
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([seconds], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, seconds: float) -> float:
+    """Whole-job tokens/s: every replica decodes the same workload (weak scaling), and the
+    job ends with the slowest one."""
+    return world * tokens_per_rank / seconds
+
+
 class ClockSampler:
     """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -291,13 +315,8 @@ def main():
         one_step()
     stats = []
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
     with ClockSampler(local) as clocks:
-        barrier()
+        replica_barrier(world)
         torch.cuda.synchronize()
         ev0 = torch.cuda.Event(enable_timing=True)
         ev1 = torch.cuda.Event(enable_timing=True)
@@ -307,18 +326,13 @@ def main():
             stats.append(st)
         ev1.record(dec.stream)
         torch.cuda.synchronize()
-        barrier()
-    elapsed = ev0.elapsed_time(ev1) / 1e3
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+        replica_barrier(world)
+    elapsed = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world)
     forwards = sum(s["forwards"] for s in stats)
     iters = sum(s["steps"] for s in stats)
     blocks = sum(s["blocks"] for s in stats)
     tokens = sum(s["tokens"] for s in stats)
-    value = world * tokens / elapsed
+    value = job_throughput(tokens, world, elapsed)
     tpf = tokens / forwards
     ms_per_forward = elapsed * 1e3 / forwards
     # per layer: q/k/v, attention, O, residual+norm, gate/up, down, residual+norm; then
@@ -386,6 +400,7 @@ def main():
     import torch as _t
     pin_prompt = _t.from_numpy(prompt.astype(np.int32)).pin_memory()
     e2e_times = []
+    replica_barrier(world)
     for _ in range(max(1, args.e2e_steps)):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
@@ -394,7 +409,8 @@ def main():
         e2e_times.append(time.perf_counter() - t0)
     from diffusion_lookahead_decoding_gb300 import _lib as L
     d2h = gen * 4 + int(st_e["steps"]) * C.sizeof(L.StepResult)
-    e2e = {"value": world * gen / statistics.mean(e2e_times), "unit": UNIT,
+    e2e_s = max_over_ranks(statistics.mean(e2e_times), world)
+    e2e = {"value": job_throughput(gen, world, e2e_s), "unit": UNIT,
            "h2d_bytes_per_step": P0 * 4, "d2h_bytes_per_step": d2h,
            "includes": "prefill of the prompt + full decode per step"}
 

@@ -1,6 +1,6 @@
 """Host-side accounting of the benchmark, without a GPU: the algorithmic bytes and flops
-its roofline fractions divide by, and the reference arm's output line (the oracle timed
-on the host cores) on the tiny workload."""
+its roofline fractions divide by, the reference arm's output line (the oracle timed on
+the host cores) on the tiny workload, and the replica path's timing over two gloo ranks."""
 import json
 import os
 import subprocess
@@ -79,3 +79,43 @@ def test_reference_arm_other_ranks_exit_quietly():
                    env_extra={"RANK": "1", "LOCAL_RANK": "1", "WORLD_SIZE": "2"}, timeout=120)
     assert r.returncode == 0, r.stderr[-2000:]
     assert not [l for l in r.stdout.splitlines() if l.startswith("{")]
+
+
+def _replica(rank, world, port, seconds, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.replica_barrier(world)
+        t = bench.max_over_ranks(seconds[rank], world)
+        out.put((rank, t, bench.job_throughput(256, world, t)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replicas_report_the_slowest_rank_over_gloo():
+    """Two CPU ranks (gloo, world size 2): both see the slower rank's time, and the job's
+    tokens/s counts both replicas' tokens over it."""
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    seconds = [0.5, 0.8]
+    procs = [ctx.Process(target=_replica, args=(r, 2, port, seconds, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [g[1] for g in got] == [0.8, 0.8]
+    assert all(abs(g[2] - 2 * 256 / 0.8) < 1e-9 for g in got)
+
+
+def test_single_process_needs_no_process_group():
+    assert bench.max_over_ranks(0.25, 1) == 0.25
+    bench.replica_barrier(1)
+    assert bench.job_throughput(256, 1, 0.5) == 512.0
