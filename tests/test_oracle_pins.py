@@ -306,6 +306,78 @@ def _greedy_token_of_step(st, c):
     return st.branches[b][c]
 
 
+# ------------------------------------------------ the completing iteration (merged start)
+def _completing_states(block, k, mask, seed):
+    """Block states whose next iteration completes the block: every masked position
+    reaches tau (the anchor completes it), or exactly one stays below tau after the anchor
+    fill (lookahead branch 1 completes it, when k >= 1)."""
+    rng = np.random.default_rng(seed)
+    for case in range(12):
+        tok = rng.integers(1, MICRO.vocab, block)
+        tok[tok == mask] = 1
+        am = rng.integers(1, MICRO.vocab, block)
+        am[am == mask] = 1
+        mp = rng.uniform(0.2, 0.99, block)
+        masked = rng.choice(block, size=1 + case % 3, replace=False)
+        tok[masked] = mask
+        mp[masked] = 0.95
+        via = "anchor"
+        if case % 2 and k >= 1:
+            free = np.setdiff1d(np.arange(block), masked)
+            j = int(rng.choice(free))
+            tok[j], mp[j] = mask, 0.5
+            via = "lookahead"
+        yield tok, am, mp, via
+
+
+@pytest.mark.parametrize("k", [0, 1, 3])
+def test_completing_iteration_winner_is_known_before_the_forward(micro_w, k):
+    """When the anchor fill leaves nothing masked, or leaves one position that lookahead
+    branch 1 fills, that branch scores exactly 1.0 and every other branch less, whatever
+    the forward returns: the oracle's full iteration picks it (anchor, else branch 1)."""
+    m = O.OracleModel(MICRO, micro_w, act="fp64")
+    prompt = synth.make_prompt(MICRO, 10, seed=4)
+    block, tau, mask = 6, 0.9, MICRO.mask_id
+    cache = O.prefill(m, prompt, len(prompt) + block)
+    n = 0
+    for tok, am, mp, via in _completing_states(block, k, mask, seed=21 + k):
+        st = O.lopa_step(m, cache, len(prompt), tok, am, mp, k, tau)
+        want = 0 if via == "anchor" else 1
+        assert st.winner == want
+        assert st.conf[want] == 1.0
+        assert all(c < 1.0 for b, c in enumerate(st.conf) if b != want)
+        assert not (st.branches[want] == mask).any()
+        n += 1
+    assert n == 12
+
+
+def test_merged_block_start_equals_commit_then_start(micro_w):
+    """The next block's first logits computed in the completing iteration's pass - the
+    finished block and the all-[MASK] next block in one block-causal forward, positions
+    running on - equal the oracle's order: commit the finished block, then the next
+    block's block-start forward.  The joint pass is the independent torch forward with
+    a block-causal mask; both in float64."""
+    m = O.OracleModel(MICRO, micro_w, act="fp64")
+    prompt = synth.make_prompt(MICRO, 10, seed=5)
+    P, block, mask = len(prompt), 6, MICRO.mask_id
+    finished = synth.make_prompt(MICRO, block, seed=6)
+    finished[finished == mask] = 1
+    blank = np.full(block, mask)
+    cache = O.prefill(m, prompt, P + 2 * block)
+    out1 = O.forward(m, cache, P, finished[None, :])
+    for l in range(MICRO.n_layers):
+        cache.k[l][P:P + block] = out1.block_k[l][0]
+        cache.v[l][P:P + block] = out1.block_v[l][0]
+    out2 = O.forward(m, cache, P + block, blank[None, :])
+    positions, visible = block_layout(P, 2, block, 0)
+    seq = np.concatenate([prompt, finished, blank])
+    z, _, _, _ = torch_forward(micro_w, MICRO, seq, positions, visible)
+    for rows, ref in ((slice(P, P + block), out1), (slice(P + block, P + 2 * block), out2)):
+        p = torch.softmax(z[rows], dim=-1)
+        np.testing.assert_array_equal(torch.argmax(z[rows], dim=-1).numpy(), ref.am[0])
+        np.testing.assert_allclose(p.max(dim=-1).values.numpy(), ref.mp[0], rtol=1e-10)
+
+
 # ------------------------------------------------------------- planted mistakes
 def _planted(monkeypatch, name, fn):
     monkeypatch.setattr(OL, name, fn)
