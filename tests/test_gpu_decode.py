@@ -12,8 +12,8 @@ import pytest
 
 from oracle import lopa_oracle as O
 from diffusion_lookahead_decoding_gb300 import synth
-from tests.gpu_util import (f32, make_decoder, oracle_forward_pair, rel_l2, seeded_branches,
-                            tokens_ok, workload_weights)
+from tests.gpu_util import (device_weights, f32, make_decoder, oracle_forward_pair, rel_l2,
+                            seeded_branches, tokens_ok, workload_weights)
 
 pytestmark = pytest.mark.gpu
 WORKLOADS = ["tiny", "small", "heads128"]
@@ -160,6 +160,32 @@ def test_decode_trajectory_matches_oracle(name, k):
     margins = [min(st.margins.values()) for (P, st) in log if P <= blk_start]
     print(f"diverged at token {div}; smallest oracle margin up to that block {min(margins):.2e} "
           f"(tie window {cond.tie:.1e})")
+    assert min(margins) < cond.tie, "diverged without an oracle near-tie"
+
+
+def test_decode_at_the_maximum_block_and_branch_count():
+    """The largest block (64) and branch count (16: k = 15) the ABI accepts, on the tiny
+    model: 1024 token rows per verification forward, every decision kernel at full width.
+    The decode matches the oracle's, or diverges only after an oracle near-tie."""
+    from diffusion_lookahead_decoding_gb300 import api
+    shape, dshape, w = workload_weights("tiny")
+    B, k, P, gen = 64, 15, dshape.prompt_len, 128
+    dec = api.LopaDecoder(shape, device_weights("tiny"), B, k, dshape.tau, P, P + gen)
+    prompt = synth.make_prompt(shape, P, seed=1)
+    dec.prefill(prompt)
+    toks, stats = dec.decode(gen)
+    cond = oracle_forward_pair(shape, w, prompt, seeded_branches(shape, 2, B, seed=5), P + B)[3]
+    m = O.OracleModel(shape, w, act="bf16")
+    otoks, ofw, _, log = O.decode(m, prompt, B, k, dshape.tau, gen, record=True)
+    print(f"B=64 k=15: GPU {stats['forwards']} passes, oracle {ofw} forwards; {cond}")
+    assert stats["tokens"] == gen and stats["blocks"] == gen // B
+    assert (toks != shape.mask_id).all()
+    div = _first_divergence(toks, otoks)
+    if div is None:
+        assert stats["forwards"] == ofw - (gen // B - 1)
+        return
+    blk_start = P + (div // B) * B
+    margins = [min(st.margins.values()) for (Pb, st) in log if Pb <= blk_start]
     assert min(margins) < cond.tie, "diverged without an oracle near-tie"
 
 
