@@ -15,11 +15,12 @@
  *   - Return 0 (LOPA_OK) on success or a negative LOPA_ERR_* code, with a message in
  *     lopa_last_error().  Argument and state errors (INVALID_ARG, BAD_STATE,
  *     UNSUPPORTED) are detected before any work is enqueued and leave the decoding state
- *     as it was.  A CUDA error or a device timeout in the middle of an iteration or a
- *     decode can leave the block state and the cache beyond the committed prefix
- *     partly updated: lopa_rewind (or lopa_prefill) brings the context back to a block
- *     boundary.  No call aborts the process or traps the device: device-side waits are
- *     bounded and report LOPA_ERR_DEVICE_TIMEOUT.
+ *     as it was.  A device timeout (or a non-sticky CUDA error) in the middle of an
+ *     iteration or a decode can leave the block state and the cache beyond the committed
+ *     prefix partly updated: lopa_rewind (or lopa_prefill) brings the context back to a
+ *     block boundary.  A sticky CUDA error (a device fault) leaves the CUDA context, and
+ *     with it the lopa_ctx, unusable.  No call aborts the process or traps the device:
+ *     device-side waits are bounded and report LOPA_ERR_DEVICE_TIMEOUT.
  *   - "device" pointers are CUDA global-memory pointers on the current device;
  *     "host" pointers are ordinary CPU memory.  bf16 = IEEE bfloat16 stored as
  *     16-bit words.  All matrices are row-major.
