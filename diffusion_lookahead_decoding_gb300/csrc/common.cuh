@@ -92,16 +92,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint3
       "l"(map), "r"(bar), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
-// As tma_load_2d, delivered to the same shared-memory offset (and completing the mbarrier
-// at the same offset) in every CTA of the cluster set in cta_mask.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* map, uint32_t bar, int x,
-                                               int y, uint16_t cta_mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
-      "l"(map), "r"(bar), "r"(x), "r"(y), "h"(cta_mask), "l"(policy)
-      : "memory");
-}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -149,14 +139,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
-// As mma_commit, arriving on the mbarrier at the same offset in every CTA of cta_mask.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
 // Store 16 consecutive fp32 columns of this thread's TMEM lane (32x32b shape); the
 // stores are complete once tmem_st_wait returns.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {

@@ -55,7 +55,7 @@ struct SmemTail {
   int abort;
 };
 
-template <int MODE, bool PAIR = false>
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const GemmArgs a) {
@@ -76,7 +76,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool a_ok[2];
   int b_row;
   constexpr bool kCluster = MODE == GEMM_QKV;
-  constexpr bool paired = PAIR && MODE == GEMM_RED_ADD;  // a separate instantiation
   if (MODE == GEMM_RED_ADD || kCluster) {
     a_row[0] = blockIdx.x * a.na * 128;
     a_row[1] = a_row[0] + 128;
@@ -109,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < SX; ++s) {
       mbar_init(smem_u32(&tail->xfull[s]), 1);
-      mbar_init(smem_u32(&tail->xempty[s]), paired ? 2 : 1);  // paired: both CTAs' MMAs
+      mbar_init(smem_u32(&tail->xempty[s]), 1);
     }
     mbar_init(smem_u32(&tail->accf), 1);
     if (kCluster) mbar_init(smem_u32(&tail->cfull), a.splits);
@@ -125,19 +124,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (kCluster || paired) cluster_arrive_relaxed();  // this CTA's mbarriers are initialised
+  if (kCluster) cluster_arrive_relaxed();  // this CTA's mbarriers are initialised
   const uint32_t tmem = tail->tmem_addr;
   volatile int* abort = &tail->abort;
   pdl_trigger();
 
-  // Paired CTAs (cluster of 2 along x): each loads half of the activation tile and
-  // multicasts it to both; an activation slot is refilled only after both CTAs' MMAs
-  // released it (xempty counts two arrivals, committed to both CTAs).
-  const uint32_t crank = paired ? cluster_ctarank() : 0u;
   if (warp == 0 || warp == 2 + kEpiWarps) {
     // Producers: warp 0 streams the weight operand, the last warp the activation operand.
     const bool weights = warp == 0;
-    if (paired && !weights) cluster_wait();  // the peer's mbarriers are initialised
     if (lane == 0) {
       if (!weights) pdl_wait();  // activations are written by the previous kernel
       const int S = weights ? SW : SX;
@@ -166,10 +160,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int y1 = packed ? ((a_row[1] >> 7) * a.k_blocks + kb) * 128 : a_row[1];
           if (a_ok[0]) tma_load_2d(dst, &mapA, fb, kx, y0, pol);
           if (a_ok[1]) tma_load_2d(dst + a.a_tile_bytes, &mapA, fb, kx, y1, pol);
-        } else if (paired) {
-          const int hb = a.nbox / 2;  // rows of each CTA's half
-          tma_load_2d_mc(dst + crank * (uint32_t)hb * 128u, &mapB, fb, kx, b_row + (int)crank * hb,
-                         (uint16_t)0x3, pol);
         } else {
           const int y = packed ? ((b_row / a.nbox) * a.k_blocks + kb) * a.nbox : b_row;
           tma_load_2d(dst, &mapB, fb, kx, y, pol);
@@ -177,7 +167,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (paired) cluster_wait();  // the peer's mbarriers are initialised
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(128, a.nbox);
       bool ok = true;
@@ -206,10 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         mma_commit(smem_u32(&tail->wempty[sw]));
-        if (paired)
-          mma_commit_mc(smem_u32(&tail->xempty[sx]), (uint16_t)0x3);
-        else
-          mma_commit(smem_u32(&tail->xempty[sx]));
+        mma_commit(smem_u32(&tail->xempty[sx]));
       }
       if (ok) mma_commit(smem_u32(&tail->accf));
     }
@@ -527,14 +513,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  if (paired) {
-    // Neither CTA leaves while the other may still signal or fill its shared memory:
-    // every MMA of both has completed once both pass this point (their accumulators were
-    // waited for), so all cross-CTA arrivals and copies have landed.
-    if (warp != 1 && warp != 2 + kEpiWarps) cluster_wait();  // (closes the start phase)
-    cluster_arrive_release();
-    cluster_wait();
-  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -600,15 +578,14 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 
 int gemm_max_smem() { return kMaxSmem; }
 
-template <int MODE, bool PAIR = false>
+template <int MODE>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(gemm_kernel<MODE, PAIR>);
+  return reinterpret_cast<const void*>(gemm_kernel<MODE>);
 }
 
-// Indexed by mode; the paired split-K instantiation last.
+// Indexed by mode.
 const void* const kKernels[] = {kernel_ptr<GEMM_RED_ADD>(), kernel_ptr<GEMM_SWIGLU>(),
-                                kernel_ptr<GEMM_LMSTATS>(), kernel_ptr<GEMM_QKV>(),
-                                kernel_ptr<GEMM_RED_ADD, true>()};
+                                kernel_ptr<GEMM_LMSTATS>(), kernel_ptr<GEMM_QKV>()};
 
 cudaError_t gemm_set_smem_limits() {
   for (const void* k : kKernels) {
@@ -651,7 +628,7 @@ int gemm_cluster_capacity(int mode, int cs, size_t smem) {
 // act: [act_rows_alloc][K] bf16 activations (T valid rows); w: [n_rows_w][K] bf16.
 const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_alloc, int T,
                       const void* w, int n_rows_w, int K, int na, int splits, int tok_box,
-                      int num_sms, bool w_packed, bool pair) {
+                      int num_sms, bool w_packed) {
   static thread_local char err[256];
   // Packed weights are viewed as [tiles * K/64 * tile_rows][64]: one box = one tile.
   auto weight_map = [&](CUtensorMap* map, int tile_rows) {
@@ -697,16 +674,9 @@ const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_all
       a.splits = a.k_blocks;
     }
     if (!weight_map(&L->mapA, 128)) return err;
-    if (!make_tmap_bf16(&L->mapB, act, act_rows_alloc, K, pair ? tok_box / 2 : tok_box, err,
-                        sizeof(err)))
-      return err;
+    if (!make_tmap_bf16(&L->mapB, act, act_rows_alloc, K, tok_box, err, sizeof(err))) return err;
     const int gx = (mode == GEMM_SWIGLU) ? (n_rows_w / 2) / 128 : (n_rows_w + a.na * 128 - 1) / (a.na * 128);
     L->grid = dim3(gx, a.splits, (T + tok_box - 1) / tok_box);
-    if (pair) {
-      if (mode != GEMM_RED_ADD || a.na != 1 || gx % 2 != 0)
-        return "paired GEMM needs the split-K mode, one 128-row tile per CTA, an even tile count";
-      a.pair = 1;
-    }
     a.w_slot_bytes = round1k(a.na * a.a_tile_bytes);
     a.x_slot_bytes = round1k(a.nbox * 128);
   }
@@ -730,9 +700,6 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s) {
   const dim3 blk(kThreads);
   switch (L.args.mode) {
     case GEMM_RED_ADD:
-      if (L.args.pair)
-        return launch_pdl_cluster(gemm_kernel<GEMM_RED_ADD, true>, L.grid, blk, L.smem, s,
-                                  dim3(2, 1, 1), L.mapA, L.mapB, L.args);
       return launch_pdl(gemm_kernel<GEMM_RED_ADD>, L.grid, blk, L.smem, s, L.mapA, L.mapB, L.args);
     case GEMM_SWIGLU:
       return launch_pdl(gemm_kernel<GEMM_SWIGLU>, L.grid, blk, L.smem, s, L.mapA, L.mapB, L.args);

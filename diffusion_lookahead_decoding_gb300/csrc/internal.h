@@ -81,8 +81,6 @@ struct GemmArgs {
   float scale;       // LMSTATS logit scale
   float* out_f32;    int ldo;
   int atomic;        // RED_ADD: 1 = atomicAdd into out_f32, 0 = store partial of split y
-  int pair;          // RED_ADD: CTAs 2i, 2i+1 form a cluster sharing the activation tile
-                     // (each loads half and multicasts it); grid.x even, na = 1
   size_t split_stride;  // RED_ADD partials: elements between splits
   bf16* out_bf16;    int ldh;
   float* part_m; float* part_s; int* part_i; int part_ld;
@@ -116,11 +114,10 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 
 // Fills `L` for one GEMM.  Returns an empty string on success, else a reason.  With
 // w_packed the weight is in the tile-major layout written by launch_pack_tiles (tiles of
-// 128 rows, 256 for the LM head); otherwise it is row-major [n_rows_w][K].  With pair
-// (RED_ADD, na = 1, even tile count) neighbouring CTAs share the activation tile.
+// 128 rows, 256 for the LM head); otherwise it is row-major [n_rows_w][K].
 const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_alloc, int T,
                       const void* w, int n_rows_w, int K, int na, int splits, int tok_box,
-                      int num_sms, bool w_packed = false, bool pair = false);
+                      int num_sms, bool w_packed = false);
 
 // Tile-major weight packing: [rows][K] row-major -> [ceil(rows/tile_rows)][K/64][tile_rows][64].
 size_t packed_elems(int rows, int K, int tile_rows);

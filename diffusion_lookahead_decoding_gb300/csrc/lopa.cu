@@ -172,19 +172,13 @@ int pick_splits(int tiles, int k_blocks, int num_sms) {
   return std::max(s, 1);
 }
 
-// Tiling of a split-K projection over T token rows: weight tiles (128 rows) per CTA, the
-// split count, and whether neighbouring CTAs pair up to share the activation tile.  Paired
-// CTAs (one tile each, even tile count) give twice the tiles of two tiles per CTA, hence
-// half the splits and half the partial sums at the same activation traffic; but a pair
-// refills an activation slot only when both have used it, so the slower weight stream
-// gates both.  That pays for a short K range per CTA (the output projection), not for a
-// long one (the down projection): allow_pair selects it.
-void proj_tiling(int nrows, int K, int T, int num_sms, bool allow_pair, int* na, int* splits,
-                 bool* pair) {
+// Tiling of a split-K projection over T token rows: weight tiles (128 rows) per CTA and the
+// split count.  Two tiles per CTA halve the activation traffic from L2 per weight byte (the
+// token tile is loaded once for both); the split count then fills the SMs.
+void proj_tiling(int nrows, int K, int T, int num_sms, int* na, int* splits) {
   const int tok_box = std::min(256, round16(T));
   const int zt = (T + tok_box - 1) / tok_box;
-  *pair = allow_pair && (nrows / 128) % 2 == 0;
-  *na = (*pair || nrows < 256) ? 1 : 2;
+  *na = nrows < 256 ? 1 : 2;
   const int tiles = ((nrows + *na * 128 - 1) / (*na * 128)) * zt;
   *splits = pick_splits(tiles, K / 64, num_sms);
 }
@@ -196,8 +190,7 @@ size_t partial_floats(const lopa_ctx* ctx, int T) {
   size_t need = 0;
   for (int i = 0; i < 2; ++i) {
     int na, splits;
-    bool pair;
-    proj_tiling(m.d_model, Ks[i], T, ctx->num_sms, i == 0, &na, &splits, &pair);
+    proj_tiling(m.d_model, Ks[i], T, ctx->num_sms, &na, &splits);
     need = std::max(need, (size_t)splits * T * m.d_model);
   }
   return need;
@@ -247,17 +240,16 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
   p.gu.resize(L);
   p.dn.resize(L);
   auto plan = [&](GemmLaunch& G, int mode, const void* act, int K, const void* w, int nrows,
-                  const char* what, bool allow_pair = false) -> int {
+                  const char* what) -> int {
     int na = 2, splits = 1;
-    bool pair = false;
     if (mode == GEMM_QKV) {
       qkv_tiling(ctx, nrows, K, p.T, &na, &splits);
     } else if (mode == GEMM_RED_ADD) {
-      proj_tiling(nrows, K, p.T, ctx->num_sms, allow_pair, &na, &splits, &pair);
+      proj_tiling(nrows, K, p.T, ctx->num_sms, &na, &splits);
       while (splits > 1 && (size_t)splits * p.T * nrows > ctx->part_floats) --splits;
     }
     const char* e = plan_gemm(&G, mode, act, ctx->Tmax, p.T, w, nrows, K, na, splits, p.tok_box,
-                              ctx->num_sms, /*w_packed=*/true, pair);
+                              ctx->num_sms, /*w_packed=*/true);
     if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s GEMM: %s", what, e);
     if (mode == GEMM_RED_ADD) {
       if ((size_t)G.args.splits * p.T * nrows > ctx->part_floats)
@@ -315,7 +307,7 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
     aa.err = &ctx->st->err;
     const char* ea = plan_attention(&p.attn[l], aa, dh, m.max_seq, ctx->vt_ld);
     if (ea[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s", ea);
-    if ((r = plan(p.o[l], GEMM_RED_ADD, ctx->attn, H * dh, ctx->wo[l], d, "o", true))) return r;
+    if ((r = plan(p.o[l], GEMM_RED_ADD, ctx->attn, H * dh, ctx->wo[l], d, "o"))) return r;
     if ((r = plan(p.gu[l], GEMM_SWIGLU, ctx->n, d, ctx->wgu[l], 2 * F, "gate/up"))) return r;
     p.gu[l].args.out_bf16 = ctx->hm;
     p.gu[l].args.ldh = F;
