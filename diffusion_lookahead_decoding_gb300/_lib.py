@@ -28,11 +28,12 @@ class ModelConfig(C.Structure):
                 ("rope_base", C.c_float), ("rms_eps", C.c_float), ("logit_scale", C.c_float)]
 
 
+LAYER_WEIGHTS = ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "wg", "wu", "wd")
+
+
 class Weights(C.Structure):
-    _fields_ = [("embed", C.c_void_p), ("lm_head", C.c_void_p), ("final_norm", C.c_void_p),
-                ("attn_norm", C.POINTER(C.c_void_p)), ("wqkv", C.POINTER(C.c_void_p)),
-                ("wo", C.POINTER(C.c_void_p)), ("mlp_norm", C.POINTER(C.c_void_p)),
-                ("wgu", C.POINTER(C.c_void_p)), ("wd", C.POINTER(C.c_void_p))]
+    _fields_ = [("embed", C.c_void_p), ("lm_head", C.c_void_p), ("final_norm", C.c_void_p)] + [
+        (name, C.POINTER(C.c_void_p)) for name in LAYER_WEIGHTS]
 
 
 class DecodeConfig(C.Structure):
@@ -88,6 +89,9 @@ SIGNATURES = {
     "lopa_branch_attention": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
                                         C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                         C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
+    "lopa_kernel_status": (C.c_int, [C.c_void_p]),
+    "lopa_set_wait_limit_ns": (C.c_int, [C.c_ulonglong]),
+    "lopa_debug_set_device_error": (C.c_int, [C.c_void_p, C.c_int]),
 }
 
 _lib = None

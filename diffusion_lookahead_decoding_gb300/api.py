@@ -33,27 +33,12 @@ class StepOutcome:
 
 
 def upload_weights(shape, weights: dict, device="cuda") -> dict:
-    """Moves generated CPU weights to the device in the library's fused layouts:
-    wqkv = [wq; wk; wv] and wgu = [wg; wu] (row-concatenated)."""
-    dev = {}
+    """Moves generated CPU weights (bf16, nn.Linear layout) to the device, one tensor per
+    matrix as lopa_weights takes them."""
     bf = torch.bfloat16
-
-    def put(t):
-        return t.to(device=device, dtype=bf).contiguous()
-
-    dev["embed"] = put(weights["embed"])
-    dev["lm_head"] = put(weights["lm_head"])
-    dev["final_norm"] = put(weights["final_norm"])
-    for l in range(shape.n_layers):
-        dev[f"wqkv.{l}"] = torch.cat([put(weights[f"wq.{l}"]), put(weights[f"wk.{l}"]),
-                                      put(weights[f"wv.{l}"])], dim=0).contiguous()
-        dev[f"wo.{l}"] = put(weights[f"wo.{l}"])
-        dev[f"wgu.{l}"] = torch.cat([put(weights[f"wg.{l}"]), put(weights[f"wu.{l}"])],
-                                    dim=0).contiguous()
-        dev[f"wd.{l}"] = put(weights[f"wd.{l}"])
-        dev[f"attn_norm.{l}"] = put(weights[f"attn_norm.{l}"])
-        dev[f"mlp_norm.{l}"] = put(weights[f"mlp_norm.{l}"])
-    return dev
+    names = ["embed", "lm_head", "final_norm"] + [f"{n}.{l}" for l in range(shape.n_layers)
+                                                  for n in L.LAYER_WEIGHTS]
+    return {n: weights[n].to(device=device, dtype=bf).contiguous() for n in names}
 
 
 class LopaDecoder:
@@ -72,13 +57,11 @@ class LopaDecoder:
                            shape.rope_base, shape.rms_eps, shape.logit_scale)
         n = shape.n_layers
         arr = lambda key: (C.c_void_p * n)(*[dev_weights[f"{key}.{l}"].data_ptr() for l in range(n)])
-        self._arrays = {k_: arr(k_) for k_ in ("attn_norm", "wqkv", "wo", "mlp_norm", "wgu", "wd")}
+        self._arrays = {k_: arr(k_) for k_ in L.LAYER_WEIGHTS}
         cast = lambda a: C.cast(a, C.POINTER(C.c_void_p))
         w = L.Weights(dev_weights["embed"].data_ptr(), dev_weights["lm_head"].data_ptr(),
-                      dev_weights["final_norm"].data_ptr(), cast(self._arrays["attn_norm"]),
-                      cast(self._arrays["wqkv"]), cast(self._arrays["wo"]),
-                      cast(self._arrays["mlp_norm"]), cast(self._arrays["wgu"]),
-                      cast(self._arrays["wd"]))
+                      dev_weights["final_norm"].data_ptr(),
+                      *[cast(self._arrays[k_]) for k_ in L.LAYER_WEIGHTS])
         dc = L.DecodeConfig(block, k, tau, max_prompt)
         ctx = C.c_void_p()
         torch.cuda.synchronize()
@@ -169,6 +152,10 @@ class LopaDecoder:
                                              v.ctypes.data_as(C.POINTER(C.c_uint16))), self.ctx)
         return bf16_words_to_f64(k), bf16_words_to_f64(v)
 
+    def debug_set_device_error(self, code: int):
+        """Test hook: plants `code` in the context's device error word."""
+        L.check(self.lib.lopa_debug_set_device_error(self.ctx, code), self.ctx)
+
     def close(self):
         if getattr(self, "ctx", None):
             self.lib.lopa_free(self.ctx)
@@ -188,6 +175,17 @@ def bf16_words_to_f64(words: np.ndarray) -> np.ndarray:
 # -- kernel-level calls (device tensors, current torch stream) ---------------------------
 def _stream_ptr():
     return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def kernel_status():
+    """Synchronizes the current stream; raises LopaError(DEVICE_TIMEOUT) when a device-side
+    wait of a kernel-level call gave up since the last check."""
+    L.check(L.load().lopa_kernel_status(_stream_ptr()))
+
+
+def set_wait_limit_ns(ns: int):
+    """Test hook: device-side wait limit of later kernel-level calls (0 = default)."""
+    L.check(L.load().lopa_set_wait_limit_ns(int(ns)))
 
 
 def linear_accumulate(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor):

@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liblopa.so")
-SOURCES = ["gemm.cu", "attention.cu", "pointwise.cu", "decide.cu", "pack.cu", "lmhead_static.cu", "lopa.cu"]
+SOURCES = ["gemm.cu", "attention.cu", "pointwise.cu", "decide.cu", "pack.cu", "lmhead_static.cu", "status.cu", "lopa.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(os.path.dirname(HERE), "include")]

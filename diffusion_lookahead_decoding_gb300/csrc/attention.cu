@@ -108,6 +108,9 @@ struct TcTail {
   uint64_t kvfull[kTcStages], kvempty[kTcStages];
   uint64_t sfull[2], pfull[2], pempty[2];
   uint64_t odone;
+  uint64_t drain;  // after a wait gave up: completion of every MMA this CTA issued
+  int kv_issued;   // K / V^T stages loaded by TMA
+  int mma_issued;  // 1 once an MMA was issued
   float xmax[2][2][kTcRows];  // [buffer][key half][row]: half-row maxima
   float xsum[2][kTcRows];     // [key half][row]: half-row sums of P
   uint32_t tmem;
@@ -219,7 +222,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(smem_u32(&tail->pempty[s]), 1);
     }
     mbar_init(smem_u32(&tail->odone), 1);
+    mbar_init(smem_u32(&tail->drain), 1);
     tail->abort = 0;
+    tail->kv_issued = 0;
+    tail->mma_issued = 0;
     fence_mbar_init();
     tma_prefetch_desc(&m.kc);
     tma_prefetch_desc(&m.vtc);
@@ -239,15 +245,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   pdl_wait();  // q and the block keys come from the previous kernel; out may be read by it
   const KeySched ks = key_sched<kTcKeys>(a, b_lo, b_hi);
   const int n = ks.n_pre + ks.n_br;
+  const uint64_t lim = wait_limit(a.wait_ns);
 
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t keep = policy_evict_last();
+      int issued = 0;
       for (int j = 0; j < n; ++j) {
         const int s = j % kTcStages;
         if (j >= kTcStages &&
             !mbar_wait_bounded(smem_u32(&tail->kvempty[s]), (uint32_t)(j / kTcStages - 1) & 1u,
-                               abort, a.err, DEV_TIMEOUT_PRODUCER))
+                               abort, a.err, DEV_TIMEOUT_PRODUCER, lim))
           break;
         const uint32_t fb = smem_u32(&tail->kvfull[s]);
         const uint32_t kdst = smem_u32(smem + s * kTcStageBytes);
@@ -261,7 +269,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_load_2d(kdst + kTcAtom, km, fb, g * 128 + 64, k0, keep);
         tma_load_2d(vdst, vm, fb, k0, g * 128, keep);
         tma_load_2d(vdst + kTcAtom, vm, fb, k0 + 64, g * 128, keep);
+        ++issued;
       }
+      tail->kv_issued = issued;
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -269,16 +279,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // P_{j-1} V_{j-1} has finished reading.
       const uint32_t idesc_s = idesc_bf16(128, kTcKeys);
       const uint32_t idesc_o = idesc_bf16(128, 128);
-      bool ok = mbar_wait_bounded(smem_u32(&tail->qfull), 0, abort, a.err, DEV_TIMEOUT_MMA);
+      bool ok = mbar_wait_bounded(smem_u32(&tail->qfull), 0, abort, a.err, DEV_TIMEOUT_MMA, lim);
       auto issue_s = [&](int j) {
         const int s = j % kTcStages, sb = j & 1;
         ok = ok && mbar_wait_bounded(smem_u32(&tail->kvfull[s]), (uint32_t)(j / kTcStages) & 1u,
-                                     abort, a.err, DEV_TIMEOUT_MMA);
+                                     abort, a.err, DEV_TIMEOUT_MMA, lim);
         ok = ok && (j < 2 || mbar_wait_bounded(smem_u32(&tail->pempty[sb]),
                                                (uint32_t)((j >> 1) - 1) & 1u, abort, a.err,
-                                               DEV_TIMEOUT_MMA));
+                                               DEV_TIMEOUT_MMA, lim));
         if (!ok) return;
         tc_fence_after();
+        tail->mma_issued = 1;
         const uint32_t kbase = smem_u32(smem + s * kTcStageBytes);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -295,7 +306,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (i + 1 < n) issue_s(i + 1);
         const int pb = i & 1, si = i % kTcStages;
         ok = ok && mbar_wait_bounded(smem_u32(&tail->pfull[pb]), (uint32_t)(i >> 1) & 1u, abort,
-                                     a.err, DEV_TIMEOUT_MMA);
+                                     a.err, DEV_TIMEOUT_MMA, lim);
         if (!ok) break;
         tc_fence_after();
         const uint32_t vbase = smem_u32(smem + si * kTcStageBytes + kTcKBytes);
@@ -359,7 +370,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory"); };
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       ok = ok && __all_sync(kAll, mbar_wait_bounded(smem_u32(bar), parity, abort, a.err,
-                                                    DEV_TIMEOUT_EPILOGUE));
+                                                    DEV_TIMEOUT_EPILOGUE, lim));
     };
     for (int j = 0; j < n; ++j) {
       const int sb = j & 1;
@@ -459,7 +470,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Epilogue: out row = O / l in bf16 (a row that saw no key is written as zeros); l is
     // the sum of the two half-row sums, which share the row's reference maximum.
     const bool got = ok && n > 0 &&
-                     mbar_wait_bounded(smem_u32(&tail->odone), 0, abort, a.err, DEV_TIMEOUT_EPILOGUE);
+                     mbar_wait_bounded(smem_u32(&tail->odone), 0, abort, a.err, DEV_TIMEOUT_EPILOGUE,
+                                       lim);
     const bool have_o = __all_sync(kAll, got);
     tc_fence_after();
     tail->xsum[h][r] = l;
@@ -493,6 +505,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (*abort) {
+    // A bounded wait gave up in this CTA: wait (bounded) for the K / V^T copies and the
+    // MMAs it started before its shared memory and TMEM are released.
+    if (lane == 0 && warp == 0) {
+      const int nl = tail->kv_issued;
+      for (int s = 0; s < kTcStages && s < nl; ++s) {
+        const int last = s + ((nl - 1 - s) / kTcStages) * kTcStages;
+        mbar_wait_drain(smem_u32(&tail->kvfull[s]), (uint32_t)(last / kTcStages) & 1u);
+      }
+    } else if (lane == 0 && warp == 1 && tail->mma_issued) {
+      mma_commit(smem_u32(&tail->drain));
+      mbar_wait_drain(smem_u32(&tail->drain), 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmCols);

@@ -60,23 +60,41 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity.  Gives up after kWaitLimitNs or when
-// *abort becomes non-zero; on giving up it records `code` in *err and sets *abort so
-// that the other roles of the CTA stop too.
+// Waits for the phase with the given parity.  Gives up after limit_ns or when *abort
+// becomes non-zero; on giving up it records `code` in *err and sets *abort so that the
+// other roles of the CTA stop too.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  volatile int* abort, int* err, int code) {
+                                                  volatile int* abort, int* err, int code,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       if (err) atomicExch(err, code);
       *abort = 1;
       return false;
     }
   }
+}
+
+// Drain wait of a CTA that gave up: waits for an asynchronous copy or MMA batch the CTA
+// itself started (so that nothing lands in its shared memory or TMEM after it exits),
+// bounded by kWaitLimitNs whatever the abort flag says.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// The wait limit a kernel uses: its launch argument, or the default when that is 0.
+__device__ __forceinline__ uint64_t wait_limit(unsigned long long ns) {
+  return ns ? (uint64_t)ns : kWaitLimitNs;
 }
 
 // ---------------------------------------------------------------- TMA
@@ -296,12 +314,13 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // Bounded wait (as mbar_wait_bounded) with cluster-scope acquire, for phases completed by
 // peers' releases.
 __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity,
-                                                          volatile int* abort, int* err, int code) {
+                                                          volatile int* abort, int* err, int code,
+                                                          uint64_t limit_ns = kWaitLimitNs) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       if (err) atomicExch(err, code);
       *abort = 1;
       return false;

@@ -51,8 +51,11 @@ struct SmemTail {
   uint64_t xfull[kMaxStages], xempty[kMaxStages];
   uint64_t accf;
   uint64_t cfull;  // clustered mode: every split's partial tile is in the exchange workspace
+  uint64_t drain;  // after a wait gave up: completion of every MMA this CTA issued
   uint32_t tmem_addr;
   int abort;
+  int w_issued, x_issued;  // TMA loads issued into the weight / activation ring
+  int mma_issued;          // 1 once the MMA warp issued an MMA
 };
 
 template <int MODE>
@@ -100,6 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t ncols = a.na == 2 ? 512u : 256u;
   const uint32_t a_bytes = (a_ok[0] ? a.a_tile_bytes : 0u) + (a_ok[1] ? a.a_tile_bytes : 0u);
   const uint32_t b_bytes = a.nbox * 128u;
+  const uint64_t lim = wait_limit(a.wait_ns);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SW; ++s) {
@@ -111,8 +115,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&tail->xempty[s]), 1);
     }
     mbar_init(smem_u32(&tail->accf), 1);
+    mbar_init(smem_u32(&tail->drain), 1);
     if (kCluster) mbar_init(smem_u32(&tail->cfull), a.splits);
     tail->abort = 0;
+    tail->w_issued = tail->x_issued = 0;
+    tail->mma_issued = 0;
     fence_mbar_init();
     tma_prefetch_desc(&mapA);
     tma_prefetch_desc(&mapB);
@@ -142,10 +149,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool is_a = weights == kWeightIsA;
       const uint64_t pol = weights ? policy_evict_first() : policy_evict_last();
       const uint32_t bytes = is_a ? a_bytes : b_bytes;
+      int issued = 0;
       for (int it = 0; it < nk; ++it) {
         const int s = it % S;
         if (it >= S && !mbar_wait_bounded(smem_u32(&empty[s]), ((uint32_t)(it / S) & 1u) ^ 1u,
-                                          abort, a.err, DEV_TIMEOUT_PRODUCER))
+                                          abort, a.err, DEV_TIMEOUT_PRODUCER, lim))
           break;
         const uint32_t fb = smem_u32(&full[s]);
         const uint32_t dst = smem_u32(ring + (size_t)s * slot);
@@ -164,7 +172,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int y = packed ? ((b_row / a.nbox) * a.k_blocks + kb) * a.nbox : b_row;
           tma_load_2d(dst, &mapB, fb, kx, y, pol);
         }
+        ++issued;
       }
+      if (weights)
+        tail->w_issued = issued;
+      else
+        tail->x_issued = issued;
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -173,13 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; it < nk; ++it) {
         const int sw = it % SW, sx = it % SX;
         if (!mbar_wait_bounded(smem_u32(&tail->wfull[sw]), (uint32_t)(it / SW) & 1u, abort, a.err,
-                               DEV_TIMEOUT_MMA) ||
+                               DEV_TIMEOUT_MMA, lim) ||
             !mbar_wait_bounded(smem_u32(&tail->xfull[sx]), (uint32_t)(it / SX) & 1u, abort, a.err,
-                               DEV_TIMEOUT_MMA)) {
+                               DEV_TIMEOUT_MMA, lim)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        tail->mma_issued = 1;
         const uint32_t ws = smem_u32(wring + (size_t)sw * a.w_slot_bytes);
         const uint32_t xs = smem_u32(xring + (size_t)sx * a.x_slot_bytes);
         const uint32_t abase = kWeightIsA ? ws : xs;
@@ -234,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // then follow one decision for all eight warps, taken after a barrier from the shared
     // abort flag (set by any wait of the CTA that gave up).
     auto accum_ready = [&]() {
-      mbar_wait_bounded(smem_u32(&tail->accf), 0, abort, a.err, DEV_TIMEOUT_EPILOGUE);
+      mbar_wait_bounded(smem_u32(&tail->accf), 0, abort, a.err, DEV_TIMEOUT_EPILOGUE, lim);
       epilogue_sync();
       return *abort == 0;
     };
@@ -275,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (te == 0)
           for (int c = 0; c < S; ++c) mbar_arrive_cluster(mapa_shared(cfull, (uint32_t)c));
         if (mbar_wait_cluster_bounded(cfull, (uint32_t)round & 1u, abort, a.err,
-                                      DEV_TIMEOUT_CLUSTER)) {
+                                      DEV_TIMEOUT_CLUSTER, lim)) {
           const float* src[kMaxClusterSplits];
 #pragma unroll
           for (int c = 0; c < kMaxClusterSplits; ++c) src[c] = region(i, c < S ? c : 0);
@@ -515,6 +529,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (*abort) {
+    // A bounded wait gave up in this CTA.  Before its shared memory and TMEM are released,
+    // wait (bounded) for every TMA copy it issued and every MMA it started.
+    if (lane == 0 && (warp == 0 || warp == 2 + kEpiWarps)) {
+      const bool weights = warp == 0;
+      const int S = weights ? SW : SX;
+      const int n = weights ? tail->w_issued : tail->x_issued;
+      uint64_t* full = weights ? tail->wfull : tail->xfull;
+      for (int s = 0; s < S && s < n; ++s) {
+        const int last = s + ((n - 1 - s) / S) * S;  // the last load issued into slot s
+        mbar_wait_drain(smem_u32(&full[s]), (uint32_t)(last / S) & 1u);
+      }
+    } else if (lane == 0 && warp == 1 && tail->mma_issued) {
+      mma_commit(smem_u32(&tail->drain));
+      mbar_wait_drain(smem_u32(&tail->drain), 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+  if (kCluster) {
+    // No CTA leaves while a peer may still signal its mbarriers: the epilogue warps closed
+    // the start phase of the cluster barrier, the other warps close it here; then the whole
+    // cluster meets once more.  Every wait before this point is bounded.
+    if (warp < 2 || warp == 2 + kEpiWarps) cluster_wait();
+    cluster_arrive_release();
+    cluster_wait();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, ncols);

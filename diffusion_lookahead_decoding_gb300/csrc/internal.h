@@ -15,6 +15,24 @@ typedef __nv_bfloat16 bf16;
 // Sets the message lopa_last_error(NULL) returns (failures of context-free calls).
 void set_global_error(const char* msg);
 
+// ------------------------------------------------------------------ file-scope device words
+constexpr int kMaxDevices = 64;
+// Per-device cache of a file-scope __device__ variable's address, keyed by the context.
+struct SymbolCache {
+  unsigned long long ctx_id[kMaxDevices] = {};
+  void* addr[kMaxDevices] = {};
+};
+// Identifier of the current CUDA context (0 if unknown).
+unsigned long long current_context_id();
+// Device address of `sym` in the current context (looked up again when the context changes).
+cudaError_t symbol_address(const void* sym, SymbolCache& cache, void** out);
+// Error word of the kernel-level entry points on the current device.
+int* call_status_word(cudaError_t* e);
+// Wait limit of the kernel-level entry points (0 = the default), see lopa_set_wait_limit_ns.
+unsigned long long call_wait_limit_ns();
+// Reads (asynchronously, into *code) and clears the error word of lopa_lmhead_argmax_static.
+cudaError_t lmhead_static_take_status(cudaStream_t s, int* code);
+
 // Launches `kern` with programmatic stream serialization (the kernels call pdl_wait
 // before reading their predecessor's outputs) and, when cluster.x > 0, as thread-block
 // clusters of `cluster` CTAs.
@@ -97,6 +115,7 @@ struct GemmArgs {
   float* xws;        // QKV: split-K exchange workspace (see qkv_exchange_floats)
   int* err;
   int w_packed;      // weight operand in tile-major layout (see launch_pack_tiles)
+  unsigned long long wait_ns;  // limit of every device-side wait (0 = the 2 s default)
 };
 
 struct GemmLaunch {
@@ -119,9 +138,15 @@ const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_all
                       const void* w, int n_rows_w, int K, int na, int splits, int tok_box,
                       int num_sms, bool w_packed = false);
 
-// Tile-major weight packing: [rows][K] row-major -> [ceil(rows/tile_rows)][K/64][tile_rows][64].
+// Tile-major weight packing: up to three row-major [rows_i][K] matrices, stacked by rows,
+// -> [ceil(rows/tile_rows)][K/64][tile_rows][64] (rows = the sum of rows_i).
+struct PackSources {
+  static constexpr int kMax = 3;
+  const bf16* ptr[kMax];
+  int rows[kMax];  // 0 for unused entries
+};
 size_t packed_elems(int rows, int K, int tile_rows);
-cudaError_t launch_pack_tiles(const bf16* src, bf16* dst, int rows, int K, int tile_rows,
+cudaError_t launch_pack_tiles(const PackSources& src, bf16* dst, int K, int tile_rows,
                               cudaStream_t s);
 // Gives every kernel of the library the same (maximal) shared-memory carveout, so that
 // consecutive kernels never make an SM change its L1/shared split.
@@ -154,6 +179,7 @@ struct AttnArgs {
                        // blocks of one sequence, e.g. a finished block and the next one)
   int Bq, Bk, Bk_stride, nbq, H, Hk;
   int* err;            // device error word (bounded waits), may be null
+  unsigned long long wait_ns;  // limit of every device-side wait (0 = the 2 s default)
 };
 struct AttnLaunch {
   CUtensorMap maps[5];  // head_dim 128: q, prefix K, prefix V^T, block K, block V^T
@@ -168,8 +194,10 @@ cudaError_t launch_attention(const AttnLaunch& L, cudaStream_t s);
 cudaError_t attention_set_smem_limits();
 
 // ------------------------------------------------------------------ pointwise
+// Token ids outside [0, V) (possible only after a device-side wait gave up and left garbage
+// in the state) read row 0 and record DEV_BAD_INDEX in *err.
 cudaError_t launch_embed_norm(const int* tok, int T, const bf16* E, const bf16* g, float* x,
-                              bf16* n, int d, float eps, cudaStream_t s);
+                              bf16* n, int d, float eps, int V, int* err, cudaStream_t s);
 // x[t] += sum over splits of part[s][t] (split order); n[t] = bf16(rmsnorm(x[t]) * g).
 cudaError_t launch_residual_norm(float* x, const float* part, int nsplit, size_t split_stride,
                                  const bf16* g, bf16* n, int T, int d, float eps, cudaStream_t s);

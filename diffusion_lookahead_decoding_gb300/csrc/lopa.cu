@@ -72,7 +72,9 @@ struct lopa_ctx {
   int ccap[kMaxClusterSplits + 1] = {};  // resident clusters of 1, 2, 4 q/k/v-GEMM CTAs
   // borrowed weights
   const bf16 *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
-  std::vector<const bf16*> attn_norm, wqkv, wo, mlp_norm, wgu, wd;
+  std::vector<const bf16*> attn_norm, mlp_norm;
+  // owned tile-major copies: q/k/v stacked, output, gate/up stacked, down (per layer)
+  std::vector<const bf16*> wqkv, wo, wgu, wd;
   // owned device memory
   std::vector<void*> allocs;
   bf16 *kc = nullptr, *vc = nullptr, *ks = nullptr, *vs = nullptr;
@@ -336,7 +338,8 @@ int enqueue_forward(lopa_ctx* ctx, const Plan& p) {
   const lopa_model_config& m = ctx->mc;
   const int L = m.n_layers, d = m.d_model;
   cudaStream_t s = ctx->stream;
-  CK(launch_embed_norm(p.tok, p.T, ctx->embed, ctx->attn_norm[0], ctx->x, ctx->n, d, m.rms_eps, s));
+  CK(launch_embed_norm(p.tok, p.T, ctx->embed, ctx->attn_norm[0], ctx->x, ctx->n, d, m.rms_eps,
+                       m.vocab, &ctx->st->err, s));
   for (int l = 0; l < L; ++l) {
     CK(launch_gemm(p.qkv[l], s));  // q, k, v + RoPE; K/V Pre-Write
     CK(launch_attention(p.attn[l], s));
@@ -467,21 +470,17 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
   }
   // weights
   if (!aligned16(w->embed) || !aligned16(w->lm_head) || !aligned16(w->final_norm) || !w->attn_norm ||
-      !w->wqkv || !w->wo || !w->mlp_norm || !w->wgu || !w->wd)
+      !w->wq || !w->wk || !w->wv || !w->wo || !w->mlp_norm || !w->wg || !w->wu || !w->wd)
     return fail(ctx, LOPA_ERR_INVALID_ARG, "weight pointers must be non-null and 16-byte aligned");
   ctx->embed = static_cast<const bf16*>(w->embed);
-  ctx->lm_head = static_cast<const bf16*>(w->lm_head);
   ctx->final_norm = static_cast<const bf16*>(w->final_norm);
   for (int l = 0; l < L; ++l) {
-    const void* ps[6] = {w->attn_norm[l], w->wqkv[l], w->wo[l], w->mlp_norm[l], w->wgu[l], w->wd[l]};
+    const void* ps[9] = {w->attn_norm[l], w->wq[l], w->wk[l], w->wv[l], w->wo[l],
+                         w->mlp_norm[l],  w->wg[l], w->wu[l], w->wd[l]};
     for (const void* p : ps)
       if (!aligned16(p)) return fail(ctx, LOPA_ERR_INVALID_ARG, "layer %d weight pointer null or unaligned", l);
     ctx->attn_norm.push_back(static_cast<const bf16*>(w->attn_norm[l]));
-    ctx->wqkv.push_back(static_cast<const bf16*>(w->wqkv[l]));
-    ctx->wo.push_back(static_cast<const bf16*>(w->wo[l]));
     ctx->mlp_norm.push_back(static_cast<const bf16*>(w->mlp_norm[l]));
-    ctx->wgu.push_back(static_cast<const bf16*>(w->wgu[l]));
-    ctx->wd.push_back(static_cast<const bf16*>(w->wd[l]));
   }
   // buffers
   ctx->nbmax = ctx->dc.k + 1;
@@ -539,21 +538,37 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
   CK(launch_rope_table(ctx->cos_t, ctx->sin_t, m.max_seq, dh, (double)m.rope_base, s));
   CK(launch_state_reset(ctx->st, 0, B, m.mask_id, s));
   // Owned tile-major copies of the projection weights and the LM head: every 16 KB
-  // (32 KB for the LM head) tile the GEMMs stream becomes one contiguous HBM run.
-  auto pack = [&](const bf16*& w, int rows, int K, int tile_rows) -> int {
+  // (32 KB for the LM head) tile the GEMMs stream becomes one contiguous HBM run; q, k and
+  // v (and gate and up) are stacked into the one matrix their GEMM streams.
+  auto pack = [&](std::vector<const bf16*>& dst, PackSources src, int K, int tile_rows) -> int {
+    int rows = 0;
+    for (int i = 0; i < PackSources::kMax; ++i) rows += src.rows[i];
     bf16* p = nullptr;
     int rr = dalloc(ctx, &p, packed_elems(rows, K, tile_rows));
     if (rr) return rr;
-    CK(launch_pack_tiles(w, p, rows, K, tile_rows, s));
-    w = p;
+    CK(launch_pack_tiles(src, p, K, tile_rows, s));
+    dst.push_back(p);
     return 0;
   };
+  auto src = [](const void* a, int ra, const void* b = nullptr, int rb = 0, const void* c = nullptr,
+                int rc = 0) {
+    PackSources ps = {{static_cast<const bf16*>(a), static_cast<const bf16*>(b),
+                       static_cast<const bf16*>(c)},
+                      {ra, rb, rc}};
+    return ps;
+  };
   for (int l = 0; l < L; ++l) {
-    if ((r = pack(ctx->wqkv[l], ctx->qkv_rows, d, 128)) || (r = pack(ctx->wo[l], d, H * dh, 128)) ||
-        (r = pack(ctx->wgu[l], 2 * F, d, 128)) || (r = pack(ctx->wd[l], d, F, 128)))
+    if ((r = pack(ctx->wqkv, src(w->wq[l], H * dh, w->wk[l], Hk * dh, w->wv[l], Hk * dh), d, 128)) ||
+        (r = pack(ctx->wo, src(w->wo[l], d), H * dh, 128)) ||
+        (r = pack(ctx->wgu, src(w->wg[l], F, w->wu[l], F), d, 128)) ||
+        (r = pack(ctx->wd, src(w->wd[l], d), F, 128)))
       return r;
   }
-  if ((r = pack(ctx->lm_head, V, d, 256))) return r;
+  {
+    std::vector<const bf16*> lm;
+    if ((r = pack(lm, src(w->lm_head, V), d, 256))) return r;
+    ctx->lm_head = lm[0];
+  }
   CK(cudaEventCreate(&ctx->ev0));
   CK(cudaEventCreate(&ctx->ev1));
   CK(cudaMallocHost(&ctx->h_res, sizeof(lopa_step_result)));
@@ -937,6 +952,13 @@ int lopa_read_kv(lopa_ctx* ctx, int layer, int pos0, int n, uint16_t* k, uint16_
   return 0;
 }
 
+int lopa_debug_set_device_error(lopa_ctx* ctx, int code) {
+  if (!ctx) return fail(nullptr, LOPA_ERR_INVALID_ARG, "ctx is null");
+  CK(cudaMemcpyAsync(&ctx->st->err, &code, sizeof(int), cudaMemcpyHostToDevice, ctx->stream));
+  CK(cudaStreamSynchronize(ctx->stream));
+  return 0;
+}
+
 int lopa_read_branch_kv(lopa_ctx* ctx, int layer, int branch, uint16_t* k, uint16_t* v) {
   if (!ctx) return fail(nullptr, LOPA_ERR_INVALID_ARG, "ctx is null");
   if (layer < 0 || layer >= ctx->mc.n_layers || branch < 0 || branch >= ctx->nbmax)
@@ -979,6 +1001,10 @@ int lopa_linear_accumulate(const void* x, const void* w, float* y, int T, int N,
   G.args.out_f32 = y;
   G.args.ldo = N;
   G.args.atomic = 1;
+  cudaError_t se = cudaSuccess;
+  G.args.err = call_status_word(&se);
+  CK(se);
+  G.args.wait_ns = call_wait_limit_ns();
   CK(launch_gemm(G, static_cast<cudaStream_t>(stream)));
   return 0;
 }
@@ -1015,6 +1041,10 @@ int lopa_lmhead_argmax(const void* hidden, const void* lm_head, int rows, int d_
   a.part_s = ps;
   a.part_i = pi;
   a.part_ld = rows;
+  cudaError_t se = cudaSuccess;
+  a.err = call_status_word(&se);
+  CK(se);
+  a.wait_ns = call_wait_limit_ns();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CK(launch_gemm(G, s));
   CK(launch_lm_merge(pm, ps, pi, nvt, rows, rows, argmax_out, maxp_out, s));
@@ -1053,7 +1083,10 @@ int lopa_branch_attention(const void* q, const void* k_prefix, const void* vt_pr
   a.nbq = n_branches;
   a.H = n_heads;
   a.Hk = n_kv_heads;
-  a.err = nullptr;
+  cudaError_t se = cudaSuccess;
+  a.err = call_status_word(&se);
+  CK(se);
+  a.wait_ns = call_wait_limit_ns();
   AttnLaunch L;
   const char* e = plan_attention(&L, a, head_dim, prefix_len, prefix_len);
   if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s", e);

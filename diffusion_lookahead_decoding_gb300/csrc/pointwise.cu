@@ -29,13 +29,18 @@ __device__ __forceinline__ void store8(bf16* p, const float (&f)[8]) {
 // x[t] = E[tok[t]] (fp32), n[t] = bf16(x * rsqrt(mean(x^2) + eps) * g).  One warp per row.
 __global__ void embed_norm_kernel(const int* __restrict__ tok, int T, const bf16* __restrict__ E,
                                   const bf16* __restrict__ g, float* __restrict__ x,
-                                  bf16* __restrict__ n, int d, float eps) {
+                                  bf16* __restrict__ n, int d, float eps, int V, int* err) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  const bf16* e = E + (size_t)tok[t] * d;
+  int id = tok[t];
+  if (id < 0 || id >= V) {
+    if (lane == 0 && err) atomicExch(err, DEV_BAD_INDEX);
+    id = 0;
+  }
+  const bf16* e = E + (size_t)id * d;
   float* xr = x + (size_t)t * d;
   float ss = 0.f;
   for (int c = lane * 8; c < d; c += 256) {
@@ -203,9 +208,9 @@ cudaError_t pointwise_set_carveout() {
 }
 
 cudaError_t launch_embed_norm(const int* tok, int T, const bf16* E, const bf16* g, float* x,
-                              bf16* n, int d, float eps, cudaStream_t s) {
+                              bf16* n, int d, float eps, int V, int* err, cudaStream_t s) {
   return launch_pdl(embed_norm_kernel, dim3((T + 7) / 8), dim3(256), 0, s, tok, T, E, g, x, n, d,
-                    eps);
+                    eps, V, err);
 }
 
 cudaError_t launch_residual_norm(float* x, const float* part, int nsplit, size_t split_stride,

@@ -68,21 +68,25 @@ typedef struct {
   float logit_scale; /* logits = logit_scale * (final_hidden . lm_head_row) */
 } lopa_model_config;
 
-/* Device pointers (bf16).  Per-layer entries are HOST arrays of n_layers device
+/* Device pointers (bf16), every matrix in the nn.Linear layout [out_features][in_features],
+ * row-major, 16-byte aligned.  Per-layer entries are HOST arrays of n_layers device
  * pointers; the arrays themselves are copied at init and need not outlive the call.
- * lopa_init_model copies the projection matrices (wqkv, wo, wgu, wd) and lm_head into
- * context-owned tile-major copies (the layout the GEMMs stream); the embedding and the
- * norm gains stay borrowed and must outlive the context.  The caller may free the
- * projection matrices and lm_head after init. */
+ * lopa_init_model copies the projection matrices and lm_head into context-owned tile-major
+ * copies (the layout the GEMMs stream; q, k and v are stacked into one matrix, gate and up
+ * into another); the embedding and the norm gains stay borrowed and must outlive the
+ * context.  The caller may free the projection matrices and lm_head after init. */
 typedef struct {
   const void* embed;              /* [vocab][d_model] */
   const void* lm_head;            /* [vocab][d_model] */
   const void* final_norm;         /* [d_model] */
   const void* const* attn_norm;   /* [L] -> [d_model] */
-  const void* const* wqkv;        /* [L] -> [(H + 2*Hk)*dh][d_model]: q rows (head-major), then k, then v */
+  const void* const* wq;          /* [L] -> [H*dh][d_model], rows head-major */
+  const void* const* wk;          /* [L] -> [Hk*dh][d_model] */
+  const void* const* wv;          /* [L] -> [Hk*dh][d_model] */
   const void* const* wo;          /* [L] -> [d_model][H*dh] */
   const void* const* mlp_norm;    /* [L] -> [d_model] */
-  const void* const* wgu;         /* [L] -> [2*ffn][d_model]: gate rows, then up rows */
+  const void* const* wg;          /* [L] -> [ffn][d_model] (gate) */
+  const void* const* wu;          /* [L] -> [ffn][d_model] (up) */
   const void* const* wd;          /* [L] -> [d_model][ffn] */
 } lopa_weights;
 
@@ -189,7 +193,28 @@ int lopa_read_kv(lopa_ctx* ctx, int layer, int pos0, int n, uint16_t* k, uint16_
  * verification forward produced) for layer to host as bf16 words [B][Hk][dh] each. */
 int lopa_read_branch_kv(lopa_ctx* ctx, int layer, int branch, uint16_t* k, uint16_t* v);
 
+/* Test hook (diagnostics): writes `code` into the context's device error word, as a
+ * device-side wait that gave up would.  The next lopa_step / lopa_decode then returns
+ * LOPA_ERR_DEVICE_TIMEOUT; lopa_rewind (or lopa_prefill) clears the word.  Synchronizes. */
+int lopa_debug_set_device_error(lopa_ctx* ctx, int code);
+
 /* ---- kernel-level entry points (device pointers, caller's stream) -------------- */
+/* These calls only enqueue work and return; argument errors are returned at once.  Their
+ * bounded device-side waits record a wait that gave up in a device word of the library
+ * (one per device; nothing is allocated), which lopa_kernel_status reads. */
+
+/* Synchronizes `stream` and reports whether a device-side wait of a kernel-level call
+ * (including lopa_lmhead_argmax_static) gave up since the last lopa_kernel_status on this
+ * device: LOPA_ERR_DEVICE_TIMEOUT (code in lopa_last_error(NULL); the outputs of that call
+ * are not valid) or LOPA_OK.  Clears the record.  Allocates nothing. */
+int lopa_kernel_status(void* stream);
+
+/* Test hook: every device-side wait of the kernel-level calls launched after this call
+ * gives up after `ns` nanoseconds instead of the default 2 s (0 restores the default).
+ * A wait that gives up stops its kernel cleanly: the kernel waits (with the default bound)
+ * for the copies and tensor-core operations it started, frees its tensor memory and
+ * returns.  Context calls (lopa_step, ...) always use the default. */
+int lopa_set_wait_limit_ns(unsigned long long ns);
 
 /* y[T][N] += x[T][K] . w[N][K]^T with bf16 inputs and fp32 accumulation on the
  * tcgen05 tensor cores (the projection kernel of the verification forward).
@@ -227,6 +252,10 @@ int lopa_lmhead_argmax(const void* hidden, const void* lm_head, int rows, int d_
  *   - All calls on a device share the array: calls that can overlap on the GPU (e.g. on
  *     different streams without ordering) race and must be avoided.  Nothing in the array
  *     needs clearing between calls.
+ *   - A device-side wait that gives up is recorded in a second fixed word beside the array
+ *     and reported by lopa_kernel_status.
+ *   - The addresses are looked up again if the device's context changes (e.g. after
+ *     cudaDeviceReset); that call, too, should come before any stream capture.
  * Other arguments, layouts and results are those of lopa_lmhead_argmax. */
 int lopa_lmhead_argmax_static(const void* hidden, const void* lm_head, int rows, int d_model,
                               int vocab, float logit_scale, int mask_id, int32_t* argmax_out,

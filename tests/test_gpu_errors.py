@@ -1,0 +1,85 @@
+"""The device-error path, exercised without faulting the GPU.
+
+(a) A failure planted on the host: the context's device error word is set as a bounded
+    device-side wait that gave up would set it.  lopa_step must report
+    LOPA_ERR_DEVICE_TIMEOUT, and after lopa_rewind the decode must reproduce the tokens of
+    an undisturbed decode.
+(b) A wait that really runs out: with a test-only wait limit of 100 ns the standalone LM
+    head's pipeline waits give up; the kernel drains its own copies and MMAs, frees its
+    tensor memory and returns, and lopa_kernel_status reports the timeout.  With the
+    default limit restored the same call is correct again, so the context stays usable.
+"""
+import numpy as np
+import pytest
+import torch
+
+from diffusion_lookahead_decoding_gb300 import _lib as L
+from diffusion_lookahead_decoding_gb300 import synth
+from tests.gpu_util import build_lib, make_decoder, workload_weights
+
+pytestmark = pytest.mark.gpu
+
+
+def test_planted_device_error_is_reported_and_rewind_recovers():
+    from diffusion_lookahead_decoding_gb300 import api
+    shape, dshape, _ = workload_weights("tiny")
+    dec = make_decoder("tiny")
+    prompt = synth.make_prompt(shape, dshape.prompt_len, seed=1)
+    dec.prefill(prompt)
+    ref, _ = dec.decode(dshape.gen_len)
+    dec.rewind(dshape.prompt_len)
+    dec.debug_set_device_error(1)
+    with pytest.raises(L.LopaError) as e:
+        dec.step()
+    assert e.value.code == L.ERR_DEVICE_TIMEOUT
+    dec.rewind(dshape.prompt_len)
+    toks, st = dec.decode(dshape.gen_len)
+    np.testing.assert_array_equal(toks, ref)
+    # A decode that meets the planted error stops with the same status.
+    dec.rewind(dshape.prompt_len)
+    dec.debug_set_device_error(3)
+    with pytest.raises(L.LopaError) as e:
+        dec.decode(dshape.gen_len)
+    assert e.value.code == L.ERR_DEVICE_TIMEOUT
+    dec.rewind(dshape.prompt_len)
+    toks, _ = dec.decode(dshape.gen_len)
+    np.testing.assert_array_equal(toks, ref)
+    dec.close()
+
+
+@pytest.mark.parametrize("static", [False, True])
+def test_short_wait_limit_reports_timeout_and_the_call_recovers(static):
+    from diffusion_lookahead_decoding_gb300 import api
+    build_lib()
+    lib = L.load()
+    rows, d, V = 256, 3584, 152064
+    g = torch.Generator().manual_seed(13)
+    h = torch.randn(rows, d, generator=g).to(torch.bfloat16).cuda()
+    w = (torch.randn(V, d, generator=g) * 0.02).to(torch.bfloat16).cuda()
+
+    def call():
+        if not static:
+            return api.lmhead_argmax(h, w, 20.0, 0)
+        am = torch.empty(rows, dtype=torch.int32, device="cuda")
+        mp = torch.empty(rows, dtype=torch.float32, device="cuda")
+        L.check(lib.lopa_lmhead_argmax_static(h.data_ptr(), w.data_ptr(), rows, d, V, 20.0, 0,
+                                              am.data_ptr(), mp.data_ptr(), api._stream_ptr()))
+        return am, mp
+
+    api.kernel_status()  # nothing pending
+    am_ref, mp_ref = call()
+    api.kernel_status()
+    am_ref, mp_ref = am_ref.cpu().numpy(), mp_ref.cpu().numpy()
+    try:
+        api.set_wait_limit_ns(100)
+        call()
+        with pytest.raises(L.LopaError) as e:
+            api.kernel_status()
+        assert e.value.code == L.ERR_DEVICE_TIMEOUT
+    finally:
+        api.set_wait_limit_ns(0)
+    api.kernel_status()  # the record was cleared
+    am, mp = call()
+    api.kernel_status()
+    np.testing.assert_array_equal(am.cpu().numpy(), am_ref)
+    np.testing.assert_array_equal(mp.cpu().numpy(), mp_ref)
