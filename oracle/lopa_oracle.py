@@ -47,7 +47,8 @@ import numpy as np
 __all__ = [
     "bf16_round", "rmsnorm", "rope", "silu", "linear", "isolated_attention", "logit_summary", "OracleModel", "prefill",
     "forward", "anchor_fill", "lookahead_candidates", "build_branches",
-    "branch_confidence", "select_winner", "lopa_step", "decode", "StepRecord",
+    "branch_confidence", "select_winner", "decision_margins", "lopa_step", "decode",
+    "StepRecord",
 ]
 
 # ----------------------------------------------------------------------------------
@@ -347,19 +348,49 @@ class StepRecord:
     margins: dict
 
 
-def _decision_margins(tok, mp, tau, mask_id):
+def decision_margins(tok, mp, p2, tau, k, mask_id, conf, winner):
+    """How close each decision of one iteration came to going the other way.  Only the
+    quantities the iteration's outcome (the positions it fills and their tokens) depends
+    on are measured; a value under a tolerance marks that decision as a near-tie.
+
+      tau      : min over masked positions of |mp - tau| (each one's threshold test).
+      fallback : when no masked position reaches tau, the gap between the two highest
+                 masked mp (which single position the anchor fills); else inf.
+      rank     : when more positions remain masked after the anchor fill than there are
+                 lookahead branches (k >= 1), the gap between the k-th and (k+1)-th
+                 highest remaining mp (which positions become candidates); else inf.
+                 The order among the chosen k only permutes the branches.
+      conf     : the winner's confidence minus the best other branch's; inf for one branch.
+      token    : min over the positions this iteration fills (anchor fills and the
+                 winner's extra position) of mp - p2, the top-2 probability gap of the
+                 logits that chose their tokens; inf when p2 is not given.
+    """
     masked = [i for i in range(len(tok)) if tok[i] == mask_id]
     m_tau = min((abs(float(mp[i]) - tau) for i in masked), default=math.inf)
-    vals = sorted(float(mp[i]) for i in masked)
-    m_rank = min((b - a for a, b in zip(vals, vals[1:])), default=math.inf)
-    return m_tau, m_rank
+    m_fb = math.inf
+    if masked and not any(float(mp[i]) >= tau for i in masked) and len(masked) >= 2:
+        top = sorted((float(mp[i]) for i in masked), reverse=True)
+        m_fb = top[0] - top[1]
+    anchor, S = anchor_fill(tok, np.zeros(len(tok), dtype=np.int64) + (mask_id + 1), mp, tau,
+                            mask_id)
+    R = sorted((float(mp[i]) for i in range(len(tok)) if anchor[i] == mask_id), reverse=True)
+    m_rank = R[k - 1] - R[k] if 1 <= k < len(R) else math.inf
+    others = [c for b, c in enumerate(conf) if b != winner]
+    m_conf = conf[winner] - max(others) if others else math.inf
+    m_tok = math.inf
+    if p2 is not None:
+        C = lookahead_candidates(anchor, mp, k, mask_id)
+        filled = list(S) + ([C[winner - 1]] if winner >= 1 else [])
+        m_tok = min(float(mp[i]) - float(p2[i]) for i in filled)
+    return {"tau": m_tau, "fallback": m_fb, "rank": m_rank, "conf": m_conf, "token": m_tok}
 
 
-def lopa_step(model, cache, P, tok, am, mp, k, tau):
+def lopa_step(model, cache, P, tok, am, mp, k, tau, p2=None):
     """One LoPA iteration on the current block state (tok, and the (am, mp) summary of
-    the logits that produced it): anchor fill, k lookahead branches, one isolated
-    forward over all branches, branch confidences, winner.  The winner's (am, mp)
-    are returned for reuse by the next iteration ([ANN]: no extra forward)."""
+    the logits that produced it; p2, their second-largest probabilities, only feeds the
+    reported margins): anchor fill, k lookahead branches, one isolated forward over all
+    branches, branch confidences, winner.  The winner's (am, mp) are returned for reuse
+    by the next iteration ([ANN]: no extra forward)."""
     sh = model.shape
     anchor, S = anchor_fill(tok, am, mp, tau, sh.mask_id)
     C = lookahead_candidates(anchor, mp, k, sh.mask_id)
@@ -367,11 +398,7 @@ def lopa_step(model, cache, P, tok, am, mp, k, tau):
     out = forward(model, cache, P, branches)
     conf = [branch_confidence(branches[b], out.mp[b], sh.mask_id) for b in range(len(branches))]
     w = select_winner(conf)
-    srt = sorted(conf, reverse=True)
-    m_tau, m_rank = _decision_margins(tok, mp, tau, sh.mask_id)
-    margins = {"tau": m_tau, "rank": m_rank,
-               "conf": (srt[0] - srt[1]) if len(srt) > 1 else math.inf,
-               "token": float(np.min(out.mp[w] - out.p2[w]))}
+    margins = decision_margins(tok, mp, p2, tau, k, sh.mask_id, conf, w)
     return StepRecord(S, C, branches, conf, w, out.am[w], out.mp[w], out.p2[w], out, margins)
 
 
@@ -392,12 +419,12 @@ def decode(model, prompt, block, k, tau, gen_len, record=False):
         tok = np.full(block, sh.mask_id, dtype=np.int64)
         first = forward(model, cache, P, tok[None, :])
         forwards += 1
-        am, mp = first.am[0], first.mp[0]
+        am, mp, p2 = first.am[0], first.mp[0], first.p2[0]
         while (tok == sh.mask_id).any():
-            st = lopa_step(model, cache, P, tok, am, mp, k, tau)
+            st = lopa_step(model, cache, P, tok, am, mp, k, tau, p2)
             forwards += 1
             w = st.winner
-            tok, am, mp = st.branches[w], st.am, st.mp
+            tok, am, mp, p2 = st.branches[w], st.am, st.mp, st.p2
             for l in range(sh.n_layers):
                 cache.k[l][P:P + block] = st.out.block_k[l][w]
                 cache.v[l][P:P + block] = st.out.block_v[l][w]

@@ -191,6 +191,13 @@ def test_decision_rules_hand_worked(case):
     conf = [O.branch_confidence(br[b], case["verify_mp"][b], mask) for b in range(len(br))]
     np.testing.assert_allclose(conf, case["expect_conf"], rtol=0, atol=1e-15)
     assert O.select_winner(conf) == case["expect_winner"]
+    m = O.decision_margins(np.array(case["tok"]), case["mp"], case["p2"], case["tau"], case["k"],
+                           mask, case["expect_conf"], case["expect_winner"])
+    for key, want in case["expect_margins"].items():
+        if want is None:
+            assert m[key] == math.inf, (key, m[key])
+        else:
+            assert abs(m[key] - want) < 1e-12, (key, m[key], want)
 
 
 def test_candidates_match_counting_definition():
@@ -408,6 +415,193 @@ def test_pins_catch_planted_decision_mistakes(monkeypatch):
     with pytest.raises(AssertionError):
         for c in cases:
             test_decision_rules_hand_worked(c)
+
+
+def _margins_all_positions_token(tok, mp, p2, tau, k, mask_id, conf, winner):
+    m = REAL_MARGINS(tok, mp, p2, tau, k, mask_id, conf, winner)
+    m["token"] = min(float(mp[i]) - float(p2[i]) for i in range(len(tok)))
+    return m
+
+
+def _margins_adjacent_rank(tok, mp, p2, tau, k, mask_id, conf, winner):
+    m = REAL_MARGINS(tok, mp, p2, tau, k, mask_id, conf, winner)
+    vals = sorted(float(mp[i]) for i in range(len(tok)) if tok[i] == mask_id)
+    m["rank"] = min((b - a for a, b in zip(vals, vals[1:])), default=math.inf)
+    return m
+
+
+def _margins_tau_over_all(tok, mp, p2, tau, k, mask_id, conf, winner):
+    m = REAL_MARGINS(tok, mp, p2, tau, k, mask_id, conf, winner)
+    m["tau"] = min(abs(float(v) - tau) for v in mp)
+    return m
+
+
+def _margins_conf_vs_lowest(tok, mp, p2, tau, k, mask_id, conf, winner):
+    m = REAL_MARGINS(tok, mp, p2, tau, k, mask_id, conf, winner)
+    others = [c for b, c in enumerate(conf) if b != winner]
+    m["conf"] = conf[winner] - min(others) if others else math.inf
+    return m
+
+
+REAL_MARGINS = O.decision_margins
+
+
+@pytest.mark.parametrize("plant", [_margins_all_positions_token, _margins_adjacent_rank,
+                                   _margins_tau_over_all, _margins_conf_vs_lowest])
+def test_pins_catch_planted_margin_mistakes(monkeypatch, plant):
+    """Each over-broad or wrong margin (the token gap over every position, the rank gap
+    between any two masked positions, the threshold distance over unmasked positions, the
+    confidence gap to the weakest branch) fails a hand-worked case."""
+    monkeypatch.setattr(OL, "decision_margins", plant)
+    with pytest.raises(AssertionError):
+        for c in _golden_cases():
+            test_decision_rules_hand_worked(c)
+
+
+# ------------------------------------------------------ exhaustive fill-order replay
+# "SJTU x Huawei Xiaoyi release LoPA", section "Problem: the token filling order limits
+# parallelism": the order in which a block's positions are filled (TFO) decides what the
+# model can fill in parallel, and confidence-driven decoding picks it greedily.  On tiny
+# blocks every one of the B! single-token fill orders is replayed with separate forwards.
+TFO_PROMPT = 9
+
+
+def _state_summary(m, cache, P, state, memo):
+    key = tuple(int(t) for t in state)
+    if key not in memo:
+        out = O.forward(m, cache, P, np.array(state)[None, :])
+        memo[key] = (out.am[0], out.mp[0])
+    return memo[key]
+
+
+def _consistent_orders(m, cache, P, block, mask, memo):
+    """All single-token fill orders (each fill takes the greedy token of a fresh forward of
+    the state before it) whose every step fills the most confident masked position (lowest
+    position on ties): the exhaustive replay walks every order and keeps those."""
+    kept, prefixes = [], set()
+    import itertools
+    for order in itertools.permutations(range(block)):
+        state = [mask] * block
+        ok = True
+        for j, pos in enumerate(order):
+            prefixes.add(order[:j])
+            am, mp = _state_summary(m, cache, P, state, memo)
+            masked = [i for i in range(block) if state[i] == mask]
+            best = max(masked, key=lambda i: (mp[i], -i))
+            ok = ok and pos == best
+            state[pos] = int(am[pos])
+        if ok:
+            kept.append((list(order), state))
+    return kept, len(prefixes)
+
+
+@pytest.fixture(scope="module")
+def tiny_w():
+    return synth.make_weights(synth.TINY[0], seed=0, threads=1)
+
+
+@pytest.mark.parametrize("block", [4, 6])
+def test_exhaustive_fill_order_replay_reproduces_the_chosen_order(tiny_w, block):
+    """k = 0 with a threshold no probability reaches: the anchor fills one position per
+    iteration, so the decode's TFO is a single-token order.  Among all block! orders,
+    replayed exhaustively with a separate forward per state, exactly one is consistent with
+    the per-step argmax choices, and it is the TFO the oracle recorded, with the same
+    tokens and one forward per fill plus the block start."""
+    shape = synth.TINY[0]
+    m = O.OracleModel(shape, tiny_w, act="fp64")
+    prompt = synth.make_prompt(shape, TFO_PROMPT, seed=3)
+    toks, fw, cache, log = O.decode(m, prompt, block, 0, 1.5, block, record=True)
+    tfo = [p for _, st in log for p in st.filled]
+    assert all(len(st.filled) == 1 for _, st in log)
+    memo = {}
+    kept, n_prefix = _consistent_orders(m, cache, TFO_PROMPT, block, shape.mask_id, memo)
+    assert n_prefix == sum(math.perm(block, j) for j in range(block))  # every order, every step
+    assert len(kept) == 1
+    order, state = kept[0]
+    assert order == tfo
+    np.testing.assert_array_equal(state, toks)
+    assert fw == block + 1
+
+
+@pytest.mark.parametrize("block", [4, 6])
+def test_exhaustive_replay_with_lookahead_branches(tiny_w, block):
+    """k >= block (every remaining position is a candidate), threshold never reached: each
+    iteration fills the most confident position (the anchor) and, when a lookahead branch
+    wins, one more.  Replaying all block! single-token orders, the recorded TFO (anchor
+    position first within an iteration) is the only order whose groups are the iterations'
+    fills, whose first fill per group is the argmax of a fresh forward of the state, and
+    whose second fill is the position of the best one-extra branch, every branch scored by
+    its own separate forward."""
+    import itertools
+    shape = synth.TINY[0]
+    mask = shape.mask_id
+    m = O.OracleModel(shape, tiny_w, act="fp64")
+    prompt = synth.make_prompt(shape, TFO_PROMPT, seed=4)
+    toks, fw, cache, log = O.decode(m, prompt, block, block, 1.5, block, record=True)
+    P = TFO_PROMPT
+    groups = []
+    state = [mask] * block
+    memo = {}
+    for _, st in log:
+        am, mp = _state_summary(m, cache, P, state, memo)  # fresh forward of the state
+        masked = [i for i in range(block) if state[i] == mask]
+        a_t = max(masked, key=lambda i: (mp[i], -i))
+        anchor = list(state)
+        anchor[a_t] = int(am[a_t])
+        best, best_c = -1.0, None
+        for c in [None] + [i for i in masked if i != a_t]:
+            br = list(anchor)
+            if c is not None:
+                br[c] = int(am[c])
+            _, mp_b = _state_summary(m, cache, P, br, memo)
+            rem = [i for i in range(block) if br[i] == mask]
+            conf = 1.0 if not rem else float(np.mean([mp_b[i] for i in rem]))
+            if conf > best:
+                best, best_c = conf, c
+        group = [a_t] + ([best_c] if best_c is not None else [])
+        groups.append(group)
+        assert st.filled == [a_t]
+        filled = sorted(i for i in range(block) if st.branches[st.winner][i] != mask and state[i] == mask)
+        assert filled == sorted(group)
+        state = list(st.branches[st.winner])
+    np.testing.assert_array_equal(state, toks)
+    tfo = [p for g in groups for p in g]
+    sizes = [len(g) for g in groups]
+    consistent = []
+    for order in itertools.permutations(range(block)):
+        i, ok = 0, True
+        for g in groups:
+            if list(order[i:i + len(g)]) != g:
+                ok = False
+                break
+            i += len(g)
+        if ok:
+            consistent.append(list(order))
+    assert consistent == [tfo] and sum(sizes) == block
+    assert fw == len(log) + 1
+
+
+def test_fill_order_replay_catches_planted_mistakes(tiny_w, monkeypatch):
+    """An anchor fallback that fills the least confident position, or a winner rule that
+    takes the lowest confidence, makes the replays fail."""
+    real_fill = OL.anchor_fill
+
+    def least_confident(tok, am, mp, tau, mask_id):
+        masked = [i for i in range(len(tok)) if tok[i] == mask_id]
+        if not any(mp[i] >= tau for i in masked) and masked:
+            worst = min(masked, key=lambda i: (mp[i], i))
+            anchor = np.array(tok, copy=True)
+            anchor[worst] = am[worst]
+            return anchor, [worst]
+        return real_fill(tok, am, mp, tau, mask_id)
+
+    monkeypatch.setattr(OL, "anchor_fill", least_confident)
+    with pytest.raises(AssertionError):
+        test_exhaustive_fill_order_replay_reproduces_the_chosen_order(tiny_w, 4)
+    monkeypatch.undo()
+    monkeypatch.setattr(OL, "select_winner", lambda conf: int(np.argmin(conf)))
+    with pytest.raises(AssertionError):
+        test_exhaustive_replay_with_lookahead_branches(tiny_w, 4)
 
 
 # ------------------------------------------------------------- isolated attention
