@@ -32,8 +32,11 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "timeline.cuh"
 
 namespace lopa {
+
+LOPA_TL_UNIT(attention)
 
 namespace {
 
@@ -198,6 +201,8 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ TcMaps m, const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
+  TL_DECL;
+  TL_START();
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   TcTail* tail = reinterpret_cast<TcTail*>(smem + kTcOffTail);
@@ -243,6 +248,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* abort = &tail->abort;
   pdl_trigger();
   pdl_wait();  // q and the block keys come from the previous kernel; out may be read by it
+  TL_WAITED();
   const KeySched ks = key_sched<kTcKeys>(a, b_lo, b_hi);
   const int n = ks.n_pre + ks.n_br;
   const uint64_t lim = wait_limit(a.wait_ns);
@@ -525,6 +531,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmCols);
   }
+  TL_END(tl::ATTN_TC);
 }
 
 // ================================================================ mma.sync path (dh 32, 64)
@@ -579,8 +586,10 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnArgs a) {
   constexpr int CH = DH / 8;        // 16-byte chunks per key row
   extern __shared__ __align__(16) uint8_t smem_raw[];
   bf16* sm = reinterpret_cast<bf16*>(smem_raw);
-
+  TL_DECL;
+  TL_START();
   pdl_wait();
+  TL_WAITED();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kg = warp >> 2, rw = warp & 3, gtid = threadIdx.x & 127;
@@ -798,6 +807,7 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnArgs a) {
     bf16* orow = a.out + ((size_t)(b * a.Bq + i) * a.H + g * G + hg) * DH;
     *reinterpret_cast<uint4*>(orow + col) = *reinterpret_cast<const uint4*>(ostage + rr * DH + col);
   }
+  TL_END(tl::ATTN_MMA);
 }
 
 template <int DH>

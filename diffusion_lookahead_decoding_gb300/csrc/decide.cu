@@ -12,20 +12,43 @@
 // Blocks are at most 64 positions, so each decision runs in one CTA.
 #include "common.cuh"
 #include "internal.h"
+#include "timeline.cuh"
 
 namespace lopa {
 
+LOPA_TL_UNIT(decide)
+
 namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// (value, index) pair reduced to the larger value, the lower index on equal values; -1
+// marks an empty slot.  Every lane of the warp gets the result.
+__device__ __forceinline__ void warp_argmax(float& v, int& idx) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(kFull, v, o);
+    const int oi = __shfl_xor_sync(kFull, idx, o);
+    const bool take = oi >= 0 && (idx < 0 || ov > v || (ov == v && oi < idx));
+    v = take ? ov : v;
+    idx = take ? oi : idx;
+  }
+}
 
 __global__ void decide_kernel(DevState* st, int B, int k, float tau, int mask_id,
                               int* __restrict__ branch_tok, int* __restrict__ valid) {
+  TL_DECL;
+  TL_START();
   pdl_wait();
+  TL_WAITED();
   pdl_trigger();
   __shared__ float s_mp[LOPA_MAX_BLOCK];
   __shared__ int s_rem[LOPA_MAX_BLOCK];
   __shared__ int s_cand[LOPA_MAX_BRANCHES];
-  __shared__ int s_best;
-  const int i = threadIdx.x;  // blockDim.x == LOPA_MAX_BLOCK
+  __shared__ float s_bv[LOPA_MAX_BLOCK / 32];
+  __shared__ int s_bi[LOPA_MAX_BLOCK / 32];
+  const int i = threadIdx.x;  // blockDim.x == LOPA_MAX_BLOCK (two warps)
+  const int lane = i & 31, wid = i >> 5;
   const int nb = k + 1;
   const int tok = i < B ? st->tok[i] : 0;
   const int am = i < B ? st->am[i] : 0;
@@ -34,20 +57,23 @@ __global__ void decide_kernel(DevState* st, int B, int k, float tau, int mask_id
   bool fill = masked && mp >= tau;
   s_mp[i] = mp;
   if (i < LOPA_MAX_BRANCHES) s_cand[i] = -1;
-  if (i == 0) s_best = -1;
   const int any_fill = __syncthreads_or(fill);
   if (!any_fill) {
-    // Fill the single most confident masked position (lowest position on ties).
-    if (i == 0) {
-      int best = -1;
-      for (int j = 0; j < B; ++j) {
-        if (st->tok[j] != mask_id) continue;
-        if (best < 0 || s_mp[j] > s_mp[best]) best = j;
-      }
-      s_best = best;
+    // Fill the single most confident masked position (lowest position on ties): a warp
+    // (max, lowest index) reduction per warp, then the two warps' winners.
+    float v = masked ? mp : -INFINITY;
+    int idx = masked ? i : -1;
+    warp_argmax(v, idx);
+    if (lane == 0) {
+      s_bv[wid] = v;
+      s_bi[wid] = idx;
     }
     __syncthreads();
-    fill = (i == s_best);
+    v = s_bv[lane & 1];
+    idx = s_bi[lane & 1];
+    if (lane >= 2) idx = -1;
+    warp_argmax(v, idx);
+    fill = (i == idx);
   }
   const int anchor = fill ? am : tok;
   const bool rem = masked && !fill;
@@ -87,40 +113,50 @@ __global__ void decide_kernel(DevState* st, int B, int k, float tau, int mask_id
     st->n_valid = 1 + nl;
     st->final_w = final_w;
   }
+  TL_END(tl::DECIDE);
 }
 
+// One warp per branch (blockDim.x == 32 * LOPA_MAX_BRANCHES).
 __global__ void select_kernel(DevState* st, int B, int nb, int mask_id,
                               const int* __restrict__ branch_tok, const int* __restrict__ valid,
                               const int* __restrict__ am_b, const float* __restrict__ mp_b) {
+  TL_DECL;
+  TL_START();
   pdl_wait();
+  TL_WAITED();
   pdl_trigger();
   __shared__ float s_conf[LOPA_MAX_BRANCHES];
   __shared__ int s_w;
   __shared__ int s_old[LOPA_MAX_BLOCK];
   __shared__ int s_new[LOPA_MAX_BLOCK];
-  const int i = threadIdx.x;  // blockDim.x == LOPA_MAX_BLOCK
-  if (i < nb) {
-    float c = -INFINITY;
-    if (valid[i]) {
-      float sum = 0.f;
-      int cnt = 0;
-      for (int j = 0; j < B; ++j) {
-        if (branch_tok[i * B + j] == mask_id) {
-          sum += mp_b[i * B + j];
-          ++cnt;
-        }
+  const int i = threadIdx.x;
+  const int lane = i & 31, b = i >> 5;
+  if (b < nb) {
+    // Branch confidence: mean maxp over the branch's masked positions (lane j holds
+    // positions j and j + 32), summed by a fixed shuffle tree; no masked position -> 1.0.
+    float sum = 0.f;
+    int cnt = 0;
+    for (int j = lane; j < B; j += 32) {
+      if (branch_tok[b * B + j] == mask_id) {
+        sum += mp_b[b * B + j];
+        ++cnt;
       }
-      c = cnt ? sum / (float)cnt : 1.0f;
     }
-    s_conf[i] = c;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sum += __shfl_xor_sync(kFull, sum, o);
+      cnt += __shfl_xor_sync(kFull, cnt, o);
+    }
+    if (lane == 0) s_conf[b] = valid[b] ? (cnt ? sum / (float)cnt : 1.0f) : -INFINITY;
   }
   if (i < B) s_old[i] = st->tok[i];
   __syncthreads();
-  if (i == 0) {
-    int w = 0;
-    for (int b = 1; b < nb; ++b)
-      if (s_conf[b] > s_conf[w]) w = b;
-    s_w = w;
+  if (b == 0) {
+    // Winner: highest confidence, lowest branch on ties.
+    float v = lane < nb ? s_conf[lane] : -INFINITY;
+    int idx = lane < nb ? lane : -1;
+    warp_argmax(v, idx);
+    if (lane == 0) s_w = idx;
   }
   __syncthreads();
   const int w = s_w;
@@ -132,24 +168,28 @@ __global__ void select_kernel(DevState* st, int B, int nb, int mask_id,
     st->mp[i] = mp_b[w * B + i];
   }
   __syncthreads();
+  // Positions this iteration filled, in ascending order: a ballot per warp, each filled
+  // position's slot = the filled positions before it (popcounts).
+  __shared__ unsigned s_bal[LOPA_MAX_BLOCK / 32];
+  const bool filled = i < B && s_old[i] == mask_id && s_new[i] != mask_id;
+  const unsigned bal = __ballot_sync(kFull, filled);
+  if (lane == 0 && b < LOPA_MAX_BLOCK / 32) s_bal[b] = bal;
+  const int any_masked = __syncthreads_or(i < B && s_new[i] == mask_id);
+  lopa_step_result& r = st->res;
+  if (filled) {
+    const int slot = (b == 1 ? __popc(s_bal[0]) : 0) + __popc(bal & ((1u << lane) - 1u));
+    r.filled_pos[slot] = i;
+    r.filled_tok[slot] = s_new[i];
+  }
+  // In a completing iteration only the winner (slot 0) was evaluated: it is reported
+  // under its branch index, every other branch as -inf.
+  const int fw = st->final_w;
+  if (i < LOPA_MAX_BRANCHES)
+    r.conf[i] = fw >= 0 ? (i == fw ? s_conf[0] : -INFINITY) : (i < nb ? s_conf[i] : -INFINITY);
   if (i == 0) {
-    lopa_step_result& r = st->res;
-    int nf = 0, done = 1;
-    for (int j = 0; j < B; ++j) {
-      if (s_old[j] == mask_id && s_new[j] != mask_id) {
-        r.filled_pos[nf] = j;
-        r.filled_tok[nf] = s_new[j];
-        ++nf;
-      }
-      if (s_new[j] == mask_id) done = 0;
-    }
-    // In a completing iteration only the winner (slot 0) was evaluated: it is reported
-    // under its branch index, every other branch as -inf.
-    const int fw = st->final_w;
-    for (int b = 0; b < LOPA_MAX_BRANCHES; ++b)
-      r.conf[b] = fw >= 0 ? (b == fw ? s_conf[0] : -INFINITY) : (b < nb ? s_conf[b] : -INFINITY);
+    const int done = !any_masked;
     r.winner = fw >= 0 ? fw : w;
-    r.n_filled = nf;
+    r.n_filled = __popc(s_bal[0]) + (B > 32 ? __popc(s_bal[1]) : 0);
     r.block_done = done;
     r.n_valid_branches = st->n_valid;
     r.prefix_len = st->P;
@@ -158,6 +198,7 @@ __global__ void select_kernel(DevState* st, int B, int nb, int mask_id,
     st->winner = w;
     st->block_done = done;
   }
+  TL_END(tl::SELECT);
 }
 
 // grid: (L, 2 [K, V], chunks); copies B rows of row_elems bf16 of the winner's branch.
@@ -167,7 +208,10 @@ __global__ void select_kernel(DevState* st, int B, int nb, int mask_id,
 __global__ void commit_kv_kernel(const DevState* st, const bf16* __restrict__ ks,
                                  const bf16* __restrict__ vts, bf16* __restrict__ kc,
                                  bf16* __restrict__ vtc, int B, int row_elems, KvStrides kv) {
+  TL_DECL;
+  TL_START();
   pdl_wait();
+  TL_WAITED();
   pdl_trigger();
   const int l = blockIdx.x;
   const int w = st->winner;
@@ -187,28 +231,34 @@ __global__ void commit_kv_kernel(const DevState* st, const bf16* __restrict__ ks
       dst[(size_t)r * kv.ld_cache + c] = src[(size_t)r * kv.ld_scr + c];
     }
   }
+  TL_END(tl::COMMIT);
 }
 
 // With am_next / mp_next (the logit summary of a block-start forward run in the same
 // pass) a finished block is followed by the next block with its first logits in place.
 __global__ void finalize_kernel(DevState* st, int B, int mask_id, int* __restrict__ out_tokens,
                                 const int* __restrict__ am_next, const float* __restrict__ mp_next) {
+  TL_DECL;
+  TL_START();
   pdl_wait();
+  TL_WAITED();
   pdl_trigger();
   const int i = threadIdx.x;
   const int P = st->P, P0 = st->P0;
   const int done = st->block_done;
   __syncthreads();
-  if (!done) return;
-  if (i < B) {
-    out_tokens[P - P0 + i] = st->tok[i];
-    st->tok[i] = mask_id;
-    if (am_next) {
-      st->am[i] = am_next[i];
-      st->mp[i] = mp_next[i];
+  if (done) {
+    if (i < B) {
+      out_tokens[P - P0 + i] = st->tok[i];
+      st->tok[i] = mask_id;
+      if (am_next) {
+        st->am[i] = am_next[i];
+        st->mp[i] = mp_next[i];
+      }
     }
+    if (i == 0) st->P = P + B;
   }
-  if (i == 0) st->P = P + B;
+  TL_END(tl::FINALIZE);
 }
 
 __global__ void state_reset_kernel(DevState* st, int P, int B, int mask_id) {
@@ -252,8 +302,8 @@ cudaError_t launch_decide(void* st, int B, int k, float tau, int mask_id, int* b
 cudaError_t launch_select(void* st, int B, int nb, int mask_id, const int* branch_tok,
                           const int* valid, const int* am_b, const float* mp_b,
                           cudaStream_t s) {
-  return launch_pdl(select_kernel, dim3(1), dim3(LOPA_MAX_BLOCK), 0, s, static_cast<DevState*>(st),
-                    B, nb, mask_id, branch_tok, valid, am_b, mp_b);
+  return launch_pdl(select_kernel, dim3(1), dim3(32 * LOPA_MAX_BRANCHES), 0, s,
+                    static_cast<DevState*>(st), B, nb, mask_id, branch_tok, valid, am_b, mp_b);
 }
 
 cudaError_t launch_commit_kv(const void* st, const bf16* ks, const bf16* vts, bf16* kc,

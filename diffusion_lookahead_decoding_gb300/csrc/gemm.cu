@@ -33,8 +33,11 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "timeline.cuh"
 
 namespace lopa {
+
+LOPA_TL_UNIT(gemm)
 
 namespace {
 
@@ -56,6 +59,7 @@ struct SmemTail {
   int abort;
   int w_issued, x_issued;  // TMA loads issued into the weight / activation ring
   int mma_issued;          // 1 once the MMA warp issued an MMA
+  unsigned long long tl_tw;  // timeline builds: when the accumulator was complete
 };
 
 template <int MODE>
@@ -63,6 +67,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
+  TL_DECL;
+  TL_START();
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* wring = smem;
@@ -249,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // abort flag (set by any wait of the CTA that gave up).
     auto accum_ready = [&]() {
       mbar_wait_bounded(smem_u32(&tail->accf), 0, abort, a.err, DEV_TIMEOUT_EPILOGUE, lim);
+      if (te == 0) TL_STAMP(tail->tl_tw);
       epilogue_sync();
       return *abort == 0;
     };
@@ -560,6 +567,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, ncols);
   }
+#ifdef LOPA_TIMELINE
+  if (threadIdx.x == 0) tl_tw = tail->tl_tw;
+#endif
+  TL_END(tl::GEMM + MODE);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,

@@ -15,6 +15,13 @@ typedef __nv_bfloat16 bf16;
 // Sets the message lopa_last_error(NULL) returns (failures of context-free calls).
 void set_global_error(const char* msg);
 
+#ifdef LOPA_TIMELINE
+cudaError_t timeline_set_buffer_gemm(unsigned* p);
+cudaError_t timeline_set_buffer_attention(unsigned* p);
+cudaError_t timeline_set_buffer_pointwise(unsigned* p);
+cudaError_t timeline_set_buffer_decide(unsigned* p);
+#endif
+
 // ------------------------------------------------------------------ file-scope device words
 constexpr int kMaxDevices = 64;
 // Per-device cache of a file-scope __device__ variable's address, keyed by the context.

@@ -672,6 +672,20 @@ extern "C" {
 
 int lopa_version(void) { return 100; }
 
+#ifdef LOPA_TIMELINE
+// Timeline builds only: every instrumented kernel launched from now on appends its per-CTA
+// records to buf (device memory: a 16-byte header {count, capacity, 0, 0}, then capacity
+// records of lopa::tl::Rec); NULL stops recording.
+int lopa_timeline_set_buffer(void* buf) {
+  unsigned* p = static_cast<unsigned*>(buf);
+  cudaError_t e = timeline_set_buffer_gemm(p);
+  if (e == cudaSuccess) e = timeline_set_buffer_attention(p);
+  if (e == cudaSuccess) e = timeline_set_buffer_pointwise(p);
+  if (e == cudaSuccess) e = timeline_set_buffer_decide(p);
+  return e == cudaSuccess ? 0 : LOPA_ERR_CUDA;
+}
+#endif
+
 const char* lopa_last_error(const lopa_ctx* ctx) {
   return ctx ? ctx->err.c_str() : g_init_error.c_str();
 }

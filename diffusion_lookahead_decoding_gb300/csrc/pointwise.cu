@@ -2,8 +2,11 @@
 // residual add + RMSNorm, the LM-head partial merge, and the RoPE table.
 #include "common.cuh"
 #include "internal.h"
+#include "timeline.cuh"
 
 namespace lopa {
+
+LOPA_TL_UNIT(pointwise)
 
 namespace {
 
@@ -30,7 +33,10 @@ __device__ __forceinline__ void store8(bf16* p, const float (&f)[8]) {
 __global__ void embed_norm_kernel(const int* __restrict__ tok, int T, const bf16* __restrict__ E,
                                   const bf16* __restrict__ g, float* __restrict__ x,
                                   bf16* __restrict__ n, int d, float eps, int V, int* err) {
+  TL_DECL;
+  TL_START();
   pdl_wait();
+  TL_WAITED();
   pdl_trigger();
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -61,6 +67,7 @@ __global__ void embed_norm_kernel(const int* __restrict__ tok, int T, const bf16
     for (int i = 0; i < 8; ++i) f[i] = f[i] * rs * gg[i];
     store8(n + (size_t)t * d + c, f);
   }
+  TL_END(tl::EMBED_NORM);
 }
 
 // Block-wide sum; every thread gets the total.  blockDim.x is a multiple of 32, <= 1024.
@@ -83,7 +90,10 @@ __global__ void __launch_bounds__(512, 2)
                          size_t split_stride, const bf16* __restrict__ g, bf16* __restrict__ n,
                          int d, float eps) {
   __shared__ float red[32];
+  TL_DECL;
+  TL_START();
   pdl_wait();
+  TL_WAITED();
   pdl_trigger();
   const int t = blockIdx.x;
   const int c = threadIdx.x * 8;
@@ -134,6 +144,7 @@ __global__ void __launch_bounds__(512, 2)
                    : "memory");
     }
   }
+  TL_END(tl::RESIDUAL_NORM);
 }
 
 struct Stat {
@@ -157,7 +168,10 @@ __device__ __forceinline__ Stat merge(Stat a, Stat b) {
 __global__ void lm_merge_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
                                 const int* __restrict__ pi, int nvt, int part_ld, int T,
                                 int* __restrict__ am, float* __restrict__ mp) {
+  TL_DECL;
+  TL_START();
   pdl_wait();
+  TL_WAITED();
   pdl_trigger();
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -179,6 +193,7 @@ __global__ void lm_merge_kernel(const float* __restrict__ pm, const float* __res
     am[t] = acc.i;
     mp[t] = 1.0f / acc.s;
   }
+  TL_END(tl::LM_MERGE);
 }
 
 // cos/sin of pos * base^(-2j/dh), evaluated in double and rounded to fp32.

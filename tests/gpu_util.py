@@ -61,48 +61,61 @@ def f32(x):
 
 class Conditioning:
     """How much the oracle itself moves when only its accumulation precision changes
-    (float64 -> float32 sums, same bf16 storage).  A correct implementation with a
-    different summation order cannot be expected to agree more closely than this, so
-    the tolerances below never go under it (times 2)."""
+    (float64 -> float32 sums, same bf16 storage): a report printed beside the GPU-oracle
+    differences, never a tolerance.  It shows how far from the oracle any correct
+    implementation with another summation order lands on these random-weight models."""
 
     def __init__(self, ref, alt):
         self.mp = float(np.abs(alt.mp - ref.mp).max())
+        self.mp_pos = np.abs(alt.mp - ref.mp)
         self.hidden = rel_l2(alt.x_final, ref.x_final)
 
-    @property
-    def mp_bound(self):
-        return max(MP_ABS, 2.0 * self.mp)
-
-    @property
-    def hidden_bound(self):
-        return max(HIDDEN_REL_L2, 2.0 * self.hidden)
-
-    @property
-    def tie(self):
-        return max(NEAR_TIE, 2.0 * self.mp)
-
     def __repr__(self):
-        return f"oracle sensitivity: maxp {self.mp:.2e}, hidden {self.hidden:.2e}"
+        return f"oracle float32-vs-float64 movement: maxp {self.mp:.2e}, hidden {self.hidden:.2e}"
 
 
 def oracle_forward_pair(shape, w, prompt, branches, capacity, cache_weights=None):
     """Oracle forward of `branches` after prefilling `prompt`, with float64 and with
-    float32 accumulation.  Returns (model, cache, out, conditioning) of the float64 run."""
+    float32 accumulation.  Returns (model, cache, out, conditioning) of the float64 run
+    (its logits included)."""
     P = len(prompt)
     m = O.OracleModel(shape, w, act="bf16", cache_weights=cache_weights)
     cache = O.prefill(m, prompt, capacity)
-    out = O.forward(m, cache, P, branches)
+    out = O.forward(m, cache, P, branches, want_logits=True)
     m32 = O.OracleModel(shape, w, act="bf16", cache_weights=cache_weights, accum="fp32")
     c32 = O.prefill(m32, prompt, capacity)
     alt = O.forward(m32, c32, P, branches)
     return m, cache, out, Conditioning(out, alt)
 
 
-def tokens_ok(gpu_am, out, tie):
-    """Greedy tokens must match except where the oracle's top-2 probabilities differ by
-    less than `tie`.  Returns (ok, number of disallowed mismatches)."""
-    bad = (np.asarray(gpu_am) != np.asarray(out.am)) & ((out.mp - out.p2) >= tie)
-    return not bad.any(), int(bad.sum())
+def softmax_rows(z):
+    z = np.asarray(z, np.float64)
+    e = np.exp(z - z.max(axis=-1, keepdims=True))
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def token_flips(gpu_am, gpu_mp, out, mask_id=0):
+    """Greedy-token differences between the GPU and the oracle: (all, beyond the window).
+
+    At a position where the GPU picks token a and the oracle token b, the oracle's
+    probabilities (from its full logits, [MASK] excluded) give the gap p(b) - p(a) between
+    exactly those two tokens, and the GPU's max-probability is its probability of a, so
+    e_a = |mp_gpu - p_oracle(a)| is the measured error on a.  The flip needs the errors on
+    a and b together to exceed the gap; it is allowed where the gap is below max(1e-3,
+    2 e_a) (the error on b taken no larger than the one measured on a)."""
+    am = np.asarray(gpu_am).reshape(-1)
+    mp = np.asarray(gpu_mp, np.float64).reshape(-1)
+    oam = np.asarray(out.am).reshape(-1)
+    z = np.array(out.logits, np.float64).reshape(len(oam), -1)
+    z[:, mask_id] = -np.inf
+    flips = np.nonzero(am != oam)[0]
+    bad = 0
+    for i in flips:
+        p = softmax_rows(z[i])
+        gap = p[oam[i]] - p[am[i]]
+        if gap >= max(NEAR_TIE, 2.0 * abs(mp[i] - p[am[i]])):
+            bad += 1
+    return int(len(flips)), bad
 
 
 def seeded_branches(shape, nb, B, seed, masked=0.6):
