@@ -163,35 +163,51 @@ __device__ __forceinline__ Stat merge(Stat a, Stat b) {
 }
 
 // Merges the per-vocab-tile (max, sum exp, argmax) partials of each token row into the
-// greedy token and its probability maxp = 1 / sum exp(z - max z).  One warp per row,
-// fixed reduction order (deterministic).
-__global__ void lm_merge_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
-                                const int* __restrict__ pi, int nvt, int part_ld, int T,
-                                int* __restrict__ am, float* __restrict__ mp) {
+// greedy token and its probability maxp = 1 / sum exp(z - max z).  A CTA serves 32 rows
+// (lane = row, so the partial loads [tile][row] are coalesced); its kMergeWarps warps each
+// fold a contiguous range of vocabulary tiles, and warp 0 merges the warps' states in warp
+// order (a fixed order: deterministic).
+constexpr int kMergeWarps = 16;
+
+__global__ void __launch_bounds__(32 * kMergeWarps)
+    lm_merge_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
+                    const int* __restrict__ pi, int nvt, int part_ld, int T,
+                    int* __restrict__ am, float* __restrict__ mp) {
+  __shared__ Stat part[kMergeWarps][32];
   TL_DECL;
   TL_START();
   pdl_wait();
   TL_WAITED();
   pdl_trigger();
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int t = blockIdx.x * 32 + lane;
+  const int v0 = (int)((long long)w * nvt / kMergeWarps);
+  const int v1 = (int)((long long)(w + 1) * nvt / kMergeWarps);
   Stat acc{-INFINITY, 0.f, 0};
-  for (int v = lane; v < nvt; v += 32) {
-    const size_t o = (size_t)v * part_ld + t;
-    acc = merge(acc, Stat{pm[o], ps[o], pi[o]});
-  }
+  if (t < T) {
+    int v = v0;
+    for (; v + 4 <= v1; v += 4) {  // four tiles' loads in flight
+      Stat s4[4];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    Stat o;
-    o.m = __shfl_xor_sync(0xffffffffu, acc.m, off);
-    o.s = __shfl_xor_sync(0xffffffffu, acc.s, off);
-    o.i = __shfl_xor_sync(0xffffffffu, acc.i, off);
-    acc = (lane & off) ? merge(o, acc) : merge(acc, o);
+      for (int u = 0; u < 4; ++u) {
+        const size_t o = (size_t)(v + u) * part_ld + t;
+        s4[u] = Stat{pm[o], ps[o], pi[o]};
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc = merge(acc, s4[u]);
+    }
+    for (; v < v1; ++v) {
+      const size_t o = (size_t)v * part_ld + t;
+      acc = merge(acc, Stat{pm[o], ps[o], pi[o]});
+    }
   }
-  if (lane == 0) {
-    am[t] = acc.i;
-    mp[t] = 1.0f / acc.s;
+  part[w][lane] = acc;
+  __syncthreads();
+  if (w == 0 && t < T) {
+    Stat r = part[0][lane];
+    for (int j = 1; j < kMergeWarps; ++j) r = merge(r, part[j][lane]);
+    am[t] = r.i;
+    mp[t] = 1.0f / r.s;
   }
   TL_END(tl::LM_MERGE);
 }
@@ -238,8 +254,8 @@ cudaError_t launch_residual_norm(float* x, const float* part, int nsplit, size_t
 
 cudaError_t launch_lm_merge(const float* pm, const float* ps, const int* pi, int nvt,
                             int part_ld, int T, int* am, float* mp, cudaStream_t s) {
-  return launch_pdl(lm_merge_kernel, dim3((T + 7) / 8), dim3(256), 0, s, pm, ps, pi, nvt, part_ld,
-                    T, am, mp);
+  return launch_pdl(lm_merge_kernel, dim3((T + 31) / 32), dim3(32 * kMergeWarps), 0, s, pm, ps, pi,
+                    nvt, part_ld, T, am, mp);
 }
 
 cudaError_t launch_rope_table(float* cos_t, float* sin_t, int S, int dh, double base,
