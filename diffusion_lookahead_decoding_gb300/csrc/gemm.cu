@@ -80,26 +80,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The weight operand is A (128-row tiles) except for the LM head, where it is B.
   constexpr bool kWeightIsA = MODE != GEMM_LMSTATS;
 
-  // Tile coordinates.
+  // Tile coordinates.  The token box (LM head: token group) is the fastest-varying index of
+  // blockIdx.x: the zt CTAs that stream the same weight tile are launched together, so the
+  // tile crosses HBM once and the other CTAs' reads hit L2.
+  const int zt = a.zt > 0 ? a.zt : 1;
+  const int bx = blockIdx.x / zt, bz = blockIdx.x - bx * zt;
   int a_row[2];
   bool a_ok[2];
   int b_row;
   constexpr bool kCluster = MODE == GEMM_QKV;
   if (MODE == GEMM_RED_ADD || kCluster) {
-    a_row[0] = blockIdx.x * a.na * 128;
+    a_row[0] = bx * a.na * 128;
     a_row[1] = a_row[0] + 128;
-    b_row = blockIdx.z * a.nbox;
+    b_row = bz * a.nbox;
     a_ok[0] = a_row[0] < a.a_rows;
     a_ok[1] = a.na > 1 && a_row[1] < a.a_rows;
   } else if (MODE == GEMM_SWIGLU) {
-    a_row[0] = blockIdx.x * 128;
-    a_row[1] = a.F + blockIdx.x * 128;
-    b_row = blockIdx.z * a.nbox;
+    a_row[0] = bx * 128;
+    a_row[1] = a.F + bx * 128;
+    b_row = bz * a.nbox;
     a_ok[0] = a_ok[1] = true;
   } else {
-    a_row[0] = blockIdx.z * a.na * 128;
+    a_row[0] = bz * a.na * 128;
     a_row[1] = a_row[0] + 128;
-    b_row = blockIdx.x * a.nbox;
+    b_row = bx * a.nbox;
     a_ok[0] = a_row[0] < a.T;
     a_ok[1] = a.na > 1 && a_row[1] < a.T;
   }
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int P = a.dP ? *a.dP : 0;
       // Exchange region of split c, round i for this cluster (tile x, token block z).
       auto region = [&](int i, int c) {
-        return a.xws + ((((size_t)blockIdx.z * gridDim.x + blockIdx.x) * 2 + i) * S + c) *
+        return a.xws + ((((size_t)bz * (gridDim.x / zt) + bx) * 2 + i) * S + c) *
                            (size_t)a.nbox * 128;
       };
       cluster_wait();  // every peer's mbarriers are initialised
@@ -472,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Each warp pair (same lane quarter) scans alternate 16-column chunks of the
         // 256-row vocabulary tile; the two running (max, sum exp, argmax) states of a
         // token are merged through shared memory.
-        const int vt = blockIdx.x;
+        const int vt = bx;
         float* xm = stage;
         float* xs = stage + 128;
         int* xi = reinterpret_cast<int*>(stage + 256);
@@ -704,7 +708,8 @@ const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_all
     a.splits = 1;
     if (!make_tmap_bf16(&L->mapA, act, act_rows_alloc, K, 128, err, sizeof(err))) return err;
     if (!weight_map(&L->mapB, 256)) return err;
-    L->grid = dim3((n_rows_w + 255) / 256, 1, (T + na * 128 - 1) / (na * 128));
+    a.zt = (T + na * 128 - 1) / (na * 128);
+    L->grid = dim3((n_rows_w + 255) / 256 * a.zt, 1, 1);
     a.w_slot_bytes = round1k(a.nbox * 128);
     a.x_slot_bytes = round1k(a.na * a.a_tile_bytes);
   } else {
@@ -728,7 +733,8 @@ const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_all
     if (!weight_map(&L->mapA, 128)) return err;
     if (!make_tmap_bf16(&L->mapB, act, act_rows_alloc, K, tok_box, err, sizeof(err))) return err;
     const int gx = (mode == GEMM_SWIGLU) ? (n_rows_w / 2) / 128 : (n_rows_w + a.na * 128 - 1) / (a.na * 128);
-    L->grid = dim3(gx, a.splits, (T + tok_box - 1) / tok_box);
+    a.zt = (T + tok_box - 1) / tok_box;
+    L->grid = dim3(gx * a.zt, a.splits, 1);
     a.w_slot_bytes = round1k(a.na * a.a_tile_bytes);
     a.x_slot_bytes = round1k(a.nbox * 128);
   }

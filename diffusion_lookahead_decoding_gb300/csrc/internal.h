@@ -122,6 +122,8 @@ struct GemmArgs {
   float* xws;        // QKV: split-K exchange workspace (see qkv_exchange_floats)
   int* err;
   int w_packed;      // weight operand in tile-major layout (see launch_pack_tiles)
+  int zt;            // token boxes (LM head: token groups); grid.x = tiles x zt with the box
+                     // index fastest, so the CTAs sharing a weight tile run side by side
   unsigned long long wait_ns;  // limit of every device-side wait (0 = the 2 s default)
 };
 

@@ -42,7 +42,7 @@ def test_linear_accumulate_matches_oracle(T, N, K):
 
 @pytest.mark.parametrize("rows,d,V,mask", [(64, 128, 1024, 0), (160, 1024, 32768, 0),
                                            (37, 256, 1000, 5), (256, 512, 4096, 0),
-                                           (200, 3584, 152064, 0)])
+                                           (300, 512, 4096, 3), (200, 3584, 152064, 0)])
 def test_lmhead_argmax_matches_oracle(rows, d, V, mask):
     from diffusion_lookahead_decoding_gb300 import api
     h = _bf16((rows, d), 4)
