@@ -203,8 +203,10 @@ size_t partial_floats(const lopa_ctx* ctx, int T) {
 // Picks the most CTAs that are resident at once (all tiles in one wave), then the larger
 // na (fewer activation re-reads), then the smaller cluster (less exchange).  When no
 // choice fits one wave, na = 2 and cs = 1.
+int qkv_box(int T) { return std::min(256, round16(T)); }
+
 void qkv_tiling(const lopa_ctx* ctx, int nrows, int K, int T, int* na, int* cs) {
-  const int tok_box = std::min(256, round16(T));
+  const int tok_box = qkv_box(T);
   const int zt = (T + tok_box - 1) / tok_box;
   int best = 0;
   *na = 2;
@@ -250,7 +252,8 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
       proj_tiling(nrows, K, p.T, ctx->num_sms, &na, &splits);
       while (splits > 1 && (size_t)splits * p.T * nrows > ctx->part_floats) --splits;
     }
-    const char* e = plan_gemm(&G, mode, act, ctx->Tmax, p.T, w, nrows, K, na, splits, p.tok_box,
+    const char* e = plan_gemm(&G, mode, act, ctx->Tmax, p.T, w, nrows, K, na, splits,
+                              mode == GEMM_QKV ? qkv_box(p.T) : p.tok_box,
                               ctx->num_sms, /*w_packed=*/true);
     if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s GEMM: %s", what, e);
     if (mode == GEMM_RED_ADD) {
@@ -502,7 +505,7 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
     auto need = [&](int T2) {
       int na, cs;
       qkv_tiling(ctx, ctx->qkv_rows, d, T2, &na, &cs);
-      const int nbox = std::min(256, round16(T2));
+      const int nbox = qkv_box(T2);
       const int gx = (ctx->qkv_rows + na * 128 - 1) / (na * 128);
       return qkv_exchange_floats(gx, cs, (T2 + nbox - 1) / nbox, nbox);
     };

@@ -94,26 +94,44 @@ def softmax_rows(z):
     return e / e.sum(axis=-1, keepdims=True)
 
 
-def token_flips(gpu_am, gpu_mp, out, mask_id=0):
+def token_flips(gpu_am, gpu_mp, out, mask_id=0, gpu_hidden=None, shape=None, weights=None):
     """Greedy-token differences between the GPU and the oracle: (all, beyond the window).
 
     At a position where the GPU picks token a and the oracle token b, the oracle's
-    probabilities (from its full logits, [MASK] excluded) give the gap p(b) - p(a) between
-    exactly those two tokens, and the GPU's max-probability is its probability of a, so
-    e_a = |mp_gpu - p_oracle(a)| is the measured error on a.  The flip needs the errors on
-    a and b together to exceed the gap; it is allowed where the gap is below max(1e-3,
-    2 e_a) (the error on b taken no larger than the one measured on a)."""
+    probabilities (its full logits, [MASK] excluded) give the gap p(b) - p(a) between
+    exactly those two tokens; the GPU's max-probability is its probability of a, so
+    e_a = |mp_gpu - p_oracle(a)| is measured.  With the GPU's final hidden state (and the
+    model's final-norm gain and LM head), the GPU's logits of a and b are recomputed from
+    it, which measures e_b as well: the flip is allowed where the gap is below
+    max(1e-3, e_a + e_b) - by the triangle inequality that holds whenever the GPU's own
+    logits rank a over b, so a position beyond it means the fused LM head's argmax
+    disagrees with its own input.  Without the hidden state the error on b is taken equal
+    to the one measured on a (window 2 e_a): a report, not a bound."""
     am = np.asarray(gpu_am).reshape(-1)
     mp = np.asarray(gpu_mp, np.float64).reshape(-1)
     oam = np.asarray(out.am).reshape(-1)
     z = np.array(out.logits, np.float64).reshape(len(oam), -1)
     z[:, mask_id] = -np.inf
+    hid = None if gpu_hidden is None else np.asarray(gpu_hidden, np.float64).reshape(len(oam), -1)
     flips = np.nonzero(am != oam)[0]
     bad = 0
     for i in flips:
         p = softmax_rows(z[i])
-        gap = p[oam[i]] - p[am[i]]
-        if gap >= max(NEAR_TIE, 2.0 * abs(mp[i] - p[am[i]])):
+        a, b = int(am[i]), int(oam[i])
+        gap = p[b] - p[a]
+        e_a = abs(mp[i] - p[a])
+        window = 2.0 * e_a
+        if hid is not None:
+            import torch
+            x = hid[i]
+            g = weights["final_norm"].to(torch.float64).numpy()
+            n = x / np.sqrt(np.mean(x * x) + shape.rms_eps) * g
+            n = torch.from_numpy(n).to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+            W = weights["lm_head"][[a, b]].to(torch.float64).numpy()
+            zg = shape.logit_scale * (W @ n)
+            p_b_gpu = mp[i] * np.exp(zg[1] - zg[0])
+            window = e_a + abs(p_b_gpu - p[b])
+        if gap >= max(NEAR_TIE, window):
             bad += 1
     return int(len(flips)), bad
 

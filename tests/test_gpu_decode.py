@@ -50,7 +50,7 @@ def test_verify_forward_matches_oracle(name):
     _, _, out, cond = oracle_forward_pair(shape, w, prompt, br, P + B)
     e_h = rel_l2(hid, out.x_final)
     e_mp = float(np.abs(mp - out.mp).max())
-    nflip, nbad = token_flips(am, mp, out, shape.mask_id)
+    nflip, nbad = token_flips(am, mp, out, shape.mask_id, hid, shape, w)
     print(f"{name}: hidden relL2 {e_h:.2e} (bound {HIDDEN_REL_L2}), maxp max|d| {e_mp:.2e} "
           f"(stated {MP_ABS}{'' if name in MP_STATED else ', not asserted'}), greedy-token "
           f"flips {nflip}, beyond their per-position window {nbad}; {cond}")
@@ -343,3 +343,41 @@ def test_timed_forwards_leave_the_decode_unchanged(wl):
     with pytest.raises(L.LopaError) as e:
         dec.time_forward(1, 1)  # the decode filled the cache
     assert e.value.code == L.ERR_BAD_STATE
+
+
+def test_prompt_of_2048_tokens_matches_oracle():
+    """A 2048-token prompt (eight 256-row token boxes per projection, one weight pass for
+    all of them) on the small model: the prompt's K/V in the static cache against the
+    oracle's prefill, a verification forward after it against the oracle's, and the first
+    LoPA iterations step by step."""
+    import dataclasses
+    from diffusion_lookahead_decoding_gb300 import api
+    shape, dshape, w = workload_weights("small")
+    P, B = 2048, dshape.block
+    ds = dataclasses.replace(dshape, prompt_len=P, gen_len=2 * B)
+    dec = api.LopaDecoder(shape, device_weights("small"), B, dshape.k, dshape.tau, P, P + 2 * B)
+    prompt = synth.make_prompt(shape, P, seed=3)
+    dec.prefill(prompt)
+    m = O.OracleModel(shape, w, act="bf16")
+    cache = O.prefill(m, prompt, P + 2 * B)
+    for l in (0, shape.n_layers - 1):
+        kg, vg = dec.read_kv(l, 0, P)
+        for what, got, ref in (("K", kg, cache.k[l][:P]), ("V", vg, cache.v[l][:P])):
+            err = np.abs(got - ref)
+            print(f"prompt 2048, layer {l} {what}: relL2 {rel_l2(got, ref):.2e}, max|d| "
+                  f"{err.max():.2e}, mean|d| {err.mean():.2e}")
+            assert rel_l2(got, ref) <= HIDDEN_REL_L2, (l, what)
+    br = seeded_branches(shape, dshape.k + 1, B, seed=9)
+    am, mp, hid = dec.verify_forward(br, want_hidden=True)
+    out = O.forward(m, cache, P, br, want_logits=True)
+    e_h = rel_l2(hid, out.x_final)
+    nflip, nbad = token_flips(am, mp, out, shape.mask_id, hid, shape, w)
+    print(f"prompt 2048: hidden relL2 {e_h:.2e}, maxp max|d| {np.abs(mp - out.mp).max():.2e}, "
+          f"flips {nflip} (beyond window {nbad})")
+    assert e_h <= HIDDEN_REL_L2 and nbad == 0
+    import copy
+    summ = steplocal.run(dec, m, shape, ds, prompt, dshape.k, max_steps=3,
+                         oracle_prompt_cache=copy.deepcopy(cache))
+    print(summ.table_row("small, prompt 2048, first 3 iterations"))
+    assert summ.n == 3
+    dec.close()

@@ -24,10 +24,10 @@ from tests.gpu_util import (HIDDEN_REL_L2, MP_ABS, make_decoder, oracle_forward_
 pytestmark = pytest.mark.gpu
 
 
-def _report(tag, hid, mp, am, out, cond):
+def _report(tag, hid, mp, am, out, cond, shape, w):
     e_h = rel_l2(hid, out.x_final)
     d = np.abs(mp - out.mp)
-    nflip, nbad = token_flips(am, mp, out, 0)
+    nflip, nbad = token_flips(am, mp, out, 0, hid, shape, w)
     well = cond.mp_pos < 0.1 * MP_ABS
     print(f"{tag}: hidden relL2 {e_h:.2e} (bound {HIDDEN_REL_L2}); maxp |d| max {d.max():.2e}, "
           f"mean {d.mean():.2e}, positions over {MP_ABS}: {(d > MP_ABS).sum()} of {d.size}; at the "
@@ -47,7 +47,7 @@ def test_dream7b_one_layer_all_rows():
     br = seeded_branches(shape, k + 1, B, seed=5)
     am, mp, hid = dec.verify_forward(br, want_hidden=True)
     _, _, out, cond = oracle_forward_pair(shape, w, prompt, br, P + B)
-    e_h, d, nbad = _report("7B one layer, 256 rows", hid, mp, am, out, cond)
+    e_h, d, nbad = _report("7B one layer, 256 rows", hid, mp, am, out, cond, shape, w)
     dec.close()
     assert e_h <= HIDDEN_REL_L2
     assert nbad == 0
@@ -83,9 +83,10 @@ def test_dream7b_verification_sampled(dream7b_oracle):
     g_am = np.stack([am0[0], am[0], am[k]])
     g_mp = np.stack([mp0[0], mp[0], mp[k]])
     g_h = np.stack([hid0[0], hid[0], hid[k]])
-    e_h, _, _ = _report("7B 28 layers, block-start rows + branches 0 and 7", g_h, g_mp, g_am, out,
-                        cond)
+    e_h, _, nbad = _report("7B 28 layers, block-start rows + branches 0 and 7", g_h, g_mp, g_am,
+                           out, cond, shape, w)
     assert e_h <= HIDDEN_REL_L2
+    assert nbad == 0
 
 
 def test_dream7b_four_iterations_step_local(dream7b_oracle):
