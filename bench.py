@@ -37,10 +37,11 @@ UNIT = "tokens/s"
 # with summation order).  The reference arm's line labels it as assumed.  The oracle's own
 # TPF is measured on the tiny and small workloads (oracle_decodes in the default run).
 ASSUMED_TPF = {"dream7b": 8.4, "dream7b_scaling": 8.4}
-# DRAM bytes (read + write) of one gemm_kernel<SWIGLU> launch at the 7B step shape, from
-# the ncu launch list of the decode (271.60 MB read + 1.11 MB written).  It describes the
-# kernel as it was profiled and must be re-taken (or set to None) when the kernel changes.
-SWIGLU_TRAFFIC_BYTES = 272.71e6
+# DRAM bytes (read + write) of one gemm_kernel<SWIGLU> launch at the 7B step shape (256 rows),
+# from ncu on the one-layer slice (profiles/gemm_swiglu_dream7b_layer.md: 273.46 MB read,
+# 1.38 MB written on average over two launches).  It describes the kernel as it was
+# profiled and must be re-taken (or set to None) when the kernel changes.
+SWIGLU_TRAFFIC_BYTES = 274.84e6
 
 
 def dist_env():
@@ -585,8 +586,8 @@ def main():
     roofline = {"kernel": "gemm_kernel<SWIGLU> (gate/up + SwiGLU)", "bound": "hbm",
                 "achieved": dom["GB/s"], "peak": peak_bw, "unit": "GB/s",
                 "frac": dom["GB/s"] / peak_bw, "traffic": SWIGLU_TRAFFIC_BYTES,
-                "traffic_source": "ncu launch list of the decode: dram__bytes_read.sum + "
-                                  "dram__bytes_write.sum per launch",
+                "traffic_source": "ncu on the one-layer 7B slice at the step shape: "
+                                  "dram__bytes_read.sum + dram__bytes_write.sum per launch",
                 "peak_source": peak_src}
 
     # Verification-step latency: the forward-only graph of the 8-branch verification (and
