@@ -45,7 +45,7 @@ import math
 import numpy as np
 
 __all__ = [
-    "bf16_round", "rmsnorm", "rope", "silu", "linear", "isolated_attention", "logit_summary", "OracleModel", "prefill",
+    "bf16_round", "e4m3_round", "quantize_e4m3_rows", "QUANTIZED_WEIGHTS", "rmsnorm", "rope", "silu", "linear", "isolated_attention", "logit_summary", "OracleModel", "prefill",
     "forward", "anchor_fill", "lookahead_candidates", "build_branches",
     "branch_confidence", "select_winner", "decision_margins", "lopa_step", "decode",
     "StepRecord",
@@ -77,6 +77,48 @@ def bf16_round(x):
 
 def _identity(x):
     return np.asarray(x, dtype=np.float64)
+
+
+# E4M3: the 8-bit float with 1 sign, 4 exponent (bias 7) and 3 fraction bits.  It has no
+# infinities; the pattern S.1111.111 is NaN, so the largest finite magnitude is
+# 2^8 * 1.75 = 448.  Exponent field 0 holds the subnormals m/8 * 2^-6.
+E4M3_MAX = 448.0
+
+
+def e4m3_round(x):
+    """Round float64 values to the nearest E4M3 value, ties to even; magnitudes beyond
+    448 saturate to 448 (a finite-saturating conversion: a quantised weight is never
+    NaN).  Within the binade [2^e, 2^(e+1)), e >= -6, the E4M3 grid has spacing
+    2^(e-3); below 2^-6 it is the subnormal spacing 2^-9."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, ex = np.frexp(a)                      # a = f * 2^ex, 0.5 <= f < 1: binade e = ex - 1
+    e = np.maximum(ex.astype(np.int64) - 1, -6)
+    spacing = np.ldexp(1.0, e - 3)
+    q = np.round(a / spacing) * spacing      # exact scaling by a power of two; half to even
+    q = np.minimum(q, E4M3_MAX)
+    return np.copysign(q, x).reshape(x.shape)
+
+
+def quantize_e4m3_rows(W):
+    """Per-output-channel E4M3 quantisation of a weight [out_features][in_features].
+
+    Reading (the pages name FP16/INT8 switching for the NVIDIA system and a quantisation
+    mechanism without a format): each row r gets the scale s_r = max|W_r| / 448 and the
+    codes c = E4M3(W_r / s_r); the row is used as c * s_r.  The scale and the quotient
+    are both formed in float32 (the precision in which the codes are decided); an
+    all-zero row gets s_r = 1.  Returns (codes as float64 values, scales as float64
+    holding the float32 values)."""
+    W32 = np.asarray(W, dtype=np.float32)
+    amax = np.max(np.abs(W32), axis=1)
+    s = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    codes = e4m3_round((W32 / s[:, None]).astype(np.float64))
+    return codes, s.astype(np.float64)
+
+
+# Weights that the E4M3 weight stream quantises (per layer and the LM head); the
+# embedding table and the norm gains stay bf16.
+QUANTIZED_WEIGHTS = ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "lm_head")
 
 
 # ----------------------------------------------------------------------------------
@@ -167,13 +209,19 @@ class OracleModel:
     format.  ``act='bf16'`` rounds every tensor that the decoding path stores (GEMM
     inputs, q/k/v and the KV cache, attention output, MLP hidden, final normed
     hidden) to bf16, as the workload's "bf16 weights/activations" states; arithmetic
-    stays float64.  ``act='fp64'`` keeps everything float64."""
+    stays float64.  ``act='fp64'`` keeps everything float64.  ``weights='e4m3'`` uses
+    every projection matrix and the LM head as its per-row E4M3 quantisation
+    (quantize_e4m3_rows: codes times scale, exact in float64)."""
 
-    def __init__(self, shape, weights, act="bf16", cache_weights=None, accum="fp64"):
+    def __init__(self, shape, weights, act="bf16", cache_weights=None, accum="fp64",
+                 weight_format="bf16"):
+        if weight_format not in ("bf16", "e4m3"):
+            raise ValueError(weight_format)
         self.shape = shape
         self._w = weights  # name -> torch bf16 CPU tensor or numpy array
         self.act = act
         self.accum = accum
+        self.weight_format = weight_format
         self.rnd = bf16_round if act == "bf16" else _identity
         if cache_weights is None:
             cache_weights = shape.streamed_params() < 400_000_000
@@ -188,6 +236,9 @@ class OracleModel:
             a = t.to(torch.float64).numpy()
         else:
             a = np.asarray(t, dtype=np.float64)
+        if self.weight_format == "e4m3" and name.split(".")[0] in QUANTIZED_WEIGHTS:
+            codes, s = quantize_e4m3_rows(a)
+            a = codes * s[:, None]
         if self._cache is not None:
             self._cache[name] = a
         return a
