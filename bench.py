@@ -160,7 +160,8 @@ def bench_config(args, shape, dshape, world):
             "prompt": dshape.prompt_len, "gen_len": dshape.gen_len, "block": dshape.block,
             "branches": dshape.k + 1, "tau": dshape.tau,
             "parallelism": "replicas" if world > 1 else "single",
-            "l2": "inputs larger than L2 (15 GB weights re-streamed per forward)"}
+            "l2": "inputs larger than L2 (15 GB weights re-streamed per forward)",
+            "weights": getattr(args, "weight_format", "bf16")}
 
 
 def oracle_decode_run(name, threads, max_blocks=None):
@@ -274,18 +275,20 @@ def run_reference(args):
     }), flush=True)
 
 
-def gemm_bytes(shape, T, kind):
-    """Algorithmic HBM bytes of one launch: weights once, activations in, outputs out."""
+def gemm_bytes(shape, T, kind, wb=2):
+    """Algorithmic HBM bytes of one launch: weights once (wb bytes per weight: 2 for bf16,
+    1 for E4M3 codes, plus 4 bytes of scale per weight row), activations in, outputs out."""
     d, F, V = shape.d_model, shape.ffn, shape.vocab
+    sc = 4 if wb == 1 else 0
     if kind == 0:
-        return 2 * shape.qkv_rows * d + 2 * T * d + 4 * T * shape.qkv_rows
+        return (wb * d + sc) * shape.qkv_rows + 2 * T * d + 4 * T * shape.qkv_rows
     if kind == 1:
-        return 2 * d * shape.n_heads * shape.head_dim + 2 * T * shape.n_heads * shape.head_dim + 4 * T * d
+        return (wb * shape.n_heads * shape.head_dim + sc) * d + 2 * T * shape.n_heads * shape.head_dim + 4 * T * d
     if kind == 2:
-        return 2 * 2 * F * d + 2 * T * d + 2 * T * F
+        return (wb * d + sc) * 2 * F + 2 * T * d + 2 * T * F
     if kind == 3:
-        return 2 * d * F + 2 * T * F + 4 * T * d
-    return 2 * V * d + 2 * T * d + 12 * T * ((V + 255) // 256)
+        return (wb * F + sc) * d + 2 * T * F + 4 * T * d
+    return (wb * d + sc) * V + 2 * T * d + 12 * T * ((V + 255) // 256)
 
 
 def gemm_flops(shape, T, kind):
@@ -295,16 +298,18 @@ def gemm_flops(shape, T, kind):
     return 2 * n * T
 
 
-def verify_bytes_flops(shape, T, P, B):
+def verify_bytes_flops(shape, T, P, B, wb=2):
     """Algorithmic bytes and flops of one verification forward over T token rows (blocks
-    of B) at prefix P: every weight read once (projections and LM head, bf16), the prefix
-    K/V read once and the block K/V written once (bf16); 2 flops per weight per row plus
-    the attention's q.k and p.v (4 per query, key and dimension, P + B keys per query)."""
+    of B) at prefix P: every weight read once (projections and LM head; wb bytes per weight,
+    2 for bf16, 1 for E4M3 codes plus 4 bytes of scale per row), the prefix K/V read once and
+    the block K/V written once (bf16); 2 flops per weight per row plus the attention's q.k
+    and p.v (4 per query, key and dimension, P + B keys per query)."""
     L, d, H, Hk, dh, F, V = (shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads,
                              shape.head_dim, shape.ffn, shape.vocab)
     params = L * (d * H * dh + 2 * d * Hk * dh + H * dh * d + 3 * d * F) + V * d
+    rows = L * (H * dh + 2 * Hk * dh + d + 2 * F + d) + V
     kv = L * 2 * Hk * dh * 2
-    by = 2 * params + P * kv + T * kv
+    by = wb * params + (4 * rows if wb == 1 else 0) + P * kv + T * kv
     fl = 2 * params * T + 4 * L * H * dh * T * (P + B)
     return by, fl
 
@@ -315,6 +320,52 @@ def prefill_flops(shape, P):
     L = shape.n_layers
     proj = sum(gemm_flops(shape, P, kind) for kind in range(4))
     return L * (proj + 4 * shape.n_heads * shape.head_dim * P * P)
+
+
+def e4m3_summary(api, shape, dshape, dev_w, prompt, peak_bw, peak_tc, steps):
+    """The same workload with the E4M3 weight stream (a second context quantising the same
+    device weights): decode tokens/s and TPF over `steps` decodes after one warm-up, the
+    verification forward against its roofline on the halved weight bytes, the block-start
+    forward, and the gate/up GEMM and LM head."""
+    import torch
+    B, P0, gen = dshape.block, dshape.prompt_len, dshape.gen_len
+    dec = api.LopaDecoder(shape, dev_w, B, dshape.k, dshape.tau, P0, P0 + gen, weight_format="e4m3")
+    dec.prefill(prompt)
+    dec.rewind(P0)
+    dec.decode(gen)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(dec.stream)
+    toks = fw = 0
+    for _ in range(steps):
+        dec.rewind(P0)
+        _, st = dec.decode(gen)
+        toks += st["tokens"]
+        fw += st["forwards"]
+    ev1.record(dec.stream)
+    torch.cuda.synchronize()
+    sec = ev0.elapsed_time(ev1) / 1e3
+    T = (dshape.k + 1) * B
+    Pv = P0 + (gen // 2 // B) * B
+    dec.rewind(Pv)
+    v_med, _ = dec.time_forward(1, 50)
+    s_med, _ = dec.time_forward(0, 50)
+    vb, vf = verify_bytes_flops(shape, T, Pv, B, 1)
+    gu = dec.time_gemm(2, 2 * shape.n_layers)
+    lm = dec.time_gemm(4, 8)
+    dec.close()
+    gb = gemm_bytes(shape, T, 2, 1)
+    lb = gemm_bytes(shape, T, 4, 1)
+    return {"tokens_per_s": toks / sec, "tpf": toks / fw, "ms_per_forward": sec * 1e3 / fw,
+            "decodes": steps,
+            "verify_step": {"ms_median": v_med, "prefix": Pv, "rows": T, "bytes": vb,
+                            "hbm_roofline_ms": vb / peak_bw / 1e6,
+                            "tensor_roofline_ms": vf / peak_tc / 1e9,
+                            "frac_hbm_roofline": vb / peak_bw / 1e6 / v_med,
+                            "block_start_forward_ms_median": s_med},
+            "gate_up_swiglu": {"ms": gu, "GB/s": gb / gu / 1e6, "frac_hbm": gb / gu / 1e6 / peak_bw,
+                               "TFLOP/s": gemm_flops(shape, T, 2) / gu / 1e9},
+            "lm_head": {"ms": lm, "GB/s": lb / lm / 1e6, "TFLOP/s": gemm_flops(shape, T, 4) / lm / 1e9}}
 
 
 def _peaks():
@@ -345,7 +396,7 @@ def sweep_branches(args):
     for k in (0, 1, 3, 7, 15):
         ds = dataclasses.replace(dshape, k=k)
         B, P0, gen = ds.block, ds.prompt_len, ds.gen_len
-        dec = api.LopaDecoder(shape, dw, B, k, ds.tau, P0, P0 + gen)
+        dec = api.LopaDecoder(shape, dw, B, k, ds.tau, P0, P0 + gen, weight_format=args.weight_format)
         dec.prefill(prompt)
         dec.decode(gen)  # warm-up
         times, stats = [], None
@@ -363,7 +414,7 @@ def sweep_branches(args):
         dec.rewind(Pv)
         v_med, _ = dec.time_forward(1, 30)
         T = (k + 1) * B
-        vb, vf = verify_bytes_flops(shape, T, Pv, B)
+        vb, vf = verify_bytes_flops(shape, T, Pv, B, 1 if args.weight_format == "e4m3" else 2)
         t_hbm, t_tc = vb / bw / 1e6, vf / tc_s / 1e9
         rows.append({"k": k, "branches": k + 1, "tok_per_s": gen / sec,
                      "tpf": stats["tokens"] / stats["forwards"],
@@ -375,6 +426,7 @@ def sweep_branches(args):
         dec.close()
         print(json.dumps(rows[-1]), flush=True)
     print(json.dumps({"sweep_branches": rows, "workload": "dream7b_scaling", "prompt": dshape.prompt_len,
+                      "weights": args.weight_format,
                       "gen_len": dshape.gen_len, "peaks": {"hbm_gbs": bw, "bf16_tflops_sustained": tc_s,
                                                            "source": src}}), flush=True)
 
@@ -459,6 +511,8 @@ def main():
                     help="branch-scaling table on the 2048-token-prompt workload, k in 0,1,3,7,15")
     ap.add_argument("--microbench", action="store_true",
                     help="attention + LM-head grid: branches x block x prefix")
+    ap.add_argument("--weight-format", default="bf16", choices=["bf16", "e4m3"],
+                    help="weights the GEMMs stream: bf16, or per-row-scaled E4M3 codes")
     ap.add_argument("--profile-attention", type=int, default=None, metavar="PREFIX",
                     help="only the branch attention of the workload's verification step over a "
                          "PREFIX-key prefix: 3 + 20 launches, CUDA-event time (small ncu case)")
@@ -517,7 +571,9 @@ def main():
         del weights
         weights = None
     t_gen = time.perf_counter() - t_gen
-    dec = api.LopaDecoder(shape, dev_w, B, dshape.k, dshape.tau, P0, P0 + gen)
+    dec = api.LopaDecoder(shape, dev_w, B, dshape.k, dshape.tau, P0, P0 + gen,
+                          weight_format=args.weight_format)
+    wb = 1 if args.weight_format == "e4m3" else 2
     if args.profile_gemm is not None:
         ms = dec.time_gemm(args.profile_gemm, 3)
         print(json.dumps({"profile_gemm": args.profile_gemm, "ms": ms}), flush=True)
@@ -574,7 +630,7 @@ def main():
     for kind, name in enumerate(["qkv", "o_proj", "gate_up_swiglu", "down", "lm_head"]):
         iters_k = 2 * shape.n_layers if kind < 4 else 8
         ms = dec.time_gemm(kind, iters_k)
-        by, fl = gemm_bytes(shape, T, kind), gemm_flops(shape, T, kind)
+        by, fl = gemm_bytes(shape, T, kind, wb), gemm_flops(shape, T, kind)
         kern[name] = {"ms": ms, "GB/s": by / ms / 1e6, "TFLOP/s": fl / ms / 1e9}
     peaks = {}
     try:
@@ -585,7 +641,8 @@ def main():
     dom = kern["gate_up_swiglu"]
     roofline = {"kernel": "gemm_kernel<SWIGLU> (gate/up + SwiGLU)", "bound": "hbm",
                 "achieved": dom["GB/s"], "peak": peak_bw, "unit": "GB/s",
-                "frac": dom["GB/s"] / peak_bw, "traffic": SWIGLU_TRAFFIC_BYTES,
+                "frac": dom["GB/s"] / peak_bw,
+                "traffic": SWIGLU_TRAFFIC_BYTES if wb == 2 else None,
                 "traffic_source": "ncu on the one-layer 7B slice at the step shape: "
                                   "dram__bytes_read.sum + dram__bytes_write.sum per launch",
                 "peak_source": peak_src}
@@ -598,7 +655,7 @@ def main():
     dec.rewind(Pv)
     v_med, v_mean = dec.time_forward(1, 50)
     s_med, _ = dec.time_forward(0, 50)
-    vb, vf = verify_bytes_flops(shape, T, Pv, B)
+    vb, vf = verify_bytes_flops(shape, T, Pv, B, wb)
     peak_tc = float(peaks.get("bf16_tflops_sustained", 1700.0)) if peaks else 1700.0
     t_hbm, t_tc = vb / peak_bw / 1e6, vf / peak_tc / 1e9
     verify = {"ms_median": v_med, "ms_mean": v_mean, "prefix": Pv, "rows": T,
@@ -650,6 +707,9 @@ def main():
                           f"head, extrapolated to {shape.n_layers} layers = {spf:.1f} s/forward; "
                           f"tokens/s at the measured TPF {tpf:.2f}")}
     dec.close()
+    e4m3 = None
+    if args.weight_format == "bf16" and rank == 0:
+        e4m3 = e4m3_summary(api, shape, dshape, dev_w, prompt, peak_bw, peak_tc, max(1, args.steps // 2))
     odec = oracle_decodes() if (rank == 0 and not args.no_cpu_baseline) else None
     if rank == 0:
         out = {
@@ -663,7 +723,7 @@ def main():
             "lopa_iterations": iters, "blocks": blocks, "forwards": forwards,
             "verify_step": verify, "prefill": prefill,
             "kernels": kern, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "oracle_decodes": odec,
+            "oracle_decodes": odec, "e4m3_weights": e4m3,
             "gpu_launches": gpu_launches, "clocks": clocks.summary(),
             "weight_gen_s": t_gen,
         }

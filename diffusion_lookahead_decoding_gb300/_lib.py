@@ -25,7 +25,12 @@ class ModelConfig(C.Structure):
     _fields_ = [("n_layers", C.c_int), ("d_model", C.c_int), ("n_heads", C.c_int),
                 ("n_kv_heads", C.c_int), ("head_dim", C.c_int), ("ffn", C.c_int),
                 ("vocab", C.c_int), ("mask_id", C.c_int), ("max_seq", C.c_int),
-                ("rope_base", C.c_float), ("rms_eps", C.c_float), ("logit_scale", C.c_float)]
+                ("rope_base", C.c_float), ("rms_eps", C.c_float), ("logit_scale", C.c_float),
+                ("weight_format", C.c_int)]
+
+
+WEIGHTS_BF16, WEIGHTS_E4M3 = 0, 1
+WEIGHT_FORMATS = {"bf16": WEIGHTS_BF16, "e4m3": WEIGHTS_E4M3}
 
 
 LAYER_WEIGHTS = ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "wg", "wu", "wd")
@@ -79,6 +84,10 @@ SIGNATURES = {
                                     C.POINTER(C.c_float)]),
     "lopa_linear_accumulate": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
                                          C.c_int, C.c_void_p]),
+    "lopa_quantize_e4m3": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p,
+                                     C.c_void_p]),
+    "lopa_linear_accumulate_e4m3": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                              C.c_int, C.c_int, C.c_int, C.c_void_p]),
     "lopa_lmhead_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int]),
     "lopa_lmhead_argmax": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                      C.c_float, C.c_int, C.c_void_p, C.c_size_t, C.c_void_p,

@@ -45,7 +45,8 @@ class LopaDecoder:
     """One decoding context: static KV cache, branch scratch, state, captured graphs."""
 
     def __init__(self, shape, dev_weights: dict, block: int, k: int, tau: float,
-                 max_prompt: int, max_seq: int, stream: torch.cuda.Stream | None = None):
+                 max_prompt: int, max_seq: int, stream: torch.cuda.Stream | None = None,
+                 weight_format: str = "bf16"):
         self.lib = L.load()
         self.shape = shape
         self.block = block
@@ -54,7 +55,9 @@ class LopaDecoder:
         self.stream = stream or torch.cuda.Stream()
         mc = L.ModelConfig(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads,
                            shape.head_dim, shape.ffn, shape.vocab, shape.mask_id, max_seq,
-                           shape.rope_base, shape.rms_eps, shape.logit_scale)
+                           shape.rope_base, shape.rms_eps, shape.logit_scale,
+                           L.WEIGHT_FORMATS[weight_format])
+        self.weight_format = weight_format
         n = shape.n_layers
         arr = lambda key: (C.c_void_p * n)(*[dev_weights[f"{key}.{l}"].data_ptr() for l in range(n)])
         self._arrays = {k_: arr(k_) for k_ in L.LAYER_WEIGHTS}
@@ -195,6 +198,27 @@ def linear_accumulate(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor):
     assert y.shape == (T, N) and y.dtype == torch.float32
     L.check(L.load().lopa_linear_accumulate(x.data_ptr(), w.data_ptr(), y.data_ptr(), T, N, K,
                                             _stream_ptr()))
+    return y
+
+
+def quantize_e4m3(w: torch.Tensor):
+    """Per-row E4M3 codes [N,K] (uint8) and float32 scales [N] of a bf16 weight [N,K]."""
+    N, K = w.shape
+    codes = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    scales = torch.empty(N, dtype=torch.float32, device=w.device)
+    L.check(L.load().lopa_quantize_e4m3(w.data_ptr(), N, K, codes.data_ptr(), scales.data_ptr(),
+                                        _stream_ptr()))
+    return codes, scales
+
+
+def linear_accumulate_e4m3(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
+                           y: torch.Tensor):
+    """y += x @ (scales[:, None] * codes).T with E4M3 codes [N,K] (uint8) from quantize_e4m3."""
+    T, K = x.shape
+    N = codes.shape[0]
+    assert y.shape == (T, N) and y.dtype == torch.float32 and codes.dtype == torch.uint8
+    L.check(L.load().lopa_linear_accumulate_e4m3(x.data_ptr(), codes.data_ptr(), scales.data_ptr(),
+                                                 y.data_ptr(), T, N, K, _stream_ptr()))
     return y
 
 

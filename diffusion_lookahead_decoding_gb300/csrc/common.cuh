@@ -19,6 +19,7 @@ enum DeviceError : int {
   DEV_TIMEOUT_EPILOGUE = 3,
   DEV_BAD_INDEX = 4,
   DEV_TIMEOUT_CLUSTER = 5,
+  DEV_TIMEOUT_CONVERT = 6,  // E4M3 weight stream: a converter warp's wait gave up
 };
 
 // Upper bound of any spin-wait on the device (nanoseconds of %globaltimer).

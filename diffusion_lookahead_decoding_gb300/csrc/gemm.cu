@@ -27,6 +27,12 @@
 // activations, warp 1 allocates TMEM and issues the MMAs, warps 2..9 run the epilogue
 // (two warps per TMEM lane quarter, splitting the columns), staging output tiles in the
 // freed rings so global writes are whole-row 16-byte stores.  All waits are bounded.
+//
+// E4M3 weight stream (template flag F8): the weight TMA brings 8-bit codes (half the HBM
+// bytes) into a staging ring; eight converter warps widen each stage to bf16 in the
+// 128-byte-swizzled K-major layout the MMA reads (exactly: every E4M3 value is a bf16
+// value) and hand the slot to the MMA warp; the epilogue multiplies each weight row's
+// accumulator by that row's float32 scale.  The MMA itself stays bf16 x bf16 -> fp32.
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -43,6 +49,14 @@ namespace {
 
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = (3 + kEpiWarps) * 32;  // W producer, MMA, 8 epilogue warps, X producer
+// E4M3 stream: 8 converter warps (codes -> bf16) after the 11 warps above.  The q/k/v kernel
+// adds none: its register-heavy exchange epilogue would spill, so there the 8 epilogue warps
+// convert during the main loop instead (measured faster for q/k/v, slower for the others,
+// whose epilogue warps then also compete for issue slots with the MMA and producer warps).
+template <int MODE>
+__host__ __device__ constexpr int conv_threads() { return (MODE == GEMM_QKV ? 0 : 8) * 32; }
+template <int MODE, bool F8>
+__host__ __device__ constexpr int threads_of() { return kThreads + (F8 ? conv_threads<MODE>() : 0); }
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kMaxStages = 8;
 
@@ -52,6 +66,7 @@ __device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 3, 256;
 struct SmemTail {
   uint64_t wfull[kMaxStages], wempty[kMaxStages];
   uint64_t xfull[kMaxStages], xempty[kMaxStages];
+  uint64_t ffull[kMaxStages], fempty[kMaxStages];  // E4M3 stream: staging ring of codes
   uint64_t accf;
   uint64_t cfull;  // clustered mode: every split's partial tile is in the exchange workspace
   uint64_t drain;  // after a wait gave up: completion of every MMA this CTA issued
@@ -62,8 +77,30 @@ struct SmemTail {
   unsigned long long tl_tw;  // timeline builds: when the accumulator was complete
 };
 
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+// E4M3 -> bf16, two codes per 32-bit pair.  Each 16-bit lane gets the code's sign in bit
+// 15 and its 7 magnitude bits in bits 4..10: the exponent field e and fraction m land in
+// the low exponent bits and the top fraction bits of a bf16, which then reads
+// 2^(e-127) * 1.m (e >= 1) or 2^-126 * 0.m (e = 0).  The code's value is 2^(e-7) * 1.m or
+// 2^-6 * 0.m, so one exact multiplication by 2^120 finishes the conversion for normal and
+// subnormal codes alike.
+__device__ __forceinline__ uint32_t bf16x2_times_2p120(uint32_t bits) {
+  __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&bits);
+  const uint32_t k2p120 = 0x7B807B80u;  // bf16 2^120 in both lanes
+  h = __hmul2(h, *reinterpret_cast<const __nv_bfloat162*>(&k2p120));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+// Four codes (bytes of w, lowest byte = lowest column) -> two bf16 pairs.  The byte
+// permutations place the magnitudes in the low bytes of the lanes and the signs in the
+// high bytes; magnitude * 16 + sign assembles a lane (the fields do not overlap).
+__device__ __forceinline__ uint2 e4m3x4_to_bf16(uint32_t w) {
+  const uint32_t m = w & 0x7F7F7F7Fu, s = w & 0x80808080u;
+  const uint32_t lo = __byte_perm(m, 0u, 0x4140) * 16u + __byte_perm(s, 0u, 0x1404);
+  const uint32_t hi = __byte_perm(m, 0u, 0x4342) * 16u + __byte_perm(s, 0u, 0x3424);
+  return make_uint2(bf16x2_times_2p120(lo), bf16x2_times_2p120(hi));
+}
+
+template <int MODE, bool F8>
+__global__ void __launch_bounds__(threads_of<MODE, F8>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -73,10 +110,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~uintptr_t(1023));
   uint8_t* wring = smem;
   uint8_t* xring = smem + (size_t)a.w_stages * a.w_slot_bytes;
-  SmemTail* tail = reinterpret_cast<SmemTail*>(xring + (size_t)a.x_stages * a.x_slot_bytes);
+  uint8_t* fring = xring + (size_t)a.x_stages * a.x_slot_bytes;
+  SmemTail* tail = reinterpret_cast<SmemTail*>(fring + (F8 ? (size_t)a.f_stages * a.f_slot_bytes : 0));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int SW = a.w_stages, SX = a.x_stages;
+  const int SW = a.w_stages, SX = a.x_stages, SF = F8 ? a.f_stages : 1;
+  constexpr bool kEpiConverts = conv_threads<MODE>() == 0;  // E4M3: epilogue warps convert
+  constexpr int kConvAll = kEpiConverts ? kEpiWarps * 32 : conv_threads<MODE>();  // converting threads
   // The weight operand is A (128-row tiles) except for the LM head, where it is B.
   constexpr bool kWeightIsA = MODE != GEMM_LMSTATS;
 
@@ -117,8 +157,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SW; ++s) {
-      mbar_init(smem_u32(&tail->wfull[s]), 1);
+      mbar_init(smem_u32(&tail->wfull[s]), F8 ? kConvAll / 32 : 1);
       mbar_init(smem_u32(&tail->wempty[s]), 1);
+    }
+    for (int s = 0; F8 && s < SF; ++s) {
+      mbar_init(smem_u32(&tail->ffull[s]), 1);
+      mbar_init(smem_u32(&tail->fempty[s]), kConvAll / 32);
     }
     for (int s = 0; s < SX; ++s) {
       mbar_init(smem_u32(&tail->xfull[s]), 1);
@@ -146,19 +190,70 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = &tail->abort;
   pdl_trigger();
 
+  // E4M3 stream, converters (the extra converter warps, or in the q/k/v kernel the epilogue
+  // warps during the main loop): stage `it` of codes (rows of 64
+  // bytes, tile after tile) becomes the bf16 operand in converted slot it % SW, 128-byte
+  // swizzled: row r, 16-byte chunk c at r * 128 + ((c ^ (r & 7)) << 4).  Item e = (row,
+  // 16-code part): one 16-byte load and two 16-byte stores (chunks 2 * part and
+  // 2 * part + 1).  A thread loads all its items of a stage before converting; each warp
+  // then fences its stores for the async proxy and one lane signals the MMA warp and the
+  // producer (barrier counts = converting warps).  ct: 0 .. kConvAll - 1.
+  auto convert_stages = [&](int ct) {
+    constexpr int kItems = (256 * 4 + kConvAll - 1) / kConvAll;  // per thread, largest stage
+    const int rows = kWeightIsA ? ((a_ok[0] ? 128 : 0) + (a_ok[1] ? 128 : 0)) : a.nbox;
+    for (int it = 0; it < nk; ++it) {
+      const int s = it % SF, sw = it % SW;
+      if (!mbar_wait_bounded(smem_u32(&tail->ffull[s]), (uint32_t)(it / SF) & 1u, abort, a.err,
+                             DEV_TIMEOUT_CONVERT, lim))
+        break;
+      if (it >= SW && !mbar_wait_bounded(smem_u32(&tail->wempty[sw]), ((uint32_t)(it / SW) & 1u) ^ 1u,
+                                         abort, a.err, DEV_TIMEOUT_CONVERT, lim))
+        break;
+      const uint8_t* src = fring + (size_t)s * a.f_slot_bytes;
+      uint8_t* dst = wring + (size_t)sw * a.w_slot_bytes;
+      uint4 v[kItems];
+#pragma unroll
+      for (int j = 0; j < kItems; ++j) {
+        const int e = ct + j * kConvAll;
+        if (e < rows * 4) v[j] = *reinterpret_cast<const uint4*>(src + (e >> 2) * 64 + (e & 3) * 16);
+      }
+#pragma unroll
+      for (int j = 0; j < kItems; ++j) {
+        const int e = ct + j * kConvAll;
+        if (e >= rows * 4) continue;
+        const int row = e >> 2, part = e & 3;
+        const uint2 p0 = e4m3x4_to_bf16(v[j].x), p1 = e4m3x4_to_bf16(v[j].y);
+        const uint2 p2 = e4m3x4_to_bf16(v[j].z), p3 = e4m3x4_to_bf16(v[j].w);
+        uint8_t* rb = dst + row * 128;
+        const int sw7 = row & 7;
+        *reinterpret_cast<uint4*>(rb + (((2 * part) ^ sw7) << 4)) = make_uint4(p0.x, p0.y, p1.x, p1.y);
+        *reinterpret_cast<uint4*>(rb + (((2 * part + 1) ^ sw7) << 4)) = make_uint4(p2.x, p2.y, p3.x, p3.y);
+      }
+      fence_proxy_async_smem();  // the MMA reads the slot through the async proxy
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&tail->wfull[sw]));
+        mbar_arrive(smem_u32(&tail->fempty[s]));
+      }
+    }
+  };
+
   if (warp == 0 || warp == 2 + kEpiWarps) {
     // Producers: warp 0 streams the weight operand, the last warp the activation operand.
     const bool weights = warp == 0;
     if (lane == 0) {
       if (!weights) pdl_wait();  // activations are written by the previous kernel
-      const int S = weights ? SW : SX;
-      uint8_t* ring = weights ? wring : xring;
-      const uint32_t slot = weights ? a.w_slot_bytes : a.x_slot_bytes;
-      uint64_t* full = weights ? tail->wfull : tail->xfull;
-      uint64_t* empty = weights ? tail->wempty : tail->xempty;
+      // E4M3: the weight loads fill the staging ring with codes (one byte per element).
+      const bool codes = F8 && weights;
+      const int S = codes ? SF : weights ? SW : SX;
+      uint8_t* ring = codes ? fring : weights ? wring : xring;
+      const uint32_t slot = codes ? a.f_slot_bytes : weights ? a.w_slot_bytes : a.x_slot_bytes;
+      uint64_t* full = codes ? tail->ffull : weights ? tail->wfull : tail->xfull;
+      uint64_t* empty = codes ? tail->fempty : weights ? tail->wempty : tail->xempty;
       const bool is_a = weights == kWeightIsA;
       const uint64_t pol = weights ? policy_evict_first() : policy_evict_last();
-      const uint32_t bytes = is_a ? a_bytes : b_bytes;
+      const uint32_t bytes = (is_a ? a_bytes : b_bytes) >> (codes ? 1 : 0);
+      const uint32_t tile_bytes = a.a_tile_bytes >> (codes ? 1 : 0);
       int issued = 0;
       for (int it = 0; it < nk; ++it) {
         const int s = it % S;
@@ -177,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int y0 = packed ? ((a_row[0] >> 7) * a.k_blocks + kb) * 128 : a_row[0];
           const int y1 = packed ? ((a_row[1] >> 7) * a.k_blocks + kb) * 128 : a_row[1];
           if (a_ok[0]) tma_load_2d(dst, &mapA, fb, kx, y0, pol);
-          if (a_ok[1]) tma_load_2d(dst + a.a_tile_bytes, &mapA, fb, kx, y1, pol);
+          if (a_ok[1]) tma_load_2d(dst + tile_bytes, &mapA, fb, kx, y1, pol);
         } else {
           const int y = packed ? ((b_row / a.nbox) * a.k_blocks + kb) * a.nbox : b_row;
           tma_load_2d(dst, &mapB, fb, kx, y, pol);
@@ -223,10 +318,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) mma_commit(smem_u32(&tail->accf));
     }
+  } else if (F8 && warp >= 3 + kEpiWarps) {
+    convert_stages((int)threadIdx.x - kThreads);
   } else if (warp >= 2 && warp < 2 + kEpiWarps) {
     // Epilogue warps 2..9: warp w may only touch TMEM lanes 32*(w%4) .. +31, so each
     // lane quarter has two warps; they take alternate 16-column chunks.  The outputs may
-    // still be read by the previous kernel until it completes.
+    // still be read by the previous kernel until it completes.  In the E4M3 q/k/v kernel they
+    // first convert the weight stream.
+    if (F8 && kEpiConverts) convert_stages((int)threadIdx.x - 64);
     pdl_wait();
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
@@ -234,9 +333,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int te = threadIdx.x - 64;  // 0..255 over the epilogue warps
     const int nchunk = a.nbox / 16;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    // E4M3 stream: the scale of the weight row of this thread's TMEM lane in accumulator i
+    // (weights on M); 1 for bf16 weights.
+    auto row_scale = [&](int i) { return F8 ? __ldg(a.wscale + a_row[i] + r) : 1.0f; };
     // Copies accumulator i to `stage` as fp32 [token][128 columns], two of this warp's
     // 16-column chunks per TMEM wait.
     auto stage_acc = [&](int i, float* stage) {
+      const float sc = row_scale(i);
       for (int ci = half; ci < nchunk; ci += 4) {
         float v[16], w[16];
         if (ci + 2 < nchunk) {
@@ -244,13 +347,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                       lane_base + (uint32_t)(i * 256 + ci * 16 + 32), v, w);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            stage[(ci * 16 + j) * 128 + r] = v[j];
-            stage[(ci * 16 + 32 + j) * 128 + r] = w[j];
+            stage[(ci * 16 + j) * 128 + r] = F8 ? v[j] * sc : v[j];
+            stage[(ci * 16 + 32 + j) * 128 + r] = F8 ? w[j] * sc : w[j];
           }
         } else {
           tmem_ld16(lane_base + (uint32_t)(i * 256 + ci * 16), v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) stage[(ci * 16 + j) * 128 + r] = v[j];
+          for (int j = 0; j < 16; ++j) stage[(ci * 16 + j) * 128 + r] = F8 ? v[j] * sc : v[j];
         }
       }
     };
@@ -288,11 +391,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!a_ok[i]) continue;  // the same for every CTA of the cluster
         if (ok) {
           float* mine = region(i, rank);
+          const float sc = row_scale(i);
           for (int ci = half; ci < nchunk; ci += 2) {
             float v[16];
             tmem_ld16(lane_base + (uint32_t)(i * 256 + ci * 16), v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) __stcg(mine + (size_t)(ci * 16 + j) * 128 + r, v[j]);
+            for (int j = 0; j < 16; ++j)
+              __stcg(mine + (size_t)(ci * 16 + j) * 128 + r, F8 ? v[j] * sc : v[j]);
           }
           __threadfence();
         }
@@ -426,12 +531,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!a_ok[i]) continue;
           if (a.atomic) {  // standalone accumulate: fp32 atomics into out_f32
             const int n = a_row[i] + r;
+            const float sc = row_scale(i);
             for (int ci = half; ci < nchunk; ci += 2) {
               float v[16];
               tmem_ld16(lane_base + (uint32_t)(i * 256 + ci * 16), v);
               for (int j = 0; j < 16; ++j) {
                 const int t = b_row + ci * 16 + j;
-                if (t < a.T) atomicAdd(a.out_f32 + (size_t)t * a.ldo + n, v[j]);
+                if (t < a.T) atomicAdd(a.out_f32 + (size_t)t * a.ldo + n, F8 ? v[j] * sc : v[j]);
               }
             }
             continue;
@@ -449,12 +555,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           epilogue_sync();
         }
       } else if (MODE == GEMM_SWIGLU) {
+        const float sg = row_scale(0), su = row_scale(1);
         for (int ci = half; ci < nchunk; ci += 2) {
           float g[16], u[16];
           tmem_ld16x2(lane_base + (uint32_t)(ci * 16), lane_base + (uint32_t)(256 + ci * 16), g, u);
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
+          for (int j = 0; j < 16; ++j) {
+            if (F8) {
+              g[j] *= sg;
+              u[j] *= su;
+            }
             stage[(ci * 16 + j) * 128 + r] = __fdividef(g[j], 1.0f + __expf(-g[j])) * u[j];
+          }
         }
         epilogue_sync();
         bf16* base = a.out_bf16 + a_row[0];
@@ -491,9 +603,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld16(lane_base + (uint32_t)(i * 256 + ci * 16), v);
             float cm = -INFINITY;
             int cidx = 0;
+            float ws[16];  // E4M3 stream: scales of these 16 vocabulary rows (same for the warp)
+            if (F8) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int id = b_row + ci * 16 + j;
+                ws[j] = id < a.V ? __ldg(a.wscale + id) : 0.f;
+              }
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int id = b_row + ci * 16 + j;
+              if (F8) v[j] *= ws[j];
               v[j] = (id < a.V && id != a.mask_id) ? v[j] * a.scale : -INFINITY;
               if (v[j] > cm) { cm = v[j]; cidx = id; }  // strict: lowest id wins ties
             }
@@ -545,9 +666,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // wait (bounded) for every TMA copy it issued and every MMA it started.
     if (lane == 0 && (warp == 0 || warp == 2 + kEpiWarps)) {
       const bool weights = warp == 0;
-      const int S = weights ? SW : SX;
+      const int S = weights ? (F8 ? SF : SW) : SX;
       const int n = weights ? tail->w_issued : tail->x_issued;
-      uint64_t* full = weights ? tail->wfull : tail->xfull;
+      uint64_t* full = weights ? (F8 ? tail->ffull : tail->wfull) : tail->xfull;
       for (int s = 0; s < S && s < n; ++s) {
         const int last = s + ((n - 1 - s) / S) * S;  // the last load issued into slot s
         mbar_wait_drain(smem_u32(&full[s]), (uint32_t)(last / S) & 1u);
@@ -563,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // No CTA leaves while a peer may still signal its mbarriers: the epilogue warps closed
     // the start phase of the cluster barrier, the other warps close it here; then the whole
     // cluster meets once more.  Every wait before this point is bounded.
-    if (warp < 2 || warp == 2 + kEpiWarps) cluster_wait();
+    if (warp < 2 || warp >= 2 + kEpiWarps) cluster_wait();  // producers, MMA, converters
     cluster_arrive_release();
     cluster_wait();
   }
@@ -632,19 +753,55 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
   return true;
 }
 
-int gemm_max_smem() { return kMaxSmem; }
-
-template <int MODE>
-const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(gemm_kernel<MODE>);
+// 2-D tensor map over a row-major [rows][cols] byte matrix (E4M3 codes) with a box of
+// box_rows x 64 bytes, no swizzle (the converter warps read it row by row); reads outside
+// [rows][cols] return zeros.
+bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                  uint32_t box_rows, char* errbuf, size_t errlen) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) {
+    snprintf(errbuf, errlen, "cuTensorMapEncodeTiled unavailable");
+    return false;
+  }
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || cols % 16 != 0) {
+    snprintf(errbuf, errlen, "E4M3 tensor map base/stride not 16-byte aligned");
+    return false;
+  }
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(errbuf, errlen, "cuTensorMapEncodeTiled (u8) failed (%d) rows=%llu cols=%llu box=%u",
+             (int)r, (unsigned long long)rows, (unsigned long long)cols, box_rows);
+    return false;
+  }
+  return true;
 }
 
-// Indexed by mode.
-const void* const kKernels[] = {kernel_ptr<GEMM_RED_ADD>(), kernel_ptr<GEMM_SWIGLU>(),
-                                kernel_ptr<GEMM_LMSTATS>(), kernel_ptr<GEMM_QKV>()};
+int gemm_max_smem() { return kMaxSmem; }
+
+template <int MODE, bool F8>
+const void* kernel_ptr() {
+  return reinterpret_cast<const void*>(gemm_kernel<MODE, F8>);
+}
+
+// Indexed by [E4M3 stream][mode].
+const void* const kKernels[2][4] = {
+    {kernel_ptr<GEMM_RED_ADD, false>(), kernel_ptr<GEMM_SWIGLU, false>(),
+     kernel_ptr<GEMM_LMSTATS, false>(), kernel_ptr<GEMM_QKV, false>()},
+    {kernel_ptr<GEMM_RED_ADD, true>(), kernel_ptr<GEMM_SWIGLU, true>(),
+     kernel_ptr<GEMM_LMSTATS, true>(), kernel_ptr<GEMM_QKV, true>()}};
 
 cudaError_t gemm_set_smem_limits() {
-  for (const void* k : kKernels) {
+  for (const void* k : kKernels[0]) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (e != cudaSuccess) return e;
+  }
+  for (const void* k : kKernels[1]) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (e != cudaSuccess) return e;
   }
@@ -652,19 +809,21 @@ cudaError_t gemm_set_smem_limits() {
 }
 
 cudaError_t gemm_set_carveout() {
-  for (const void* k : kKernels) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-  }
+  for (const auto& row : kKernels)
+    for (const void* k : row) {
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           (int)cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return e;
+    }
   return cudaSuccess;
 }
 
-int gemm_cluster_capacity(int mode, int cs, size_t smem) {
+int gemm_cluster_capacity(int mode, int cs, size_t smem, bool w8) {
   if (mode < 0 || mode > GEMM_QKV || cs < 1 || cs > kMaxClusterSplits) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, (unsigned)cs, 1);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(w8 ? threads_of<GEMM_QKV, true>() : kThreads);
+  if (mode != GEMM_QKV) cfg.blockDim = dim3(w8 ? threads_of<GEMM_RED_ADD, true>() : kThreads);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -674,7 +833,7 @@ int gemm_cluster_capacity(int mode, int cs, size_t smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kKernels[mode], &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, kKernels[w8 ? 1 : 0][mode], &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -684,12 +843,16 @@ int gemm_cluster_capacity(int mode, int cs, size_t smem) {
 // act: [act_rows_alloc][K] bf16 activations (T valid rows); w: [n_rows_w][K] bf16.
 const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_alloc, int T,
                       const void* w, int n_rows_w, int K, int na, int splits, int tok_box,
-                      int num_sms, bool w_packed) {
+                      int num_sms, bool w_packed, const float* w_scale) {
   static thread_local char err[256];
+  const bool w8 = w_scale != nullptr;
   // Packed weights are viewed as [tiles * K/64 * tile_rows][64]: one box = one tile.
   auto weight_map = [&](CUtensorMap* map, int tile_rows) {
-    if (!w_packed) return make_tmap_bf16(map, w, n_rows_w, K, tile_rows, err, sizeof(err));
     const uint64_t tiles = (uint64_t)(n_rows_w + tile_rows - 1) / tile_rows;
+    if (w8)
+      return w_packed ? make_tmap_u8(map, w, tiles * (K / 64) * tile_rows, 64, tile_rows, err, sizeof(err))
+                      : make_tmap_u8(map, w, n_rows_w, K, tile_rows, err, sizeof(err));
+    if (!w_packed) return make_tmap_bf16(map, w, n_rows_w, K, tile_rows, err, sizeof(err));
     return make_tmap_bf16(map, w, tiles * (K / 64) * tile_rows, 64, tile_rows, err, sizeof(err));
   };
   memset(L, 0, sizeof(*L));
@@ -697,6 +860,8 @@ const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_all
   if (K % 64 != 0 || K <= 0) return "GEMM K must be a positive multiple of 64";
   if (T <= 0) return "GEMM needs at least one token row";
   a.mode = mode;
+  a.w8 = w8 ? 1 : 0;
+  a.wscale = w_scale;
   a.w_packed = w_packed ? 1 : 0;
   a.k_blocks = K / 64;
   a.T = T;
@@ -740,35 +905,51 @@ const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_all
   }
   (void)num_sms;
   // Activations come from L2 (short latency): 3 slots, more when they are small.  The
-  // weight ring takes the rest of shared memory.
+  // weight ring takes the rest of shared memory.  E4M3 stream: two converted bf16 slots
+  // and the rest as the staging ring of codes (the bytes in flight from HBM).
   const int budget = kMaxSmem - 1024 - (int)sizeof(SmemTail) - 64;
   a.x_stages = a.x_slot_bytes <= 8192 ? 6 : 3;
-  a.w_stages = (budget - a.x_stages * (int)a.x_slot_bytes) / (int)a.w_slot_bytes;
-  if (a.w_stages > kMaxStages) a.w_stages = kMaxStages;
-  if (a.w_stages < 2) return "GEMM tile does not fit in shared memory";
-  if ((size_t)a.w_stages * a.w_slot_bytes + (size_t)a.x_stages * a.x_slot_bytes <
-      stage_bytes(mode, a.nbox))
-    return "GEMM output tile does not fit in the staging area";
-  L->smem = 1024 + (size_t)a.w_stages * a.w_slot_bytes + (size_t)a.x_stages * a.x_slot_bytes +
-            sizeof(SmemTail) + 64;
+  if (w8) {
+    a.f_slot_bytes = a.w_slot_bytes / 2;  // one byte per element instead of two (1 KB multiple)
+    a.w_stages = 2;
+    a.f_stages = (budget - a.x_stages * (int)a.x_slot_bytes - a.w_stages * (int)a.w_slot_bytes) /
+                 (int)a.f_slot_bytes;
+    if (a.f_stages > kMaxStages) a.f_stages = kMaxStages;
+    if (a.f_stages < 2) return "GEMM tile does not fit in shared memory";
+  } else {
+    a.w_stages = (budget - a.x_stages * (int)a.x_slot_bytes) / (int)a.w_slot_bytes;
+    if (a.w_stages > kMaxStages) a.w_stages = kMaxStages;
+    if (a.w_stages < 2) return "GEMM tile does not fit in shared memory";
+  }
+  const size_t rings = (size_t)a.w_stages * a.w_slot_bytes + (size_t)a.x_stages * a.x_slot_bytes +
+                       (size_t)a.f_stages * a.f_slot_bytes;
+  if (rings < stage_bytes(mode, a.nbox)) return "GEMM output tile does not fit in the staging area";
+  L->smem = 1024 + rings + sizeof(SmemTail) + 64;
   return "";
 }
 
-cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s) {
-  const dim3 blk(kThreads);
+template <bool F8>
+cudaError_t launch_gemm_t(const GemmLaunch& L, cudaStream_t s) {
   switch (L.args.mode) {
     case GEMM_RED_ADD:
-      return launch_pdl(gemm_kernel<GEMM_RED_ADD>, L.grid, blk, L.smem, s, L.mapA, L.mapB, L.args);
+      return launch_pdl(gemm_kernel<GEMM_RED_ADD, F8>, L.grid, dim3(threads_of<GEMM_RED_ADD, F8>()),
+                        L.smem, s, L.mapA, L.mapB, L.args);
     case GEMM_SWIGLU:
-      return launch_pdl(gemm_kernel<GEMM_SWIGLU>, L.grid, blk, L.smem, s, L.mapA, L.mapB, L.args);
+      return launch_pdl(gemm_kernel<GEMM_SWIGLU, F8>, L.grid, dim3(threads_of<GEMM_SWIGLU, F8>()),
+                        L.smem, s, L.mapA, L.mapB, L.args);
     case GEMM_LMSTATS:
-      return launch_pdl(gemm_kernel<GEMM_LMSTATS>, L.grid, blk, L.smem, s, L.mapA, L.mapB, L.args);
+      return launch_pdl(gemm_kernel<GEMM_LMSTATS, F8>, L.grid, dim3(threads_of<GEMM_LMSTATS, F8>()),
+                        L.smem, s, L.mapA, L.mapB, L.args);
     case GEMM_QKV:
-      return launch_pdl_cluster(gemm_kernel<GEMM_QKV>, L.grid, blk, L.smem, s,
-                                dim3(1, L.args.splits, 1), L.mapA, L.mapB, L.args);
+      return launch_pdl_cluster(gemm_kernel<GEMM_QKV, F8>, L.grid, dim3(threads_of<GEMM_QKV, F8>()),
+                                L.smem, s, dim3(1, L.args.splits, 1), L.mapA, L.mapB, L.args);
     default:
       return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s) {
+  return L.args.w8 ? launch_gemm_t<true>(L, s) : launch_gemm_t<false>(L, s);
 }
 
 }  // namespace lopa

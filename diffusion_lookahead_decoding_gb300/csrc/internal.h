@@ -122,6 +122,10 @@ struct GemmArgs {
   float* xws;        // QKV: split-K exchange workspace (see qkv_exchange_floats)
   int* err;
   int w_packed;      // weight operand in tile-major layout (see launch_pack_tiles)
+  int w8;            // weights are E4M3 codes with one float32 scale per weight row
+  const float* wscale;  // E4M3: scale per weight row ([a_rows]; LM head: padded to 256 rows)
+  int f_stages;      // E4M3: depth of the staging ring of codes
+  uint32_t f_slot_bytes;
   int zt;            // token boxes (LM head: token groups); grid.x = tiles x zt with the box
                      // index fastest, so the CTAs sharing a weight tile run side by side
   unsigned long long wait_ns;  // limit of every device-side wait (0 = the 2 s default)
@@ -142,10 +146,12 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 
 // Fills `L` for one GEMM.  Returns an empty string on success, else a reason.  With
 // w_packed the weight is in the tile-major layout written by launch_pack_tiles (tiles of
-// 128 rows, 256 for the LM head); otherwise it is row-major [n_rows_w][K].
+// 128 rows, 256 for the LM head); otherwise it is row-major [n_rows_w][K].  With w_scale
+// the weight holds E4M3 codes (one byte per element, same layouts) and w_scale one float32
+// scale per weight row.
 const char* plan_gemm(GemmLaunch* L, int mode, const void* act, int act_rows_alloc, int T,
                       const void* w, int n_rows_w, int K, int na, int splits, int tok_box,
-                      int num_sms, bool w_packed = false);
+                      int num_sms, bool w_packed = false, const float* w_scale = nullptr);
 
 // Tile-major weight packing: up to three row-major [rows_i][K] matrices, stacked by rows,
 // -> [ceil(rows/tile_rows)][K/64][tile_rows][64] (rows = the sum of rows_i).
@@ -157,6 +163,14 @@ struct PackSources {
 size_t packed_elems(int rows, int K, int tile_rows);
 cudaError_t launch_pack_tiles(const PackSources& src, bf16* dst, int K, int tile_rows,
                               cudaStream_t s);
+// E4M3 weight stream: scale[r] = max|row r| / 448 (float32; 1 for a zero row) for rows
+// [0, rows_out) of the stacked sources (rows past their end are zero), and the codes
+// E4M3(w / scale) packed tile-major ([tiles][K/64][tile_rows][64] bytes) or row-major
+// ([rows_out][K] bytes).
+cudaError_t launch_row_scales(const PackSources& src, int K, float* scale, int rows_out,
+                              cudaStream_t s);
+cudaError_t launch_pack_e4m3(const PackSources& src, const float* scale, uint8_t* dst, int K,
+                             int tile_rows, bool row_major, int rows_out, cudaStream_t s);
 // Gives every kernel of the library the same (maximal) shared-memory carveout, so that
 // consecutive kernels never make an SM change its L1/shared split.
 cudaError_t set_uniform_carveout();
@@ -168,7 +182,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t s);
 cudaError_t gemm_set_smem_limits();
 // Clusters of `cs` GEMM CTAs (with `smem` bytes of dynamic shared memory each) that can
 // be resident at once; 0 if such clusters cannot be launched.
-int gemm_cluster_capacity(int mode, int cs, size_t smem);
+int gemm_cluster_capacity(int mode, int cs, size_t smem, bool w8 = false);
 int gemm_max_smem();
 
 // ------------------------------------------------------------------ attention

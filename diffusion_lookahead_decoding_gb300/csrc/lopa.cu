@@ -71,10 +71,15 @@ struct lopa_ctx {
   int num_sms = 0;
   int ccap[kMaxClusterSplits + 1] = {};  // resident clusters of 1, 2, 4 q/k/v-GEMM CTAs
   // borrowed weights
-  const bf16 *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
+  const bf16 *embed = nullptr, *final_norm = nullptr;
   std::vector<const bf16*> attn_norm, mlp_norm;
-  // owned tile-major copies: q/k/v stacked, output, gate/up stacked, down (per layer)
-  std::vector<const bf16*> wqkv, wo, wgu, wd;
+  // owned tile-major copies: q/k/v stacked, output, gate/up stacked, down (per layer), and
+  // the LM head: bf16, or E4M3 codes with one float32 scale per row (w8)
+  bool w8 = false;
+  std::vector<const void*> wqkv, wo, wgu, wd;
+  const void* lm_head = nullptr;
+  std::vector<const float*> sqkv, so, sgu, sd;
+  const float* slm = nullptr;
   // owned device memory
   std::vector<void*> allocs;
   bf16 *kc = nullptr, *vc = nullptr, *ks = nullptr, *vs = nullptr;
@@ -243,8 +248,8 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
   p.o.resize(L);
   p.gu.resize(L);
   p.dn.resize(L);
-  auto plan = [&](GemmLaunch& G, int mode, const void* act, int K, const void* w, int nrows,
-                  const char* what) -> int {
+  auto plan = [&](GemmLaunch& G, int mode, const void* act, int K, const void* w,
+                  const float* wscale, int nrows, const char* what) -> int {
     int na = 2, splits = 1;
     if (mode == GEMM_QKV) {
       qkv_tiling(ctx, nrows, K, p.T, &na, &splits);
@@ -254,7 +259,7 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
     }
     const char* e = plan_gemm(&G, mode, act, ctx->Tmax, p.T, w, nrows, K, na, splits,
                               mode == GEMM_QKV ? qkv_box(p.T) : p.tok_box,
-                              ctx->num_sms, /*w_packed=*/true);
+                              ctx->num_sms, /*w_packed=*/true, wscale);
     if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s GEMM: %s", what, e);
     if (mode == GEMM_RED_ADD) {
       if ((size_t)G.args.splits * p.T * nrows > ctx->part_floats)
@@ -269,7 +274,9 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
   };
   for (int l = 0; l < L; ++l) {
     int r;
-    if ((r = plan(p.qkv[l], GEMM_QKV, ctx->n, d, ctx->wqkv[l], ctx->qkv_rows, "qkv"))) return r;
+    auto sc = [&](const std::vector<const float*>& v) { return ctx->w8 ? v[l] : nullptr; };
+    if ((r = plan(p.qkv[l], GEMM_QKV, ctx->n, d, ctx->wqkv[l], sc(ctx->sqkv), ctx->qkv_rows, "qkv")))
+      return r;
     GemmArgs& qa = p.qkv[l].args;
     qa.q = ctx->q;
     bf16* kcl = ctx->kc + (size_t)l * ctx->cache_layer;
@@ -312,16 +319,17 @@ int build_plan(lopa_ctx* ctx, Plan& p, int nb, int Bq, int kv_to_cache, bool lm,
     aa.err = &ctx->st->err;
     const char* ea = plan_attention(&p.attn[l], aa, dh, m.max_seq, ctx->vt_ld);
     if (ea[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s", ea);
-    if ((r = plan(p.o[l], GEMM_RED_ADD, ctx->attn, H * dh, ctx->wo[l], d, "o"))) return r;
-    if ((r = plan(p.gu[l], GEMM_SWIGLU, ctx->n, d, ctx->wgu[l], 2 * F, "gate/up"))) return r;
+    if ((r = plan(p.o[l], GEMM_RED_ADD, ctx->attn, H * dh, ctx->wo[l], sc(ctx->so), d, "o"))) return r;
+    if ((r = plan(p.gu[l], GEMM_SWIGLU, ctx->n, d, ctx->wgu[l], sc(ctx->sgu), 2 * F, "gate/up")))
+      return r;
     p.gu[l].args.out_bf16 = ctx->hm;
     p.gu[l].args.ldh = F;
-    if ((r = plan(p.dn[l], GEMM_RED_ADD, ctx->hm, F, ctx->wd[l], d, "down"))) return r;
+    if ((r = plan(p.dn[l], GEMM_RED_ADD, ctx->hm, F, ctx->wd[l], sc(ctx->sd), d, "down"))) return r;
   }
   if (lm) {
     const int na = p.T > 128 ? 2 : 1;
     const char* e = plan_gemm(&p.lmh, GEMM_LMSTATS, ctx->n, ctx->Tmax, p.T, ctx->lm_head, m.vocab,
-                              d, na, 1, 0, ctx->num_sms, /*w_packed=*/true);
+                              d, na, 1, 0, ctx->num_sms, /*w_packed=*/true, ctx->w8 ? ctx->slm : nullptr);
     if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "lm-head GEMM: %s", e);
     GemmArgs& a = p.lmh.args;
     a.V = m.vocab;
@@ -448,6 +456,8 @@ int validate(const lopa_model_config* c, const lopa_decode_config* d) {
   if (d->max_prompt < 1 || d->max_prompt + d->block > c->max_seq)
     return fail(ctx, LOPA_ERR_INVALID_ARG, "need 1 <= max_prompt and max_prompt + block <= max_seq");
   if (!std::isfinite(d->tau)) return fail(ctx, LOPA_ERR_INVALID_ARG, "tau must be finite");
+  if (c->weight_format != LOPA_WEIGHTS_BF16 && c->weight_format != LOPA_WEIGHTS_E4M3)
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "unknown weight_format %d", c->weight_format);
   return 0;
 }
 
@@ -464,8 +474,9 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
   if (major != 10) return fail(ctx, LOPA_ERR_UNSUPPORTED, "needs an sm_10x GPU (found sm_%d%d)", major, minor);
   CK(gemm_set_smem_limits());
   CK(attention_set_smem_limits());
+  ctx->w8 = m.weight_format == LOPA_WEIGHTS_E4M3;
   for (int c = 1; c <= kMaxClusterSplits; c *= 2)
-    ctx->ccap[c] = gemm_cluster_capacity(GEMM_QKV, c, (size_t)gemm_max_smem());
+    ctx->ccap[c] = gemm_cluster_capacity(GEMM_QKV, c, (size_t)gemm_max_smem(), ctx->w8);
   if (ctx->ccap[1] < 1) return fail(ctx, LOPA_ERR_UNSUPPORTED, "projection GEMM cannot be resident");
   if (!ctx->stream) {
     CK(cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking));
@@ -543,12 +554,27 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
   // Owned tile-major copies of the projection weights and the LM head: every 16 KB
   // (32 KB for the LM head) tile the GEMMs stream becomes one contiguous HBM run; q, k and
   // v (and gate and up) are stacked into the one matrix their GEMM streams.
-  auto pack = [&](std::vector<const bf16*>& dst, PackSources src, int K, int tile_rows) -> int {
+  // E4M3 weight stream: per-row scales, then the codes in the same tile-major layout
+  // (rows past the end of the last tile have code 0 and scale 1).
+  auto pack = [&](std::vector<const void*>& dst, std::vector<const float*>& dscale, PackSources src,
+                  int K, int tile_rows) -> int {
     int rows = 0;
     for (int i = 0; i < PackSources::kMax; ++i) rows += src.rows[i];
+    const size_t elems = packed_elems(rows, K, tile_rows);
+    int rr;
+    if (ctx->w8) {
+      const int rows_pad = (int)(elems / K);
+      uint8_t* p = nullptr;
+      float* sp = nullptr;
+      if ((rr = dalloc(ctx, &p, elems)) || (rr = dalloc(ctx, &sp, (size_t)rows_pad))) return rr;
+      CK(launch_row_scales(src, K, sp, rows_pad, s));
+      CK(launch_pack_e4m3(src, sp, p, K, tile_rows, false, rows_pad, s));
+      dst.push_back(p);
+      dscale.push_back(sp);
+      return 0;
+    }
     bf16* p = nullptr;
-    int rr = dalloc(ctx, &p, packed_elems(rows, K, tile_rows));
-    if (rr) return rr;
+    if ((rr = dalloc(ctx, &p, elems))) return rr;
     CK(launch_pack_tiles(src, p, K, tile_rows, s));
     dst.push_back(p);
     return 0;
@@ -561,16 +587,18 @@ int init_impl(lopa_ctx* ctx, const lopa_weights* w) {
     return ps;
   };
   for (int l = 0; l < L; ++l) {
-    if ((r = pack(ctx->wqkv, src(w->wq[l], H * dh, w->wk[l], Hk * dh, w->wv[l], Hk * dh), d, 128)) ||
-        (r = pack(ctx->wo, src(w->wo[l], d), H * dh, 128)) ||
-        (r = pack(ctx->wgu, src(w->wg[l], F, w->wu[l], F), d, 128)) ||
-        (r = pack(ctx->wd, src(w->wd[l], d), F, 128)))
+    if ((r = pack(ctx->wqkv, ctx->sqkv, src(w->wq[l], H * dh, w->wk[l], Hk * dh, w->wv[l], Hk * dh), d, 128)) ||
+        (r = pack(ctx->wo, ctx->so, src(w->wo[l], d), H * dh, 128)) ||
+        (r = pack(ctx->wgu, ctx->sgu, src(w->wg[l], F, w->wu[l], F), d, 128)) ||
+        (r = pack(ctx->wd, ctx->sd, src(w->wd[l], d), F, 128)))
       return r;
   }
   {
-    std::vector<const bf16*> lm;
-    if ((r = pack(lm, src(w->lm_head, V), d, 256))) return r;
+    std::vector<const void*> lm;
+    std::vector<const float*> slm;
+    if ((r = pack(lm, slm, src(w->lm_head, V), d, 256))) return r;
     ctx->lm_head = lm[0];
+    ctx->slm = ctx->w8 ? slm[0] : nullptr;
   }
   CK(cudaEventCreate(&ctx->ev0));
   CK(cudaEventCreate(&ctx->ev1));
@@ -673,7 +701,7 @@ int step_impl(lopa_ctx* ctx, lopa_step_result* out, bool allow_merge) {
 
 extern "C" {
 
-int lopa_version(void) { return 100; }
+int lopa_version(void) { return 200; }
 
 #ifdef LOPA_TIMELINE
 // Timeline builds only: every instrumented kernel launched from now on appends its per-CTA
@@ -1014,6 +1042,46 @@ int lopa_linear_accumulate(const void* x, const void* w, float* y, int T, int N,
   GemmLaunch G;
   const char* e = plan_gemm(&G, GEMM_RED_ADD, x, T, T, w, N, K, na, pick_splits(tiles, K / 64, sms),
                             tok_box, sms);
+  if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s", e);
+  G.args.out_f32 = y;
+  G.args.ldo = N;
+  G.args.atomic = 1;
+  cudaError_t se = cudaSuccess;
+  G.args.err = call_status_word(&se);
+  CK(se);
+  G.args.wait_ns = call_wait_limit_ns();
+  CK(launch_gemm(G, static_cast<cudaStream_t>(stream)));
+  return 0;
+}
+
+int lopa_quantize_e4m3(const void* w, int rows, int K, uint8_t* codes, float* scales, void* stream) {
+  lopa_ctx* ctx = nullptr;
+  if (!aligned16(w) || !aligned16(codes) || !scales) return fail(ctx, LOPA_ERR_INVALID_ARG, "null or unaligned pointer");
+  if (rows < 1 || K < 64 || K % 64) return fail(ctx, LOPA_ERR_INVALID_ARG, "need rows >= 1 and K % 64 == 0");
+  PackSources src = {{static_cast<const bf16*>(w), nullptr, nullptr}, {rows, 0, 0}};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CK(launch_row_scales(src, K, scales, rows, s));
+  CK(launch_pack_e4m3(src, scales, codes, K, 128, true, rows, s));
+  return 0;
+}
+
+int lopa_linear_accumulate_e4m3(const void* x, const uint8_t* codes, const float* scales, float* y,
+                                int T, int N, int K, void* stream) {
+  lopa_ctx* ctx = nullptr;
+  if (!aligned16(x) || !aligned16(codes) || !scales || !y)
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "null or unaligned pointer");
+  if (T < 1 || N < 128 || N % 128 || K < 64 || K % 64)
+    return fail(ctx, LOPA_ERR_UNSUPPORTED, "need T >= 1, N % 128 == 0, K % 64 == 0");
+  CK(gemm_set_smem_limits());
+  int dev = 0, sms = 0;
+  CK(cudaGetDevice(&dev));
+  CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int tok_box = std::min(256, round16(T));
+  const int na = N >= 256 ? 2 : 1;
+  const int tiles = ((N + na * 128 - 1) / (na * 128)) * ((T + tok_box - 1) / tok_box);
+  GemmLaunch G;
+  const char* e = plan_gemm(&G, GEMM_RED_ADD, x, T, T, codes, N, K, na, pick_splits(tiles, K / 64, sms),
+                            tok_box, sms, false, scales);
   if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s", e);
   G.args.out_f32 = y;
   G.args.ldo = N;

@@ -66,7 +66,22 @@ typedef struct {
   float rope_base;   /* RoPE theta base */
   float rms_eps;     /* RMSNorm epsilon */
   float logit_scale; /* logits = logit_scale * (final_hidden . lm_head_row) */
+  int weight_format; /* LOPA_WEIGHTS_BF16 (0) or LOPA_WEIGHTS_E4M3 (1), see below */
 } lopa_model_config;
+
+/* Format of the weights the GEMMs stream (lopa_model_config.weight_format).  The caller
+ * always passes bf16 matrices; with LOPA_WEIGHTS_E4M3, lopa_init_model quantises every
+ * projection matrix and the LM head on the GPU, per output row r: scale s_r = max|W_r| /
+ * 448 and codes E4M3(W_r / s_r) (the 8-bit float with 4 exponent bits, bias 7, and 3
+ * fraction bits; round to nearest even, saturating at +-448; both quotients in float32;
+ * an all-zero row gets s_r = 1), and the forward uses codes * s_r as the weight: half the
+ * weight bytes per forward.  Activations, the embedding table and the norm gains stay
+ * bf16, the arithmetic bf16 x bf16 -> fp32.  ("Decoding-efficiency revolution" blog,
+ * section 4.1 and the LoPA announcement's "LoPA-Dist" section name quantisation as part of
+ * the system without fixing a format; this per-channel E4M3 weight stream is this
+ * library's reading.) */
+#define LOPA_WEIGHTS_BF16 0
+#define LOPA_WEIGHTS_E4M3 1
 
 /* Device pointers (bf16), every matrix in the nn.Linear layout [out_features][in_features],
  * row-major, 16-byte aligned.  Per-layer entries are HOST arrays of n_layers device
@@ -222,6 +237,19 @@ int lopa_set_wait_limit_ns(unsigned long long ns);
  * update is applied with atomic adds, so y must not be written concurrently by others. */
 int lopa_linear_accumulate(const void* x, const void* w, float* y, int T, int N, int K,
                            void* stream);
+
+/* Per-row E4M3 quantisation as lopa_init_model does it for LOPA_WEIGHTS_E4M3:
+ * w [rows][K] bf16 (device, 16-byte aligned), K a multiple of 64 -> codes [rows][K] bytes
+ * (device, 16-byte aligned), scales [rows] float32 (device).  The weight row r is then
+ * codes[r] * scales[r]. */
+int lopa_quantize_e4m3(const void* w, int rows, int K, uint8_t* codes, float* scales, void* stream);
+
+/* lopa_linear_accumulate with an E4M3 weight: y[T][N] += x[T][K] . (diag(scales) codes)^T,
+ * codes [N][K] bytes and scales [N] as lopa_quantize_e4m3 writes them (device, 16-byte
+ * aligned codes); the codes are widened to bf16 on chip and the scale is applied to the
+ * fp32 sum.  Same limits as lopa_linear_accumulate. */
+int lopa_linear_accumulate_e4m3(const void* x, const uint8_t* codes, const float* scales, float* y,
+                                int T, int N, int K, void* stream);
 
 /* Bytes of device workspace lopa_lmhead_argmax needs for `rows` rows. */
 size_t lopa_lmhead_workspace_bytes(int rows, int vocab);

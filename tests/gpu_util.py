@@ -38,14 +38,16 @@ def device_weights(name: str, seed: int = 0):
     return api.upload_weights(shape, w)
 
 
-def make_decoder(name: str, k: int | None = None, max_seq: int | None = None):
+def make_decoder(name: str, k: int | None = None, max_seq: int | None = None,
+                 weight_format: str = "bf16"):
     from diffusion_lookahead_decoding_gb300 import api
     build_lib()
     shape, dshape, _ = workload_weights(name)
     dw = device_weights(name)
     k = dshape.k if k is None else k
     max_seq = max_seq or dshape.prompt_len + dshape.gen_len
-    return api.LopaDecoder(shape, dw, dshape.block, k, dshape.tau, dshape.prompt_len, max_seq)
+    return api.LopaDecoder(shape, dw, dshape.block, k, dshape.tau, dshape.prompt_len, max_seq,
+                           weight_format=weight_format)
 
 
 def rel_l2(a, b):
@@ -74,15 +76,18 @@ class Conditioning:
         return f"oracle float32-vs-float64 movement: maxp {self.mp:.2e}, hidden {self.hidden:.2e}"
 
 
-def oracle_forward_pair(shape, w, prompt, branches, capacity, cache_weights=None):
+def oracle_forward_pair(shape, w, prompt, branches, capacity, cache_weights=None,
+                        weight_format="bf16"):
     """Oracle forward of `branches` after prefilling `prompt`, with float64 and with
     float32 accumulation.  Returns (model, cache, out, conditioning) of the float64 run
     (its logits included)."""
     P = len(prompt)
-    m = O.OracleModel(shape, w, act="bf16", cache_weights=cache_weights)
+    m = O.OracleModel(shape, w, act="bf16", cache_weights=cache_weights,
+                      weight_format=weight_format)
     cache = O.prefill(m, prompt, capacity)
     out = O.forward(m, cache, P, branches, want_logits=True)
-    m32 = O.OracleModel(shape, w, act="bf16", cache_weights=cache_weights, accum="fp32")
+    m32 = O.OracleModel(shape, w, act="bf16", cache_weights=cache_weights, accum="fp32",
+                        weight_format=weight_format)
     c32 = O.prefill(m32, prompt, capacity)
     alt = O.forward(m32, c32, P, branches)
     return m, cache, out, Conditioning(out, alt)
@@ -94,7 +99,8 @@ def softmax_rows(z):
     return e / e.sum(axis=-1, keepdims=True)
 
 
-def token_flips(gpu_am, gpu_mp, out, mask_id=0, gpu_hidden=None, shape=None, weights=None):
+def token_flips(gpu_am, gpu_mp, out, mask_id=0, gpu_hidden=None, shape=None, weights=None,
+                weight_format="bf16"):
     """Greedy-token differences between the GPU and the oracle: (all, beyond the window).
 
     At a position where the GPU picks token a and the oracle token b, the oracle's
@@ -106,7 +112,8 @@ def token_flips(gpu_am, gpu_mp, out, mask_id=0, gpu_hidden=None, shape=None, wei
     max(1e-3, e_a + e_b) - by the triangle inequality that holds whenever the GPU's own
     logits rank a over b, so a position beyond it means the fused LM head's argmax
     disagrees with its own input.  Without the hidden state the error on b is taken equal
-    to the one measured on a (window 2 e_a): a report, not a bound."""
+    to the one measured on a (window 2 e_a): a report, not a bound.  With E4M3 weights the
+    two LM-head rows are their quantised values (the quantisation is per row)."""
     am = np.asarray(gpu_am).reshape(-1)
     mp = np.asarray(gpu_mp, np.float64).reshape(-1)
     oam = np.asarray(out.am).reshape(-1)
@@ -128,6 +135,9 @@ def token_flips(gpu_am, gpu_mp, out, mask_id=0, gpu_hidden=None, shape=None, wei
             n = x / np.sqrt(np.mean(x * x) + shape.rms_eps) * g
             n = torch.from_numpy(n).to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
             W = weights["lm_head"][[a, b]].to(torch.float64).numpy()
+            if weight_format == "e4m3":
+                codes, s = O.quantize_e4m3_rows(W)
+                W = codes * s[:, None]
             zg = shape.logit_scale * (W @ n)
             p_b_gpu = mp[i] * np.exp(zg[1] - zg[0])
             window = e_a + abs(p_b_gpu - p[b])

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_struct_layouts_match_header_sizes(lib):
     # lopa_step_result: 7 ints + 16 floats + 2*64 ints
     assert C.sizeof(L.StepResult) == 4 * (7 + 16 + 128)
-    assert C.sizeof(L.ModelConfig) == 4 * 12
+    assert C.sizeof(L.ModelConfig) == 4 * 13
     assert C.sizeof(L.DecodeConfig) == 16
 
 
@@ -66,6 +66,9 @@ def test_host_side_argument_errors_without_gpu(lib):
     dc.k, dc.max_prompt = 3, 200  # prompt + block beyond max_seq
     assert lib.lopa_init_model(C.byref(mc), C.byref(w), C.byref(dc), None, C.byref(out)) == L.ERR_INVALID_ARG
     assert lib.lopa_linear_accumulate(None, None, None, 1, 128, 64, None) == L.ERR_INVALID_ARG
+    assert lib.lopa_linear_accumulate_e4m3(None, None, None, None, 1, 128, 64, None) == L.ERR_INVALID_ARG
+    assert lib.lopa_quantize_e4m3(None, 1, 64, None, None, None) == L.ERR_INVALID_ARG
+    assert lib.lopa_quantize_e4m3(4096, 1, 60, 4096, 4096, None) == L.ERR_INVALID_ARG  # K % 64
     assert lib.lopa_prefill(None, None, 0) == L.ERR_INVALID_ARG
     assert lib.lopa_step(None, None) == L.ERR_INVALID_ARG
     assert lib.lopa_lmhead_workspace_bytes(256, 152064) == 594 * 256 * 12 + 256
@@ -91,6 +94,7 @@ def _cfgs():
     ("k", -1, "INVALID_ARG"),
     ("max_prompt", 0, "INVALID_ARG"),
     ("tau", float("nan"), "INVALID_ARG"),
+    ("weight_format", 2, "INVALID_ARG"),   # neither bf16 (0) nor E4M3 (1)
 ])
 def test_config_validation_without_gpu(lib, field, value, code):
     """Every configuration the kernels do not implement is refused on the host, before
