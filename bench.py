@@ -368,6 +368,41 @@ def e4m3_summary(api, shape, dshape, dev_w, prompt, peak_bw, peak_tc, steps):
             "lm_head": {"ms": lm, "GB/s": lb / lm / 1e6, "TFLOP/s": gemm_flops(shape, T, 4) / lm / 1e9}}
 
 
+def kernel_table(args):
+    """Per-kernel CUDA-event times of the five projection GEMMs (layers cycled) and the
+    verification-forward latency for bf16 and E4M3 weights at k in {0, 3, 7} (32, 128 and
+    256 token rows) on the 7B shape, with each GEMM's fraction of the measured HBM peak on its
+    own algorithmic bytes."""
+    import torch
+    from diffusion_lookahead_decoding_gb300 import api, build, synth
+    build.build()
+    shape, dshape = synth.WORKLOADS["dream7b"]
+    w = synth.make_weights(shape, 0)
+    dw = api.upload_weights(shape, w)
+    del w
+    bw, _, _, src = _peaks()
+    prompt = synth.make_prompt(shape, dshape.prompt_len, seed=1)
+    B, P0, gen = dshape.block, dshape.prompt_len, dshape.gen_len
+    rows = []
+    for fmt in ("bf16", "e4m3"):
+        for k in (0, 3, 7):
+            dec = api.LopaDecoder(shape, dw, B, k, dshape.tau, P0, P0 + gen, weight_format=fmt)
+            dec.prefill(prompt)
+            T, wb = (k + 1) * B, 1 if fmt == "e4m3" else 2
+            row = {"weights": fmt, "k": k, "rows": T}
+            for kind, name in enumerate(["qkv", "o_proj", "gate_up_swiglu", "down", "lm_head"]):
+                ms = dec.time_gemm(kind, 2 * shape.n_layers if kind < 4 else 8)
+                row[name] = {"us": ms * 1e3, "frac_hbm": gemm_bytes(shape, T, kind, wb) / ms / 1e6 / bw}
+            dec.decode(gen)
+            dec.rewind(P0 + (gen // 2 // B) * B)
+            row["verify_ms"] = dec.time_forward(1, 30)[0]
+            row["block_start_ms"] = dec.time_forward(0, 30)[0]
+            dec.close()
+            rows.append(row)
+            print(json.dumps(row), flush=True)
+    print(json.dumps({"kernel_table": rows, "peaks": {"hbm_gbs": bw, "source": src}}), flush=True)
+
+
 def _peaks():
     try:
         p = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -509,6 +544,8 @@ def main():
     ap.add_argument("--max-blocks", type=int, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--sweep-branches", action="store_true",
                     help="branch-scaling table on the 2048-token-prompt workload, k in 0,1,3,7,15")
+    ap.add_argument("--kernel-table", action="store_true",
+                    help="per-GEMM times and verification latency, bf16 vs E4M3 weights, k in 0,3,7")
     ap.add_argument("--microbench", action="store_true",
                     help="attention + LM-head grid: branches x block x prefix")
     ap.add_argument("--weight-format", default="bf16", choices=["bf16", "e4m3"],
@@ -527,6 +564,8 @@ def main():
         return sweep_branches(args)
     if args.microbench:
         return microbench(args)
+    if args.kernel_table:
+        return kernel_table(args)
     profiling = args.profile_decode or args.profile_gemm is not None or args.profile_attention is not None
     if args.warmup < 3 and args.impl == "ours" and not profiling:
         args.warmup = 3
