@@ -111,6 +111,7 @@ struct lopa_ctx {
   std::vector<Plan> step_plans;
   Plan& step_plan() { return step_plans.back(); }
   Plan merged_plan, start_plan;
+  Plan prefill_plan;  // the prompt forward of the last prompt length (rebuilt when it changes)
   std::vector<cudaGraphExec_t> step_execs;
   cudaGraphExec_t merged_exec = nullptr, start_exec = nullptr;
   int cur_nb = 0;  // branch count of the graph being captured
@@ -754,10 +755,15 @@ int lopa_prefill(lopa_ctx* ctx, const int32_t* prompt, int n) {
   cudaStream_t s = ctx->stream;
   CK(cudaMemcpyAsync(ctx->tok_rows, prompt, sizeof(int) * n, cudaMemcpyHostToDevice, s));
   CK(launch_state_reset(ctx->st, 0, ctx->dc.block, ctx->mc.mask_id, s));
-  Plan p;
-  int r = build_plan(ctx, p, 1, n, 1, false, ctx->tok_rows, nullptr, nullptr);
-  if (r) return r;
-  if ((r = enqueue_forward(ctx, p))) return r;
+  int r;
+  if (ctx->prefill_plan.T != n) {
+    ctx->prefill_plan = Plan();
+    if ((r = build_plan(ctx, ctx->prefill_plan, 1, n, 1, false, ctx->tok_rows, nullptr, nullptr))) {
+      ctx->prefill_plan = Plan();
+      return r;
+    }
+  }
+  if ((r = enqueue_forward(ctx, ctx->prefill_plan))) return r;
   CK(launch_state_reset(ctx->st, n, ctx->dc.block, ctx->mc.mask_id, s));
   if ((r = check_device_error(ctx))) return r;
   ctx->prefilled = true;

@@ -9,6 +9,7 @@ the distribution of start / ready / end times.  Kernels overlap under programmat
 dependent launch; a profiler that serialises them cannot show this.
 
     python -m diffusion_lookahead_decoding_gb300.timeline [--workload dream7b] [--prefix 640]
+    python -m diffusion_lookahead_decoding_gb300.timeline --prefill   # the prompt forward
 """
 from __future__ import annotations
 
@@ -50,6 +51,45 @@ def build_timeline_lib() -> str:
     return LIB
 
 
+def _records(buf):
+    n = int(buf[0].item())
+    raw = buf[4:4 + n * 10].cpu().numpy().view(np.uint32).reshape(n, 10)
+    t = raw[:, 4:].view(np.uint64).reshape(n, 3).astype(np.int64)
+    ready = np.where((t[:, 1] >= t[:, 0]) & (t[:, 1] <= t[:, 2]), t[:, 1], 0)
+    return np.stack([raw[:, 0].astype(np.int64), t[:, 0], ready, t[:, 2],
+                     raw[:, 1].astype(np.int64), raw[:, 2].astype(np.int64)], axis=1)
+
+
+def record_prefill(workload: str):
+    """Runs the prompt forward (lopa_prefill; one warm-up call) with recording on; returns
+    the records, the shape and the CUDA-event time of the recorded call in ms."""
+    import torch
+    from . import _lib as L, api, synth
+    lib = L.load(build_timeline_lib())
+    lib.lopa_timeline_set_buffer.argtypes = [C.c_void_p]
+    lib.lopa_timeline_set_buffer.restype = C.c_int
+    shape, dshape = synth.WORKLOADS[workload]
+    dw = api.upload_weights(shape, synth.make_weights(shape, 0))
+    P0, Bk = dshape.prompt_len, dshape.block
+    dec = api.LopaDecoder(shape, dw, Bk, dshape.k, dshape.tau, P0, P0 + dshape.gen_len)
+    prompt = synth.make_prompt(shape, P0, seed=1)
+    dec.prefill(prompt)
+    buf = torch.zeros(4 + 400000 * 10, dtype=torch.int32, device="cuda")
+    buf[1] = 400000
+    torch.cuda.synchronize()
+    if lib.lopa_timeline_set_buffer(C.c_void_p(buf.data_ptr())) != 0:
+        raise RuntimeError("timeline buffer")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(dec.stream)
+    dec.prefill(prompt)
+    e1.record(dec.stream)
+    torch.cuda.synchronize()
+    lib.lopa_timeline_set_buffer(None)
+    recs = _records(buf)
+    dec.close()
+    return recs, shape, e0.elapsed_time(e1)
+
+
 def record(workload: str, prefix: int, forwards: int = 2):
     """Runs the verification-forward graph (one warm-up + `forwards` launches) with
     recording on; returns records (tag, t0, t_ready, t1, cta, sm) as an int64 array."""
@@ -75,12 +115,7 @@ def record(workload: str, prefix: int, forwards: int = 2):
     dec.time_forward(1, forwards)
     torch.cuda.synchronize()
     lib.lopa_timeline_set_buffer(None)
-    n = int(buf[0].item())
-    raw = buf[4:4 + n * 10].cpu().numpy().view(np.uint32).reshape(n, 10)
-    t = raw[:, 4:].view(np.uint64).reshape(n, 3).astype(np.int64)
-    ready = np.where((t[:, 1] >= t[:, 0]) & (t[:, 1] <= t[:, 2]), t[:, 1], 0)
-    recs = np.stack([raw[:, 0].astype(np.int64), t[:, 0], ready, t[:, 2],
-                     raw[:, 1].astype(np.int64), raw[:, 2].astype(np.int64)], axis=1)
+    recs = _records(buf)
     dec.close()
     return recs, shape, med
 
@@ -142,7 +177,14 @@ def main():
     ap.add_argument("--workload", default="dream7b")
     ap.add_argument("--prefix", type=int, default=640)
     ap.add_argument("--layer", type=int, default=10)
+    ap.add_argument("--prefill", action="store_true", help="record the prompt forward instead")
     args = ap.parse_args()
+    if args.prefill:
+        recs, shape, ms = record_prefill(args.workload)
+        print(f"prompt forward (recorded call, CUDA events around lopa_prefill): {ms:.3f} ms; "
+              f"{len(recs)} CTA records")
+        print(report(recs, shape.n_layers, min(args.layer, shape.n_layers - 1)))
+        return
     recs, shape, med = record(args.workload, args.prefix)
     print(f"verification forward (no recording): {med:.3f} ms median; {len(recs)} CTA records")
     print(report(recs, shape.n_layers, min(args.layer, shape.n_layers - 1)))
