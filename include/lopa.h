@@ -88,8 +88,9 @@ typedef struct {
  * pointers; the arrays themselves are copied at init and need not outlive the call.
  * lopa_init_model copies the projection matrices and lm_head into context-owned tile-major
  * copies (the layout the GEMMs stream; q, k and v are stacked into one matrix, gate and up
- * into another); the embedding and the norm gains stay borrowed and must outlive the
- * context.  The caller may free the projection matrices and lm_head after init. */
+ * into another) - bf16, or E4M3 codes plus per-row scales with LOPA_WEIGHTS_E4M3; the
+ * embedding and the norm gains stay borrowed and must outlive the context.  The caller may
+ * free the projection matrices and lm_head after init. */
 typedef struct {
   const void* embed;              /* [vocab][d_model] */
   const void* lm_head;            /* [vocab][d_model] */
@@ -142,7 +143,8 @@ typedef struct {
  * [L][max_seq][Hk][dh], V transposed as [L][Hk*dh][positions]), the per-branch Pre-Write
  * scratch, activations and state, precomputes RoPE tables and captures the iteration
  * into CUDA graphs.  stream: cudaStream_t to enqueue on (borrowed).  *out receives the
- * context.  Weight memory: about the size of the projection weights plus lm_head. */
+ * context.  Weight memory: about the size of the projection weights plus lm_head (half of it
+ * with LOPA_WEIGHTS_E4M3). */
 int lopa_init_model(const lopa_model_config* cfg, const lopa_weights* w,
                     const lopa_decode_config* dcfg, void* stream, lopa_ctx** out);
 
