@@ -25,8 +25,10 @@
 // flight per SM.  Roles in a CTA of 352 threads: warp 0 streams weights (before waiting
 // on the previous kernel, since weights never depend on it), warp 10 streams
 // activations, warp 1 allocates TMEM and issues the MMAs, warps 2..9 run the epilogue
-// (two warps per TMEM lane quarter, splitting the columns), staging output tiles in the
-// freed rings so global writes are whole-row 16-byte stores.  All waits are bounded.
+// (two warps per TMEM lane quarter, splitting the columns).  Split-K partials are stored
+// straight from the TMEM registers (a warp's lanes are 32 consecutive output features: one
+// 128-byte line per store); the SwiGLU output is staged in the freed rings so that its bf16
+// rows leave as 16-byte stores.  All waits are bounded.
 //
 // E4M3 weight stream (template flag F8): the weight TMA brings 8-bit codes (half the HBM
 // bytes) into a staging ring; eight converter warps widen each stage to bf16 in the
@@ -336,27 +338,6 @@ __global__ void __launch_bounds__(threads_of<MODE, F8>(), 1)
     // E4M3 stream: the scale of the weight row of this thread's TMEM lane in accumulator i
     // (weights on M); 1 for bf16 weights.
     auto row_scale = [&](int i) { return F8 ? __ldg(a.wscale + a_row[i] + r) : 1.0f; };
-    // Copies accumulator i to `stage` as fp32 [token][128 columns], two of this warp's
-    // 16-column chunks per TMEM wait.
-    auto stage_acc = [&](int i, float* stage) {
-      const float sc = row_scale(i);
-      for (int ci = half; ci < nchunk; ci += 4) {
-        float v[16], w[16];
-        if (ci + 2 < nchunk) {
-          tmem_ld16x2(lane_base + (uint32_t)(i * 256 + ci * 16),
-                      lane_base + (uint32_t)(i * 256 + ci * 16 + 32), v, w);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            stage[(ci * 16 + j) * 128 + r] = F8 ? v[j] * sc : v[j];
-            stage[(ci * 16 + 32 + j) * 128 + r] = F8 ? w[j] * sc : w[j];
-          }
-        } else {
-          tmem_ld16(lane_base + (uint32_t)(i * 256 + ci * 16), v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) stage[(ci * 16 + j) * 128 + r] = F8 ? v[j] * sc : v[j];
-        }
-      }
-    };
     // Every epilogue thread waits for the accumulator (bounded); the warp-wide TMEM reads
     // then follow one decision for all eight warps, taken after a barrier from the shared
     // abort flag (set by any wait of the CTA that gave up).
@@ -542,17 +523,21 @@ __global__ void __launch_bounds__(threads_of<MODE, F8>(), 1)
             }
             continue;
           }
-          stage_acc(i, stage);
-          epilogue_sync();
-          // This split's partial sums; the consumer adds the splits in a fixed order.
-          float* base = a.out_f32 + (size_t)blockIdx.y * a.split_stride + a_row[i];
-          for (int e = te; e < a.nbox * 32; e += kEpiWarps * 32) {
-            const int tt = e >> 5, c4 = (e & 31) * 4;
-            if (b_row + tt < a.T)
-              *reinterpret_cast<float4*>(base + (size_t)(b_row + tt) * a.ldo + c4) =
-                  *reinterpret_cast<const float4*>(stage + tt * 128 + c4);
+          // This split's partial sums, stored straight from the TMEM registers: a warp's
+          // lanes are 32 consecutive output features, so every store instruction writes one
+          // whole 128-byte line of a token's row.  The consumer adds the splits in a fixed
+          // order.
+          const float sc = row_scale(i);
+          float* base = a.out_f32 + (size_t)blockIdx.y * a.split_stride + a_row[i] + r;
+          for (int ci = half; ci < nchunk; ci += 2) {
+            float v[16];
+            tmem_ld16(lane_base + (uint32_t)(i * 256 + ci * 16), v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int t = b_row + ci * 16 + j;
+              if (t < a.T) base[(size_t)t * a.ldo] = F8 ? v[j] * sc : v[j];
+            }
           }
-          epilogue_sync();
         }
       } else if (MODE == GEMM_SWIGLU) {
         const float sg = row_scale(0), su = row_scale(1);
