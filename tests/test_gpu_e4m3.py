@@ -6,9 +6,10 @@ against the oracle's e4m3 weight mode.
 * The GEMM with E4M3 weights: every one of the 254 finite codes, through one-hot
   activations, comes back exactly (the on-chip widening to bf16, the swizzled layout and
   the per-row scale); random shapes against the oracle's float64 product.
-* The verification forward and whole decodes (step-local) on the tiny and small
-  workloads, and all 256 rows of the 7B layer slice, against the oracle with the same
-  quantised weights, under the bounds of the bf16 path.
+* The verification forward and whole decodes (step-local) on the tiny, small and heads128
+  (head_dim 128: the tensor-core attention) workloads, and all 256 rows of the 7B layer
+  slice, against the oracle with the same quantised weights, under the bounds of the bf16
+  path.
 """
 import numpy as np
 import pytest
@@ -95,7 +96,7 @@ def test_e4m3_gemm_matches_oracle(api, T, N, K):
     assert (err <= bound).all()
 
 
-@pytest.mark.parametrize("name", ["tiny", "small"])
+@pytest.mark.parametrize("name", ["tiny", "small", "heads128"])
 def test_verify_forward_e4m3_matches_oracle(name):
     shape, dshape, w = workload_weights(name)
     dec = make_decoder(name, weight_format="e4m3")
@@ -117,7 +118,7 @@ def test_verify_forward_e4m3_matches_oracle(name):
     assert nbad == 0
 
 
-@pytest.mark.parametrize("name", ["tiny", "small"])
+@pytest.mark.parametrize("name", ["tiny", "small", "heads128"])
 def test_decode_e4m3_step_local(name):
     shape, dshape, w = workload_weights(name)
     dec = make_decoder(name, weight_format="e4m3")
