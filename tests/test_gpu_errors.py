@@ -8,6 +8,7 @@
     head's pipeline waits give up; the kernel drains its own copies and MMAs, frees its
     tensor memory and returns, and lopa_kernel_status reports the timeout.  With the
     default limit restored the same call is correct again, so the context stays usable.
+    The same with the E4M3 weight stream's GEMM (its converter warps wait too).
 """
 import numpy as np
 import pytest
@@ -83,3 +84,36 @@ def test_short_wait_limit_reports_timeout_and_the_call_recovers(static):
     api.kernel_status()
     np.testing.assert_array_equal(am.cpu().numpy(), am_ref)
     np.testing.assert_array_equal(mp.cpu().numpy(), mp_ref)
+
+
+def test_short_wait_limit_in_the_e4m3_gemm_reports_timeout_and_recovers():
+    """The same for the E4M3 weight stream, whose converter warps add their own bounded
+    waits (staging ring of codes, converted slots): a wait that gives up stops the kernel
+    cleanly (the codes' copies and the MMAs it started are drained) and is reported; the
+    next call with the default limit is correct."""
+    from diffusion_lookahead_decoding_gb300 import api
+    from oracle import lopa_oracle as O
+    build_lib()
+    T, N, K = 256, 3584, 18944
+    g = torch.Generator().manual_seed(17)
+    x = torch.randn(T, K, generator=g).to(torch.bfloat16).cuda()
+    w = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16).cuda()
+    codes, scales = api.quantize_e4m3(w)
+    api.kernel_status()
+    try:
+        api.set_wait_limit_ns(100)
+        y = torch.zeros(T, N, dtype=torch.float32, device="cuda")
+        api.linear_accumulate_e4m3(x, codes, scales, y)
+        with pytest.raises(L.LopaError) as e:
+            api.kernel_status()
+        assert e.value.code == L.ERR_DEVICE_TIMEOUT
+    finally:
+        api.set_wait_limit_ns(0)
+    api.kernel_status()
+    y = torch.zeros(T, N, dtype=torch.float32, device="cuda")
+    api.linear_accumulate_e4m3(x, codes, scales, y)
+    api.kernel_status()
+    c_ref, s_ref = O.quantize_e4m3_rows(w.cpu().to(torch.float64).numpy())
+    xd, wq = x.cpu().to(torch.float64).numpy(), c_ref * s_ref[:, None]
+    err = np.abs(y.cpu().numpy() - O.linear(xd, wq))
+    assert (err <= 1e-4 * (np.abs(xd) @ np.abs(wq).T) + 1e-6).all()
