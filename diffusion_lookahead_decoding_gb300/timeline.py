@@ -10,6 +10,7 @@ dependent launch; a profiler that serialises them cannot show this.
 
     python -m diffusion_lookahead_decoding_gb300.timeline [--workload dream7b] [--prefix 640]
     python -m diffusion_lookahead_decoding_gb300.timeline --prefill   # the prompt forward
+    python -m diffusion_lookahead_decoding_gb300.timeline --decode    # idle gaps of a decode
 """
 from __future__ import annotations
 
@@ -88,6 +89,50 @@ def record_prefill(workload: str):
     recs = _records(buf)
     dec.close()
     return recs, shape, e0.elapsed_time(e1)
+
+
+def record_decode(workload: str):
+    """Records one whole decode (after a warm-up decode); returns the records, the shape and
+    the CUDA-event time of the decode in ms."""
+    import torch
+    from . import _lib as L, api, synth
+    lib = L.load(build_timeline_lib())
+    lib.lopa_timeline_set_buffer.argtypes = [C.c_void_p]
+    lib.lopa_timeline_set_buffer.restype = C.c_int
+    shape, dshape = synth.WORKLOADS[workload]
+    dw = api.upload_weights(shape, synth.make_weights(shape, 0))
+    P0, Bk = dshape.prompt_len, dshape.block
+    dec = api.LopaDecoder(shape, dw, Bk, dshape.k, dshape.tau, P0, P0 + dshape.gen_len)
+    dec.prefill(synth.make_prompt(shape, P0, seed=1))
+    dec.decode(dshape.gen_len)
+    dec.rewind(P0)
+    cap = 2000000
+    buf = torch.zeros(4 + cap * 10, dtype=torch.int32, device="cuda")
+    buf[1] = cap
+    torch.cuda.synchronize()
+    if lib.lopa_timeline_set_buffer(C.c_void_p(buf.data_ptr())) != 0:
+        raise RuntimeError("timeline buffer")
+    _, st = dec.decode(dshape.gen_len)
+    torch.cuda.synchronize()
+    lib.lopa_timeline_set_buffer(None)
+    recs = _records(buf)
+    dec.close()
+    return recs, shape, st["seconds"] * 1e3
+
+
+def gaps(recs, min_ns: int = 2000):
+    """Intervals in which no CTA of any kernel was resident: (total busy span, idle time in
+    gaps of at least min_ns, the number of such gaps)."""
+    iv = recs[np.argsort(recs[:, 1])][:, [1, 3]]
+    idle, n, end = 0, 0, iv[0, 1]
+    for t0, t1 in iv[1:]:
+        if t0 > end:
+            g = t0 - end
+            if g >= min_ns:
+                idle += g
+                n += 1
+        end = max(end, t1)
+    return int(iv[:, 1].max() - iv[0, 0]), int(idle), n
 
 
 def record(workload: str, prefix: int, forwards: int = 2):
@@ -178,7 +223,15 @@ def main():
     ap.add_argument("--prefix", type=int, default=640)
     ap.add_argument("--layer", type=int, default=10)
     ap.add_argument("--prefill", action="store_true", help="record the prompt forward instead")
+    ap.add_argument("--decode", action="store_true", help="record a whole decode: idle gaps")
     args = ap.parse_args()
+    if args.decode:
+        recs, shape, ms = record_decode(args.workload)
+        span, idle, n = gaps(recs)
+        print(f"decode: {ms:.3f} ms (CUDA events), {len(recs)} CTA records, GPU span "
+              f"{span / 1e6:.3f} ms, idle {idle / 1e6:.3f} ms in {n} gaps of >= 2 us "
+              f"({100.0 * idle / span:.1f} % of the span)")
+        return
     if args.prefill:
         recs, shape, ms = record_prefill(args.workload)
         print(f"prompt forward (recorded call, CUDA events around lopa_prefill): {ms:.3f} ms; "
