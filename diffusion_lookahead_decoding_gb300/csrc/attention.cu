@@ -26,7 +26,11 @@
 // (two MMAs keep P's fp32 accuracy), write it over S, and rescale O in TMEM only when a
 // row's running maximum grows by more than 2^8 (the result is unchanged: O and the
 // normaliser share the same reference).  Shared memory holds only the K / V^T ring.
-// Eight softmax warps: two per TMEM lane quarter, each on half of the 128 keys.
+// Eight softmax warps: two per TMEM lane quarter, each on half of the 128 keys.  A row
+// tile's CTA walks its key tiles in sequence, so with a long prefix (8 or more key tiles)
+// the two CTAs of a cluster pair split the tiles and rank 0 merges the two softmax states
+// (reference maximum, sum, O) through distributed shared memory; pairs are launched only
+// when a prefix can reach that length and the pairs fit the SMs in one wave.
 // head_dim 32 and 64 run on bf16 mma.sync with the same layouts.
 #include <cstring>
 
@@ -105,6 +109,13 @@ constexpr uint32_t kTcOffTail = kTcStages * kTcStageBytes;
 // fp32 columns, overwritten in place by P); O (fp32) [384, 512).
 constexpr uint32_t kTmQ = 0, kTmS = 128, kTmO = 384, kTmCols = 512;
 constexpr float kLazyRescale = 8.0f;  // log2 units
+// Split keys: a CTA pair (cluster of 2 along z) shares a row tile; when the prefix spans at
+// least this many key tiles, rank 0 takes the first half of the tiles and rank 1 the rest,
+// and rank 0 merges the two softmax states through distributed shared memory.
+constexpr int kSplitMinTiles = 8;
+// Merge stash (in the freed K / V^T ring): O as [128 columns][128 rows] fp32, then the
+// rows' reference maxima and sums.
+constexpr int kExM = 128 * kTcRows, kExL = kExM + kTcRows;
 
 struct TcTail {
   uint64_t qfull;
@@ -214,6 +225,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int R0 = blockIdx.x * kTcRows;
   const int b_lo = (R0 / G) / a.Bq;
   const int b_hi = (min(R0 + kTcRows, rows) - 1) / G / a.Bq;
+  // The key schedule depends on the committed prefix length *dP only, which kernels of
+  // earlier, completed launches wrote, so it is read before the wait on the previous kernel.
+  // Key tiles [j0, j0 + nl) of this CTA (both CTAs of a pair compute the same `split`); the
+  // second CTA of a pair has nothing to do unless the keys are split and leaves at once.
+  const KeySched ks = key_sched<kTcKeys>(a, b_lo, b_hi);
+  const int n = ks.n_pre + ks.n_br;
+  const int rank = gridDim.z > 1 ? (int)blockIdx.z : 0;
+  const bool split = gridDim.z > 1 && ks.n_pre >= kSplitMinTiles;
+  const int hsplit = split ? min(ks.n_pre, n / 2) : n;
+  const int j0 = (split && rank == 1) ? hsplit : 0;
+  const int nl = split ? (rank == 0 ? hsplit : n - hsplit) : (rank == 0 ? n : 0);
+  if (rank == 1 && nl == 0) {
+    pdl_trigger();
+    TL_END(tl::ATTN_TC);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&tail->qfull), kTcSoftWarps * 32);
@@ -249,18 +276,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   pdl_trigger();
   pdl_wait();  // q and the block keys come from the previous kernel; out may be read by it
   TL_WAITED();
-  const KeySched ks = key_sched<kTcKeys>(a, b_lo, b_hi);
-  const int n = ks.n_pre + ks.n_br;
   const uint64_t lim = wait_limit(a.wait_ns);
 
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t keep = policy_evict_last();
       int issued = 0;
-      for (int j = 0; j < n; ++j) {
-        const int s = j % kTcStages;
-        if (j >= kTcStages &&
-            !mbar_wait_bounded(smem_u32(&tail->kvempty[s]), (uint32_t)(j / kTcStages - 1) & 1u,
+      for (int jl = 0; jl < nl; ++jl) {
+        const int j = j0 + jl;  // key tile; ring slots and phases count local tiles
+        const int s = jl % kTcStages;
+        if (jl >= kTcStages &&
+            !mbar_wait_bounded(smem_u32(&tail->kvempty[s]), (uint32_t)(jl / kTcStages - 1) & 1u,
                                abort, a.err, DEV_TIMEOUT_PRODUCER, lim))
           break;
         const uint32_t fb = smem_u32(&tail->kvfull[s]);
@@ -304,12 +330,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         mma_commit(smem_u32(&tail->sfull[sb]));
       };
-      if (ok && n > 0) {
+      if (ok && nl > 0) {
         tc_fence_after();
         issue_s(0);
       }
-      for (int i = 0; ok && i < n; ++i) {
-        if (i + 1 < n) issue_s(i + 1);
+      for (int i = 0; ok && i < nl; ++i) {
+        if (i + 1 < nl) issue_s(i + 1);
         const int pb = i & 1, si = i % kTcStages;
         ok = ok && mbar_wait_bounded(smem_u32(&tail->pfull[pb]), (uint32_t)(i >> 1) & 1u, abort,
                                      a.err, DEV_TIMEOUT_MMA, lim);
@@ -378,10 +404,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ok = ok && __all_sync(kAll, mbar_wait_bounded(smem_u32(bar), parity, abort, a.err,
                                                     DEV_TIMEOUT_EPILOGUE, lim));
     };
-    for (int j = 0; j < n; ++j) {
-      const int sb = j & 1;
+    for (int jl = 0; jl < nl; ++jl) {
+      const int j = j0 + jl;  // key tile (masks); buffers and phases count local tiles
+      const int sb = jl & 1;
       const uint32_t s_col = lane_base + kTmS + 128u * sb + (uint32_t)(h * 64);
-      wait_all(&tail->sfull[sb], (uint32_t)(j >> 1) & 1u);
+      wait_all(&tail->sfull[sb], (uint32_t)(jl >> 1) & 1u);
       float sv[64];
       if (ok) {
         tc_fence_after();
@@ -419,10 +446,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // P_0..P_{j-1} V relative to the old reference and is rescaled once P_{j-1} V has
       // landed; the warp rescales together, rows that keep their reference with alpha = 1.
       const bool need = mx > m_ref + kLazyRescale;
-      const bool need_o = need && m_ref != -INFINITY;  // only for j >= 1
+      const bool need_o = need && m_ref != -INFINITY;  // only for jl >= 1
       const float alpha = need_o ? exp2f(m_ref - mx) : 1.f;
       if (ok && __any_sync(kAll, need_o)) {
-        wait_all(&tail->pempty[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u);
+        wait_all(&tail->pempty[(jl - 1) & 1], (uint32_t)((jl - 1) >> 1) & 1u);
         if (ok) {
           tc_fence_after();
 #pragma unroll
@@ -475,7 +502,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     // Epilogue: out row = O / l in bf16 (a row that saw no key is written as zeros); l is
     // the sum of the two half-row sums, which share the row's reference maximum.
-    const bool got = ok && n > 0 &&
+    const bool got = ok && nl > 0 &&
                      mbar_wait_bounded(smem_u32(&tail->odone), 0, abort, a.err, DEV_TIMEOUT_EPILOGUE,
                                        lim);
     const bool have_o = __all_sync(kAll, got);
@@ -483,10 +510,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tail->xsum[h][r] = l;
     pair_sync();
     const float lt = l + tail->xsum[h ^ 1][r];
+    if (split) {
+      // Stash this CTA's softmax state for the merge after the role branches: O (relative to
+      // the row's reference maximum m_ref) as ex[column][row] fp32, then m_ref and the row sum.
+      // The K / V^T ring is free: every MMA has completed (odone).
+      float* ex = reinterpret_cast<float*>(smem);
+#pragma unroll
+      for (int c = 0; c < 64; c += 32) {
+        float u[16], w[16];
+        if (have_o) {
+          tmem_ld16x2(o_base + c, o_base + c + 16, u, w);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) u[e] = w[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          ex[(h * 64 + c + e) * kTcRows + r] = u[e];
+          ex[(h * 64 + c + 16 + e) * kTcRows + r] = w[e];
+        }
+      }
+      if (h == 0) {
+        ex[kExM + r] = have_o ? m_ref : -INFINITY;
+        ex[kExL + r] = have_o ? lt : 0.f;
+      }
+    }
     const float inv = lt > 0.f ? 1.0f / lt : 0.f;
     bf16* orow = a.out + ((size_t)t * a.H + g * G + hg) * 128 + h * 64;
 #pragma unroll
-    for (int c = 0; c < 64; c += 32) {
+    for (int c = 0; c < 64 && !split && rank == 0; c += 32) {
       float u[16], w[16];
       if (have_o) {
         tmem_ld16x2(o_base + c, o_base + c + 16, u, w);
@@ -508,6 +560,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int e = 0; e < 4; ++e) reinterpret_cast<uint4*>(orow + c)[e] = o4[e];
       }
     }
+  }
+  if (split) {
+    // Both CTAs of the pair have stashed their state (every wait before this point is
+    // bounded, so both arrive); rank 0 merges the two halves of the keys and writes the
+    // output; the second barrier keeps rank 1's shared memory alive until it is read.
+    cluster_arrive_release();
+    cluster_wait();
+    if (rank == 0 && warp >= 2) {
+      const int q = warp & 3, h = (warp - 2) >> 2;
+      const int r = q * 32 + lane;
+      const int R = R0 + r;
+      if (R < rows) {
+        const int t = R / G, hg = R - t * G;
+        const float* mine = reinterpret_cast<const float*>(smem);
+        const uint32_t peer = mapa_shared(smem_u32(smem), 1u);
+        const float m0 = mine[kExM + r], l0 = mine[kExL + r];
+        const float m1 = ld_dsmem_f32(peer + 4u * (uint32_t)(kExM + r));
+        const float l1 = ld_dsmem_f32(peer + 4u * (uint32_t)(kExL + r));
+        const float mm = fmaxf(m0, m1);
+        const float a0 = m0 == -INFINITY ? 0.f : exp2f(m0 - mm);
+        const float a1 = m1 == -INFINITY ? 0.f : exp2f(m1 - mm);
+        const float lt = l0 * a0 + l1 * a1;
+        const float inv = lt > 0.f ? 1.0f / lt : 0.f;
+        bf16* orow = a.out + ((size_t)t * a.H + g * G + hg) * 128 + h * 64;
+#pragma unroll 2
+        for (int c = 0; c < 64; c += 8) {
+          float o[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int idx = (h * 64 + c + e) * kTcRows + r;
+            o[e] = (mine[idx] * a0 + ld_dsmem_f32(peer + 4u * (uint32_t)idx) * a1) * inv;
+          }
+          uint4 o4;
+          uint32_t* ow = reinterpret_cast<uint32_t*>(&o4);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 v = __floats2bfloat162_rn(o[2 * e], o[2 * e + 1]);
+            ow[e] = *reinterpret_cast<const uint32_t*>(&v);
+          }
+          *reinterpret_cast<uint4*>(orow + c) = o4;
+        }
+      }
+    }
+    cluster_arrive_release();
+    cluster_wait();
   }
   tc_fence_before();
   __syncthreads();
@@ -876,7 +973,19 @@ const char* plan_attention(AttnLaunch* L, const AttnArgs& a, int dh, int kc_rows
                       a.Bk > 0 ? (uint64_t)a.Hk * 128 : T, a.Bk > 0 ? kbr : 128, 128, err,
                       sizeof(err), a.Bk > 0 ? (uint64_t)a.ldvb : 0))
     return err;
-  L->grid = dim3((T * G + kTcRows - 1) / kTcRows, a.Hk, 1);
+  // z: the CTA pair of a row tile, when a prefix can reach the split threshold (kc_rows is
+  // the most prefix keys the launch can see) and the pairs fit the SMs in one wave
+  // (otherwise the row tiles alone fill the GPU and the keys are not split).
+  const unsigned tiles = (unsigned)((T * G + kTcRows - 1) / kTcRows) * (unsigned)a.Hk;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    sms = 0;
+  }
+  const bool may_split = (max(kc_rows, a.pk_add) + kTcKeys - 1) / kTcKeys >= kSplitMinTiles;
+  L->grid = dim3((T * G + kTcRows - 1) / kTcRows, a.Hk,
+                 may_split && 2 * tiles <= (unsigned)sms ? 2 : 1);
   return "";
 }
 
@@ -889,7 +998,8 @@ cudaError_t launch_attention(const AttnLaunch& L, cudaStream_t s) {
     case 128: {
       TcMaps m;
       memcpy(&m, L.maps, sizeof(m));
-      return launch_pdl(attn_tc_kernel, L.grid, dim3(kTcThreads), kTcSmem, s, m, L.args);
+      return launch_pdl_cluster(attn_tc_kernel, L.grid, dim3(kTcThreads), kTcSmem, s,
+                                dim3(1, 1, L.grid.z), m, L.args);
     }
     default:
       return cudaErrorInvalidValue;

@@ -381,3 +381,35 @@ def test_prompt_of_2048_tokens_matches_oracle():
     print(summ.table_row("small, prompt 2048, first 3 iterations"))
     assert summ.n == 3
     dec.close()
+
+
+def test_long_prefix_splits_the_keys_over_a_cta_pair():
+    """head_dim 128 with a committed prefix of 9+ key tiles: the tensor-core attention splits
+    the prefix keys over the two CTAs of a pair and merges their softmax states through
+    distributed shared memory.  A 1100-token prompt on the heads128 model, then a
+    verification forward and the first LoPA iterations against the oracle, the first of
+    them on a prefix of 9 tiles, step by step."""
+    import copy
+    import dataclasses
+    from diffusion_lookahead_decoding_gb300 import api
+    shape, dshape, w = workload_weights("heads128")
+    P, B = 1100, dshape.block
+    ds = dataclasses.replace(dshape, prompt_len=P, gen_len=2 * B)
+    dec = api.LopaDecoder(shape, device_weights("heads128"), B, dshape.k, dshape.tau, P, P + 2 * B)
+    prompt = synth.make_prompt(shape, P, seed=4)
+    dec.prefill(prompt)
+    m = O.OracleModel(shape, w, act="bf16")
+    cache = O.prefill(m, prompt, P + 2 * B)
+    br = seeded_branches(shape, dshape.k + 1, B, seed=11)
+    am, mp, hid = dec.verify_forward(br, want_hidden=True)
+    out = O.forward(m, cache, P, br, want_logits=True)
+    e_h = rel_l2(hid, out.x_final)
+    nflip, nbad = token_flips(am, mp, out, shape.mask_id, hid, shape, w)
+    print(f"heads128, prefix {P}: hidden relL2 {e_h:.2e}, maxp max|d| "
+          f"{np.abs(mp - out.mp).max():.2e}, flips {nflip} (beyond window {nbad})")
+    assert e_h <= HIDDEN_REL_L2 and nbad == 0
+    summ = steplocal.run(dec, m, shape, ds, prompt, dshape.k, max_steps=3,
+                         oracle_prompt_cache=copy.deepcopy(cache))
+    print(summ.table_row(f"heads128, prefix {P}, first 3 iterations"))
+    assert summ.n == 3
+    dec.close()
