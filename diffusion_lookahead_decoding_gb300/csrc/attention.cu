@@ -27,7 +27,7 @@
 // row's running maximum grows by more than 2^8 (the result is unchanged: O and the
 // normaliser share the same reference).  Shared memory holds only the K / V^T ring.
 // Eight softmax warps: two per TMEM lane quarter, each on half of the 128 keys.  A row
-// tile's CTA walks its key tiles in sequence, so with a long prefix (8 or more key tiles)
+// tile's CTA walks its key tiles in sequence, so with a prefix of 4 or more key tiles
 // the two CTAs of a cluster pair split the tiles and rank 0 merges the two softmax states
 // (reference maximum, sum, O) through distributed shared memory; pairs are launched only
 // when a prefix can reach that length and the pairs fit the SMs in one wave.
@@ -110,9 +110,9 @@ constexpr uint32_t kTcOffTail = kTcStages * kTcStageBytes;
 constexpr uint32_t kTmQ = 0, kTmS = 128, kTmO = 384, kTmCols = 512;
 constexpr float kLazyRescale = 8.0f;  // log2 units
 // Split keys: a CTA pair (cluster of 2 along z) shares a row tile; when the prefix spans at
-// least this many key tiles, rank 0 takes the first half of the tiles and rank 1 the rest,
+// least this many key tiles (512 keys), rank 0 takes the first half of the tiles and rank 1 the rest,
 // and rank 0 merges the two softmax states through distributed shared memory.
-constexpr int kSplitMinTiles = 8;
+constexpr int kSplitMinTiles = 4;
 // Merge stash (in the freed K / V^T ring): O as [128 columns][128 rows] fp32, then the
 // rows' reference maxima and sums.
 constexpr int kExM = 128 * kTcRows, kExL = kExM + kTcRows;

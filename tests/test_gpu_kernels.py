@@ -61,7 +61,7 @@ def test_lmhead_argmax_matches_oracle(rows, d, V, mask):
     (1, 16, 0, 4, 4, 32), (4, 16, 32, 4, 4, 32), (5, 32, 256, 16, 4, 64),
     (8, 32, 100, 28, 4, 128), (8, 32, 1024, 28, 4, 128), (2, 64, 4096, 28, 4, 128),
     (16, 16, 257, 16, 4, 64), (1, 512, 0, 28, 4, 128),
-    # head_dim 128 with the keys split over a CTA pair (prefix of 8 or more key tiles): an odd
+    # head_dim 128 with the keys split over a CTA pair (prefix of 4 or more key tiles): an odd
     # tile count with a ragged last prefix tile, and a long ragged prefix
     (3, 32, 1100, 28, 4, 128), (8, 32, 2000, 28, 4, 128)])
 def test_branch_attention_matches_oracle(nb, B, P, H, Hk, dh):
