@@ -92,12 +92,16 @@ __global__ void __launch_bounds__(512, 2)
   __shared__ float red[32];
   TL_DECL;
   TL_START();
-  pdl_wait();
-  TL_WAITED();
-  pdl_trigger();
   const int t = blockIdx.x;
   const int c = threadIdx.x * 8;
   const bool active = c < d;
+  // The norm weight is a constant of the model: loaded before the wait on the producer of
+  // the partials, so its latency is off the critical path.
+  float gg[8];
+  if (active) load8(g + c, gg);
+  pdl_wait();
+  TL_WAITED();
+  pdl_trigger();
   float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
   if (active) {
     float* xr = x + (size_t)t * d + c;
@@ -128,8 +132,7 @@ __global__ void __launch_bounds__(512, 2)
   ss = block_sum(ss, red);  // also a barrier: every thread has read its partials
   const float rs = rsqrtf(ss / (float)d + eps);
   if (active) {
-    float gg[8], f[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    load8(g + c, gg);
+    float f[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) f[i] = f[i] * rs * gg[i];
     store8(n + (size_t)t * d + c, f);
