@@ -201,6 +201,18 @@ def linear_accumulate(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor):
     return y
 
 
+def swiglu(x: torch.Tensor, w: torch.Tensor, h: torch.Tensor = None):
+    """h = bf16(silu(x @ w[:F].T) * (x @ w[F:].T))  (x [T,K] bf16, w [2F,K] bf16 with the gate
+    rows first, h [T,F] bf16; all contiguous on cuda)."""
+    T, K = x.shape
+    F = w.shape[0] // 2
+    if h is None:
+        h = torch.empty((T, F), dtype=torch.bfloat16, device=x.device)
+    assert h.shape == (T, F) and h.dtype == torch.bfloat16 and w.shape == (2 * F, K)
+    L.check(L.load().lopa_swiglu(x.data_ptr(), w.data_ptr(), h.data_ptr(), T, F, K, _stream_ptr()))
+    return h
+
+
 def quantize_e4m3(w: torch.Tensor):
     """Per-row E4M3 codes [N,K] (uint8) and float32 scales [N] of a bf16 weight [N,K]."""
     N, K = w.shape

@@ -1060,6 +1060,29 @@ int lopa_linear_accumulate(const void* x, const void* w, float* y, int T, int N,
   return 0;
 }
 
+int lopa_swiglu(const void* x, const void* w, void* h, int T, int F, int K, void* stream) {
+  lopa_ctx* ctx = nullptr;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(h))
+    return fail(ctx, LOPA_ERR_INVALID_ARG, "null or unaligned pointer");
+  if (T < 1 || F < 128 || F % 128 || K < 64 || K % 64)
+    return fail(ctx, LOPA_ERR_UNSUPPORTED, "need T >= 1, F % 128 == 0, K % 64 == 0");
+  CK(gemm_set_smem_limits());
+  int dev = 0, sms = 0;
+  CK(cudaGetDevice(&dev));
+  CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  GemmLaunch G;
+  const char* e = plan_gemm(&G, GEMM_SWIGLU, x, T, T, w, 2 * F, K, 2, 1, std::min(256, round16(T)), sms);
+  if (e[0]) return fail(ctx, LOPA_ERR_UNSUPPORTED, "%s", e);
+  G.args.out_bf16 = static_cast<bf16*>(h);
+  G.args.ldh = F;
+  cudaError_t se = cudaSuccess;
+  G.args.err = call_status_word(&se);
+  CK(se);
+  G.args.wait_ns = call_wait_limit_ns();
+  CK(launch_gemm(G, static_cast<cudaStream_t>(stream)));
+  return 0;
+}
+
 int lopa_quantize_e4m3(const void* w, int rows, int K, uint8_t* codes, float* scales, void* stream) {
   lopa_ctx* ctx = nullptr;
   if (!aligned16(w) || !aligned16(codes) || !scales) return fail(ctx, LOPA_ERR_INVALID_ARG, "null or unaligned pointer");

@@ -240,6 +240,16 @@ int lopa_set_wait_limit_ns(unsigned long long ns);
 int lopa_linear_accumulate(const void* x, const void* w, float* y, int T, int N, int K,
                            void* stream);
 
+/* Gate/up projection with the SwiGLU activation, the first half of the MLP of every layer
+ * of the verification forward (Dream-7B follows the Qwen2.5 architecture; the branch rows
+ * of all branches share one matmul: "Decoding-efficiency revolution" blog, section 3.3):
+ *   h[t][f] = bf16( silu(g) * u ),  g = x[t] . w[f],  u = x[t] . w[F + f],
+ *   silu(g) = g / (1 + exp(-g)), sums in fp32 on the tcgen05 tensor cores.
+ * x [T][K] bf16, w [2F][K] bf16 (the F gate rows, then the F up rows; row-major),
+ * h [T][F] bf16 (written); all device pointers, 16-byte aligned.  T >= 1, F a multiple of
+ * 128, K a multiple of 64. */
+int lopa_swiglu(const void* x, const void* w, void* h, int T, int F, int K, void* stream);
+
 /* Per-row E4M3 quantisation as lopa_init_model does it for LOPA_WEIGHTS_E4M3:
  * w [rows][K] bf16 (device, 16-byte aligned), K a multiple of 64 -> codes [rows][K] bytes
  * (device, 16-byte aligned), scales [rows] float32 (device).  The weight row r is then

@@ -66,6 +66,8 @@ def test_host_side_argument_errors_without_gpu(lib):
     dc.k, dc.max_prompt = 3, 200  # prompt + block beyond max_seq
     assert lib.lopa_init_model(C.byref(mc), C.byref(w), C.byref(dc), None, C.byref(out)) == L.ERR_INVALID_ARG
     assert lib.lopa_linear_accumulate(None, None, None, 1, 128, 64, None) == L.ERR_INVALID_ARG
+    assert lib.lopa_swiglu(None, None, None, 1, 128, 64, None) == L.ERR_INVALID_ARG
+    assert lib.lopa_swiglu(4096, 4096, 4096, 1, 100, 64, None) == L.ERR_UNSUPPORTED  # F % 128
     assert lib.lopa_linear_accumulate_e4m3(None, None, None, None, 1, 128, 64, None) == L.ERR_INVALID_ARG
     assert lib.lopa_quantize_e4m3(None, 1, 64, None, None, None) == L.ERR_INVALID_ARG
     assert lib.lopa_quantize_e4m3(4096, 1, 60, 4096, 4096, None) == L.ERR_INVALID_ARG  # K % 64

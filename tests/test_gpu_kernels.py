@@ -24,7 +24,7 @@ def _bf16(shape, seed, scale=1.0):
 
 @pytest.mark.parametrize("T,N,K", [(64, 384, 128), (160, 1536, 1024), (256, 4608, 512),
                                    (37, 256, 64), (300, 384, 192), (1, 128, 64),
-                                   (256, 3584, 3584)])
+                                   (256, 3584, 3584), (256, 3584, 18944), (77, 384, 18944)])
 def test_linear_accumulate_matches_oracle(T, N, K):
     from diffusion_lookahead_decoding_gb300 import api
     x = _bf16((T, K), 1)
@@ -38,6 +38,40 @@ def test_linear_accumulate_matches_oracle(T, N, K):
     bound = 1e-4 * (np.abs(xd) @ np.abs(wd).T) + 1e-6 * np.abs(y0.double().numpy()) + 1e-6
     err = np.abs(got - ref)
     assert (err <= bound).all(), f"max err {err.max()} (bound {bound[err > bound][:3]})"
+
+
+@pytest.mark.parametrize("T,F,K", [(64, 128, 128), (37, 256, 64), (300, 384, 192), (1, 128, 1024),
+                                   (160, 1536, 1024), (256, 18944, 3584)])
+def test_swiglu_matches_oracle(T, F, K):
+    """Gate/up GEMM with the SwiGLU epilogue (the last case is the 7B layer's, 256 rows)
+    against the oracle's silu(x Wg^T) * (x Wu^T) rounded to bf16."""
+    from diffusion_lookahead_decoding_gb300 import api
+    x = _bf16((T, K), 11)
+    w = _bf16((2 * F, K), 12, 0.02)
+    h = api.swiglu(x.cuda(), w.cuda())
+    api.kernel_status()
+    got = h.cpu().double().numpy()
+    xd, wd = x.double().numpy(), w.double().numpy()
+    g, u = O.linear(xd, wd[:F]), O.linear(xd, wd[F:])
+    ref = O.silu(g) * u
+    # fp32 sums (within 1e-4 of the absolute sum, as above), then one bf16 rounding
+    eg = 1e-4 * (np.abs(xd) @ np.abs(wd[:F]).T) + 1e-6
+    eu = 1e-4 * (np.abs(xd) @ np.abs(wd[F:]).T) + 1e-6
+    bound = 2.0 ** -8 * np.abs(ref) + 1.1 * np.abs(u) * eg + np.abs(O.silu(g)) * eu + 1e-6
+    err = np.abs(got - ref)
+    assert (err <= bound).all(), f"max err {err.max()}"
+    # The oracle's bf16 value exactly, except where the fp32 sums land on the other side of a
+    # rounding boundary: then one bf16 step apart.  Checked where |ref| >= 1e-2, so that the
+    # bf16 step (>= 2^-14) is far above the fp32 error of the sums (a few 1e-6); a wrong
+    # formula (no silu, gate and up swapped) disagrees almost everywhere.
+    exact = O.bf16_round(ref)
+    big = np.abs(ref) >= 1e-2
+    diff = (got != exact) & big
+    step = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+    print(f"T={T} F={F} K={K}: {int(diff.sum())} of {int(big.sum())} outputs one bf16 step from "
+          f"the oracle's rounding")
+    assert diff.sum() <= 1e-2 * big.sum()
+    assert (np.abs(got - exact)[diff] <= step[diff] * 1.0001).all()
 
 
 @pytest.mark.parametrize("rows,d,V,mask", [(64, 128, 1024, 0), (160, 1024, 32768, 0),
