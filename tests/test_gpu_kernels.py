@@ -96,8 +96,10 @@ def test_lmhead_argmax_matches_oracle(rows, d, V, mask):
     (8, 32, 100, 28, 4, 128), (8, 32, 1024, 28, 4, 128), (2, 64, 4096, 28, 4, 128),
     (16, 16, 257, 16, 4, 64), (1, 512, 0, 28, 4, 128),
     # head_dim 128 with the keys split over a CTA pair (prefix of 4 or more key tiles): an odd
-    # tile count with a ragged last prefix tile, and a long ragged prefix
-    (3, 32, 1100, 28, 4, 128), (8, 32, 2000, 28, 4, 128)])
+    # tile count with a ragged last prefix tile, and a long ragged prefix; the threshold
+    # itself (4 tiles), the 7B step's prefix (5 tiles), and just below it (3 tiles, one CTA)
+    (3, 32, 1100, 28, 4, 128), (8, 32, 2000, 28, 4, 128), (8, 32, 512, 28, 4, 128),
+    (8, 32, 640, 28, 4, 128), (8, 32, 383, 28, 4, 128)])
 def test_branch_attention_matches_oracle(nb, B, P, H, Hk, dh):
     from diffusion_lookahead_decoding_gb300 import api
     q, kp, vp, kb, vb = synth.make_attention_inputs(nb, B, P, H, Hk, dh, seed=7)
