@@ -8,7 +8,8 @@
     head's pipeline waits give up; the kernel drains its own copies and MMAs, frees its
     tensor memory and returns, and lopa_kernel_status reports the timeout.  With the
     default limit restored the same call is correct again, so the context stays usable.
-    The same with the E4M3 weight stream's GEMM (its converter warps wait too).
+    The same with the E4M3 weight stream's GEMM (its converter warps wait too) and the
+    gate/up GEMM with its SwiGLU epilogue.
 """
 import numpy as np
 import pytest
@@ -117,3 +118,34 @@ def test_short_wait_limit_in_the_e4m3_gemm_reports_timeout_and_recovers():
     xd, wq = x.cpu().to(torch.float64).numpy(), c_ref * s_ref[:, None]
     err = np.abs(y.cpu().numpy() - O.linear(xd, wq))
     assert (err <= 1e-4 * (np.abs(xd) @ np.abs(wq).T) + 1e-6).all()
+
+
+def test_short_wait_limit_in_the_swiglu_gemm_reports_timeout_and_recovers():
+    """The same for the gate/up GEMM with its SwiGLU epilogue (`lopa_swiglu`): a wait that
+    gives up is reported, and the next call with the default limit matches the oracle."""
+    from diffusion_lookahead_decoding_gb300 import api
+    from oracle import lopa_oracle as O
+    build_lib()
+    T, F, K = 256, 1536, 3584
+    g = torch.Generator().manual_seed(19)
+    x = torch.randn(T, K, generator=g).to(torch.bfloat16).cuda()
+    w = (torch.randn(2 * F, K, generator=g) * 0.02).to(torch.bfloat16).cuda()
+    api.kernel_status()
+    try:
+        api.set_wait_limit_ns(100)
+        api.swiglu(x, w)
+        with pytest.raises(L.LopaError) as e:
+            api.kernel_status()
+        assert e.value.code == L.ERR_DEVICE_TIMEOUT
+    finally:
+        api.set_wait_limit_ns(0)
+    api.kernel_status()
+    h = api.swiglu(x, w)
+    api.kernel_status()
+    xd, wd = x.cpu().to(torch.float64).numpy(), w.cpu().to(torch.float64).numpy()
+    g_, u = O.linear(xd, wd[:F]), O.linear(xd, wd[F:])
+    ref = O.silu(g_) * u
+    eg = 1e-4 * (np.abs(xd) @ np.abs(wd[:F]).T) + 1e-6
+    eu = 1e-4 * (np.abs(xd) @ np.abs(wd[F:]).T) + 1e-6
+    bound = 2.0 ** -8 * np.abs(ref) + 1.1 * np.abs(u) * eg + np.abs(O.silu(g_)) * eu + 1e-6
+    assert (np.abs(h.cpu().to(torch.float64).numpy() - ref) <= bound).all()
